@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the paged multi-token attention step on GB300.
+
+One step = the whole hot path over one unified batch: paged KV append of the
+batch's new tokens, host planning, the split-KV and tensor-core attention
+kernels, the log-sum-exp merge, and a swap-out of one conversation's blocks to
+pinned host memory on a side stream (the CPU cache tier), joined at the end.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  `value` is query tokens per second of the
+whole job with inputs resident in HBM (device-timed with CUDA events, L2
+flushed between steps); `e2e` is the same metric through the public API with
+host inputs copied in and O/LSE copied out inside the timed region;
+`roofline` reports the dominant kernel against MEASURED_PEAKS.json;
+`cpu_baseline` times the CPU oracle on a bounded sample of the same workload.
+With --gpus N under torchrun every rank runs its own replica of the workload
+(weak scaling; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged multi-token attn: query tok/s, KV GB/s & TC util vs GB300 roofline"
+UNIT = "query tok/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="llama13b_mixed")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- multi-rank plumbing
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate_ranks(tokens: float, seconds: float):
+    """Whole-job totals: tokens summed over ranks, time = max over ranks (no-op on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return tokens, seconds
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([tokens], dtype=torch.float64, device=dev)
+    s = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(t.item()), float(s.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- peaks, clocks, profiles
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM traffic per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    src = {"split_kv": "decode.cu", "tensor_core": "attn_tc.cu"}.get(kernel)
+    if not src or not os.path.exists(path):
+        return None
+    with open(os.path.join(ROOT, "paged_kv_attention_25_gb300", "csrc", src), "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(batch, budget_s: float, kp=None, vp=None):
+    """Time the CPU oracle on a stratified sample of the batch's query tokens (all heads each).
+
+    Returns (tokens_per_s, seconds, n_tokens, threads, description)."""
+    import oracle
+    oracle.build()
+    if kp is None:
+        kp, vp = batch.pool_arrays()
+        oracle.append(kp, vp, batch.block_tables, batch.cu_q_lens, batch.q_positions, batch.k_new, batch.v_new)
+    T, Hq = batch.num_tokens, batch.num_q_heads
+
+    def run(tokens):
+        t = np.repeat(tokens, Hq).astype(np.int32)
+        h = np.tile(np.arange(Hq, dtype=np.int32), len(tokens))
+        t0 = time.perf_counter()
+        oracle.paged_attn_rows(batch.q, kp, vp, batch.block_tables, batch.ctx_lens, batch.cu_q_lens,
+                               batch.q_positions, batch.scale, t, h)
+        return time.perf_counter() - t0
+
+    pilot_stride = max(1, T // 16)
+    pilot = np.arange(0, T, pilot_stride)[:16]
+    dt = run(pilot)
+    per_tok = dt / len(pilot)
+    n = int(max(1, min(T, budget_s / max(per_tok, 1e-9))))
+    stride = max(1, T // n)
+    tokens = np.arange(0, T, stride)[:n]
+    dt = run(tokens)
+    desc = (f"{len(tokens)} of {T} query tokens (every {stride}th, all {Hq} heads) of {batch.name}; "
+            f"fp64 C oracle")
+    return len(tokens) / dt, dt, len(tokens), oracle.num_threads(), desc
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    from paged_kv_attention_25_gb300 import workloads as wl
+    import oracle
+    batch = wl.WORKLOADS[args.workload]()
+    kp, vp = batch.pool_arrays()
+    oracle.append(kp, vp, batch.block_tables, batch.cu_q_lens, batch.q_positions, batch.k_new, batch.v_new)
+    per_step = max(0.05, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(batch, per_step, kp, vp)
+    toks = secs = 0.0
+    info = None
+    for _ in range(args.steps):
+        rate, dt, n, thr, desc = oracle_sample(batch, per_step, kp, vp)
+        toks += n
+        secs += dt
+        info = (thr, desc)
+    value = toks / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**batch.describe(), "sample_per_step": info[1]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": info[0], "kind": "oracle", "sample": info[1]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_attention_25_gb300 import build as pkv_build
+    from paged_kv_attention_25_gb300 import pkv
+    from paged_kv_attention_25_gb300 import workloads as wl
+
+    world, rank, local = dist_info()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        pkv_build.build()
+    barrier()
+    pkv_build.build()   # no-op when fresh; other ranks wait for rank 0 above
+
+    maker = wl.WORKLOADS[args.workload]
+    batch = maker() if world == 1 else maker(seed=maker.__defaults__[0] + 1000 * rank)
+    pool = pkv.Pool(batch.num_blocks, batch.num_kv_heads, batch.head_dim, device=dev)
+    wl.fill_pool(batch, pool.k, pool.v)
+    d = wl.upload(batch, dev)
+    meta = pkv.HostMeta(batch.cu_q_lens, batch.ctx_lens, batch.q_positions)
+    T, Hq, D = batch.num_tokens, batch.num_q_heads, batch.head_dim
+    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    ws = pool.workspace(pkv.pkv_paged_attn_workspace_size(pool, Hq, meta))
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=dev)
+
+    # Swap-out target: the history blocks of the conversation with the longest context
+    # among requests that are not appended into past their history (read-only this step).
+    q_lens = np.diff(batch.cu_q_lens)
+    r_swap = int(np.argmax(np.where(q_lens > 0, batch.ctx_lens, -1)))
+    first_q = int(batch.q_positions[batch.cu_q_lens[r_swap]:batch.cu_q_lens[r_swap + 1]].min())
+    swap_ids = batch.block_tables[r_swap, :max(1, first_q // 16)].astype(np.int32)
+    swap_host = torch.empty((len(swap_ids), 2, batch.num_kv_heads, 16, D), dtype=torch.bfloat16).pin_memory()
+    swap_bytes = swap_host.numel() * 2
+    appended = torch.cuda.Event()
+    swapped = torch.cuda.Event()
+
+    def step():
+        pkv.pkv_append(pool, d["block_tables"], d["cu_q_lens"], d["q_positions"], d["k_new"], d["v_new"])
+        appended.record(main)
+        side.wait_event(appended)
+        pkv.pkv_swap_out(pool, swap_ids, swap_host, stream=side)
+        swapped.record(side)
+        pkv.pkv_paged_attn(pool, d["q"], d["q_positions"], d["block_tables"], d["ctx_lens"], d["cu_q_lens"],
+                           meta, batch.scale, out=out, lse=lse, workspace=ws)
+        main.wait_event(swapped)
+
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if pkv.pkv_check_device_errors(pool) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- timed region: K steps, L2 flushed between steps, per-step CUDA events
+    pkv.pkv_profile_read(pool, reset=True)
+    pkv.pkv_profile_enable(pool, True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    gpu_index = int(visible[dev.index]) if dev.index < len(visible) and visible[dev.index].isdigit() else dev.index
+    with ClockSampler(gpu_index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(main)
+            step()
+            ends[i].record(main)
+        torch.cuda.synchronize()
+        wall1 = time.perf_counter()
+        barrier()
+    pkv.pkv_profile_enable(pool, False)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    prof = pkv.pkv_profile_read(pool, reset=True)
+    if pkv.pkv_check_device_errors(pool) != 0:
+        raise RuntimeError("device error word set during the timed region")
+    dev_s = sum(step_ms) / 1e3
+    tokens_all, secs_all = aggregate_ranks(float(T * args.steps), dev_s)
+    value = tokens_all / secs_all
+    st = pkv.pkv_last_plan_stats(pool)
+
+    # ---- end to end: host inputs in, O/LSE out, through the public API
+    e2e_steps = args.e2e_steps or max(10, args.steps // 4)
+    host_in = {k: (v.cpu().pin_memory()) for k, v in d.items()}
+    host_out = torch.empty_like(out, device="cpu").pin_memory()
+    host_lse = torch.empty_like(lse, device="cpu").pin_memory()
+    dev_in = {k: torch.empty_like(v) for k, v in d.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * 2 + host_lse.numel() * 4
+
+    def e2e_step():
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        meta_e = pkv.HostMeta(host_in["cu_q_lens"].numpy(), host_in["ctx_lens"].numpy(), host_in["q_positions"].numpy())
+        pkv.pkv_append(pool, dev_in["block_tables"], dev_in["cu_q_lens"], dev_in["q_positions"], dev_in["k_new"],
+                       dev_in["v_new"])
+        pkv.pkv_paged_attn(pool, dev_in["q"], dev_in["q_positions"], dev_in["block_tables"], dev_in["ctx_lens"],
+                           dev_in["cu_q_lens"], meta_e, batch.scale, out=out, lse=lse, workspace=ws)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    barrier()
+    for i in range(e2e_steps):
+        flush.zero_()
+        es[i].record(main)
+        e2e_step()
+        ee[i].record(main)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_s = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / 1e3
+    e_tok, e_sec = aggregate_ranks(float(T * e2e_steps), e2e_s)
+
+    # ---- swap bandwidth alone (both directions, pinned host)
+    ids = batch.used_blocks[:min(len(batch.used_blocks), 4096)].astype(np.int32)
+    sh = torch.empty((len(ids), 2, batch.num_kv_heads, 16, D), dtype=torch.bfloat16).pin_memory()
+    pkv.pkv_swap_out(pool, ids, sh)
+    torch.cuda.synchronize()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    e0.record(main)
+    pkv.pkv_swap_out(pool, ids, sh)
+    e1.record(main)
+    pkv.pkv_swap_in(pool, ids, sh)
+    e2.record(main)
+    torch.cuda.synchronize()
+    swap_out_gbs = sh.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
+    swap_in_gbs = sh.numel() * 2 / (e1.elapsed_time(e2) / 1e3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    fam = {k: v for k, v in prof.items() if k in ("split_kv", "tensor_core") and v["launches"]}
+    dom = max(fam, key=lambda k: fam[k]["total_ms"]) if fam else None
+    roof = None
+    if dom:
+        avg_s = fam[dom]["total_ms"] / fam[dom]["launches"] / 1e3
+        if dom == "split_kv":
+            nbytes, flops = st["decode_kv_bytes"] + st["decode_io_bytes"], st["decode_flops"]
+        else:
+            nbytes, flops = st["tc_kv_bytes"] + st["tc_io_bytes"], st["tc_flops"]
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+        if t_tc > t_hbm:
+            achieved, peak, unit, bound = flops / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor"
+        else:
+            achieved, peak, unit, bound = nbytes / avg_s / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
+        roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "peak_source": f"{peak_src} (burst)",
+                "traffic": recorded_traffic(dom, batch.name), "algorithmic_bytes": nbytes,
+                "algorithmic_flops": flops, "avg_launch_us": avg_s * 1e6}
+
+    step_ms_avg = 1e3 * secs_all / args.steps
+    kv_bytes = st["decode_kv_bytes"] + st["tc_kv_bytes"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms_avg, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**batch.describe(), "l2": "flushed between steps (258 MB write)",
+                   "parallelism": f"replicas x{world}", "swap_out_bytes_per_step": swap_bytes},
+        "kv_gbs": kv_bytes / (step_ms_avg / 1e3) / 1e9,
+        "tflops": (st["decode_flops"] + st["tc_flops"]) / (step_ms_avg / 1e3) / 1e12,
+        "kernels": {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(1, v["launches"])}
+                    for k, v in prof.items()},
+        "plan": {k: st[k] for k in ("num_decode_items", "num_tc_items", "num_merge_items")},
+        "gpu_launches": int(sum(v["launches"] for v in prof.values())),
+        "roofline": roof,
+        "e2e": {"value": e_tok / e_sec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "swap": {"out_gbs": swap_out_gbs, "in_gbs": swap_in_gbs, "bytes": sh.numel() * 2},
+        "clocks": clk.summary(),
+        "wall_s_timed": wall1 - wall0,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        rate, dt, n, thr, desc = oracle_sample(batch, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc,
+                                "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

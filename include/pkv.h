@@ -1,0 +1,251 @@
+/*
+ * pkv.h - C ABI of a GB300 (sm_103a) library for paged multi-token attention.
+ *
+ * The operation is the generalised PagedAttention of "Stateful Large Language
+ * Model Serving with Pensieve" (abstract): in one unified batch every request
+ * brings one or more new input tokens (a new-turn prefill, a single decode
+ * token, or recomputed evicted history) that attend over that conversation's
+ * cached keys and values, which sit in fixed-size blocks scattered over
+ * non-contiguous GPU memory.  The block pool and the per-request block table
+ * follow the PagedAttention description in the blog "LLM上下文缓存与状态复用机制的
+ * 分析和探索" (section 3.1: fixed-size blocks allocated on demand, stored in
+ * non-contiguous physical memory).  The CPU tier of Pensieve's multi-tier
+ * cache (abstract; "ahead-of-time swapping" in the method summary) is served
+ * by the swap calls.
+ *
+ * Conventions for every call
+ *   - Return value: PKV_OK (0) or one of the PKV_E* codes below.  On error,
+ *     pkv_last_error() returns a message (thread-local, valid until the next
+ *     call on the same thread).  Arguments are validated on the host before
+ *     anything is launched; an invalid argument launches nothing.
+ *   - "device" pointers are CUDA device memory of the current device;
+ *     "host" pointers are CPU memory.  The caller owns every buffer it passes
+ *     (queries, new K/V, outputs, metadata, workspace, host swap buffers); the
+ *     library owns only what pkv_pool_create allocated.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous with respect to the host unless stated.
+ *   - Data that violates a precondition which can only be seen on the device
+ *     (a block id outside the pool, a position outside the block table) is
+ *     skipped by the kernels and recorded in the pool's device error word;
+ *     pkv_check_device_errors() reads it.  Kernels never trap.  Every wait
+ *     inside a kernel is bounded; a wait that runs out records
+ *     PKV_DEVERR_TIMEOUT and the kernel returns.
+ *
+ * Layouts (row-major, bf16 = IEEE bfloat16 bit patterns)
+ *   Kpool, Vpool : [num_blocks][num_kv_heads][block_size][head_dim] bf16
+ *   block_tables : [num_reqs][max_blocks] int32; entry i of request r is the
+ *                  physical block holding positions [i*B, (i+1)*B).  Entries at
+ *                  or beyond ceil(ctx_len/B) are never read (-1 is customary).
+ *   cu_q_lens    : [num_reqs+1] int32, cu_q_lens[0] = 0, nondecreasing; the
+ *                  query tokens of request r are rows [cu_q_lens[r], cu_q_lens[r+1]).
+ *   positions / q_positions : [num_tokens] int32 absolute positions.
+ *   Q            : [num_tokens][num_q_heads][head_dim] bf16
+ *   K, V (new)   : [num_tokens][num_kv_heads][head_dim] bf16
+ *   O            : [num_tokens][num_q_heads][head_dim] bf16
+ *   LSE          : [num_tokens][num_q_heads] fp32, natural log
+ *   swap buffer  : [n][2][num_kv_heads][block_size][head_dim] bf16 (K then V)
+ *
+ * Supported shapes: block_size 16; head_dim 64 or 128; num_q_heads a
+ * multiple of num_kv_heads with group size G = num_q_heads/num_kv_heads <= 128.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_OK 0
+#define PKV_EINVAL 1       /* invalid argument, shape or size */
+#define PKV_ENOMEM 2       /* device allocation failed (pkv_pool_create only) */
+#define PKV_ECUDA 3        /* a CUDA runtime or driver call failed */
+#define PKV_ETIMEOUT 4     /* a bounded device-side wait ran out */
+#define PKV_EDEVICE 5      /* kernels skipped invalid data; see the error word */
+#define PKV_EUNSUPPORTED 6 /* valid but not supported (e.g. head_dim 96) */
+
+#define PKV_DTYPE_BF16 0
+
+/* Bits of the device error word (pkv_check_device_errors). */
+#define PKV_DEVERR_BLOCK_ID 1u   /* a block-table entry outside [0, num_blocks) */
+#define PKV_DEVERR_POSITION 2u   /* a position outside [0, max_blocks*block_size) */
+#define PKV_DEVERR_TIMEOUT 4u    /* a bounded wait inside a kernel gave up */
+#define PKV_DEVERR_INTERNAL 8u   /* a kernel found its launch configuration unusable */
+
+typedef struct pkv_pool pkv_pool; /* opaque */
+
+typedef struct {
+  int num_blocks;   /* physical blocks in the pool, >= 1 */
+  int block_size;   /* tokens per block; must be 16 */
+  int num_kv_heads; /* >= 1 */
+  int head_dim;     /* 64 or 128 */
+  int dtype;        /* PKV_DTYPE_BF16 */
+  /* Optional caller-owned device storage for the two pools (each
+   * num_blocks*num_kv_heads*block_size*head_dim*2 bytes, 16-byte aligned).
+   * NULL: the library allocates (and zero-fills) the storage itself. */
+  void* k_storage;
+  void* v_storage;
+} pkv_pool_desc;
+
+/* Host copies of the batch metadata, used to plan the work split.
+ * cu_q_lens [num_reqs+1] and ctx_lens [num_reqs] are required;
+ * q_positions [num_tokens] is optional (NULL: every query tile is assumed to
+ * see the whole context, and kernels clip their key ranges on the device). */
+typedef struct {
+  const int32_t* cu_q_lens;
+  const int32_t* ctx_lens;
+  const int32_t* q_positions;
+} pkv_host_meta;
+
+/* What one planned batch contains (for reporting and the roofline). */
+typedef struct {
+  int num_decode_items;     /* CTAs of the CUDA-core split-KV kernel */
+  int num_tc_items;         /* CTAs of the tensor-core kernel */
+  int num_merge_items;      /* (token tile, KV head) groups merged by log-sum-exp */
+  int num_partial_rows;     /* fp32 partial rows held in the workspace */
+  int64_t decode_kv_bytes;  /* algorithmic K+V bytes read by the split-KV kernel */
+  int64_t tc_kv_bytes;      /* algorithmic K+V bytes read by the tensor-core kernel */
+  int64_t decode_flops;     /* 4*D per visible (query row, key) pair */
+  int64_t tc_flops;
+  int64_t decode_io_bytes;  /* Q read + O/LSE written for the split-KV kernel's rows */
+  int64_t tc_io_bytes;      /* Q read + O/LSE written for the tensor-core kernel's rows */
+  size_t workspace_bytes;   /* what pkv_paged_attn needs for this batch */
+} pkv_plan_stats;
+
+/* Accumulated device time per kernel family while profiling is on. */
+typedef struct {
+  int launches[4];          /* 0 append, 1 split-KV, 2 tensor-core, 3 merge */
+  double total_ms[4];
+} pkv_profile;
+
+/* Create a KV block pool.  Allocates the pools (unless caller storage is
+ * given), a device error word, and builds the TMA descriptors the
+ * tensor-core kernel uses.  Synchronous.  Errors: PKV_EINVAL (bad desc),
+ * PKV_EUNSUPPORTED (block_size != 16, head_dim not 64/128), PKV_ENOMEM,
+ * PKV_ECUDA (no device, driver too old). */
+int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out);
+
+/* Destroy a pool: synchronises the device, frees what the library allocated.
+ * NULL is accepted.  Caller storage is not freed. */
+int pkv_pool_destroy(pkv_pool* pool);
+
+/* Device addresses of the K and V pools (for tests and host gathers). */
+int pkv_pool_kv_ptrs(const pkv_pool* pool, void** k, void** v);
+
+/*
+ * Paged KV append ("LLM上下文缓存与状态复用机制的分析和探索" section 3.1; the new
+ * tokens of Pensieve's unified batch): for every token t of request r at
+ * position p = positions[t] and every KV head g,
+ *   Kpool[block_tables[r][p / B]][g][p % B][:] = k_new[t][g][:]   (bit copy)
+ * and the same for V.  Device inputs: block_tables, cu_q_lens, positions,
+ * k_new, v_new.  Positions of one request must be distinct (two tokens writing
+ * one slot leave either value).  Out-of-range slots are skipped and flagged in
+ * the device error word.  num_tokens == 0 is a no-op.
+ */
+int pkv_append(pkv_pool* pool, const int32_t* block_tables, int max_blocks, int num_reqs,
+               const int32_t* cu_q_lens, const int32_t* positions, const void* k_new,
+               const void* v_new, int num_tokens, void* stream);
+
+/*
+ * Workspace bytes pkv_paged_attn needs for this batch (plans the batch on the
+ * host; the plan is cached and reused by a following pkv_paged_attn with the
+ * same metadata).  Synchronous, host only.
+ */
+int pkv_paged_attn_workspace_size(pkv_pool* pool, int num_q_heads, int num_reqs, int num_tokens,
+                                  const pkv_host_meta* host_meta, size_t* bytes);
+
+/*
+ * Generalised paged attention (Pensieve abstract: attention between multiple
+ * input tokens over a GPU cache spread across non-contiguous memory).
+ * For query token t of request r at position p_t = q_positions[t] and query
+ * head h, with KV head g = h / (num_q_heads / num_kv_heads):
+ *   s_j = scale * q[t][h] . K_r[j][g]   for keys j = 0 .. p_t   (causal on
+ *         absolute position; K_r[j] is slot j % B of block block_tables[r][j / B])
+ *   O[t][h]   = sum_j exp(s_j - m) V_r[j][g] / sum_j exp(s_j - m),  m = max_j s_j
+ *   LSE[t][h] = m + ln(sum_j exp(s_j - m))
+ * Preconditions: 0 <= p_t < ctx_lens[r] <= max_blocks * 16; every key
+ * position < ctx_lens[r] has been written (append before attention);
+ * block-table entries for positions < ctx_lens[r] are valid pool blocks.
+ * The host checks the first two against host_meta (PKV_EINVAL); the kernels
+ * check block ids and never read past a block-table row.
+ *
+ * Device inputs: q, q_positions, block_tables, ctx_lens, cu_q_lens.
+ * Device outputs: o (bf16), lse (fp32; may be NULL).  host_meta holds host
+ * copies of cu_q_lens / ctx_lens (and optionally q_positions) for planning.
+ * workspace: device memory of at least pkv_paged_attn_workspace_size() bytes,
+ * 256-byte aligned, owned by the caller and not used by other work in flight.
+ * The split-KV partials and the uploaded work list live there.
+ * num_tokens == 0 is a no-op.  Errors: PKV_EINVAL for bad shapes, a workspace
+ * that is too small, or host metadata that is inconsistent.
+ */
+int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t* q_positions,
+                   const int32_t* block_tables, int max_blocks, const int32_t* ctx_lens,
+                   const int32_t* cu_q_lens, int num_reqs, int num_tokens,
+                   const pkv_host_meta* host_meta, float scale, void* o, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Statistics of the last plan built on this pool. */
+int pkv_last_plan_stats(const pkv_pool* pool, pkv_plan_stats* out);
+
+/*
+ * CPU cache tier (Pensieve abstract: multi-tier GPU/CPU caching).  Copy n whole
+ * physical blocks (all KV heads, K then V) from the pool to host memory laid
+ * out [n][2][Hkv][B][D] (swap out), or back into the pool (swap in).
+ * block_ids is a HOST array; host_buf should be pinned (cudaHostAlloc) for
+ * the copies to be asynchronous and overlap with kernels on other streams.
+ * Runs of consecutive ids are coalesced into one 2-D copy per pool.  Issue on
+ * a side stream and record an event to overlap with attention.
+ * Errors: PKV_EINVAL for an id outside [0, num_blocks) (nothing is copied).
+ */
+int pkv_swap_out(pkv_pool* pool, const int32_t* block_ids, int n, void* host_buf, void* stream);
+int pkv_swap_in(pkv_pool* pool, const int32_t* block_ids, int n, const void* host_buf, void* stream);
+
+/* Synchronise `stream`, read the device error word into *flags (may be NULL)
+ * and clear it.  Returns PKV_EDEVICE if any bit was set (PKV_ETIMEOUT if the
+ * timeout bit was), else PKV_OK. */
+int pkv_check_device_errors(pkv_pool* pool, void* stream, unsigned* flags);
+
+/* Kernel timing with CUDA events recorded around every launch on the launch
+ * stream.  Enabling adds one event pair per launch.  pkv_profile_read
+ * synchronises the recorded events, adds their durations into *out and, if
+ * reset != 0, clears the totals. */
+int pkv_profile_enable(pkv_pool* pool, int on);
+int pkv_profile_read(pkv_pool* pool, pkv_profile* out, int reset);
+
+/* One planned work item, as reported by pkv_plan_inspect.  Rows of an item
+ * are (token q_start + i, query head kv_head*G + j), i < q_count, j < G. */
+typedef struct {
+  int32_t kernel;    /* 1: split-KV (CUDA cores), 2: tensor-core tile */
+  int32_t req;
+  int32_t kv_head;
+  int32_t q_start;
+  int32_t q_count;
+  int32_t kv_start;  /* key positions [kv_start, kv_end) */
+  int32_t kv_end;
+  int32_t part;      /* -1: writes O/LSE directly; else first partial row */
+} pkv_work_desc;
+
+/* Plan a batch on the host only (no device needed) and copy out its work
+ * items: the split-KV items first, then the tensor-core items.  At most
+ * max_items are written; *num_items receives the total.  stats may be NULL.
+ * Used to test the planner; pkv_paged_attn plans internally. */
+int pkv_plan_inspect(int num_q_heads, int num_kv_heads, int head_dim, int num_sms, int num_reqs,
+                     int num_tokens, const pkv_host_meta* host_meta, pkv_work_desc* items,
+                     int max_items, int* num_items, pkv_plan_stats* stats);
+
+/* Number of SMs the planner sizes the work split for (current device). */
+int pkv_device_sm_count(int* sms);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* pkv_last_error(void);
+
+/* Library version string. */
+const char* pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

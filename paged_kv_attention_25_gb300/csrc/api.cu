@@ -1,0 +1,427 @@
+// Host side of the C ABI declared in include/pkv.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using namespace pkv;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define PKV_CUDA(call, what)                 \
+  do {                                       \
+    cudaError_t e_ = (call);                 \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct ProfRec {
+  int kernel;
+  cudaEvent_t a, b;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct pkv_pool {
+  int num_blocks = 0, block_size = 0, num_kv_heads = 0, head_dim = 0;
+  void* k = nullptr;
+  void* v = nullptr;
+  bool owns = false;
+  unsigned* d_err = nullptr;
+  int device = 0, num_sms = 0;
+  CUtensorMap tmap_k;  // 64-byte aligned by its type
+  CUtensorMap tmap_v;
+  std::mutex mu;
+  Plan plan;
+  std::vector<uint8_t> staging;
+  // profiling
+  bool prof_on = false;
+  std::vector<cudaEvent_t> ev_free;
+  std::vector<ProfRec> pending;
+  pkv_profile totals{};
+
+  PoolView view() const { return PoolView{k, v, num_blocks, num_kv_heads, head_dim, d_err}; }
+
+  cudaEvent_t take_event() {
+    if (ev_free.empty()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      return e;
+    }
+    cudaEvent_t e = ev_free.back();
+    ev_free.pop_back();
+    return e;
+  }
+};
+
+namespace {
+
+// Launch `fn` on `stream`, bracketed by profiling events when profiling is on.
+template <class F>
+int timed_launch(pkv_pool* pool, int kernel, void* stream, F&& fn) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (pool->prof_on) {
+    a = pool->take_event();
+    b = pool->take_event();
+    if (a && b) cudaEventRecord(a, static_cast<cudaStream_t>(stream));
+  }
+  const int rc = fn();
+  if (a && b) {
+    cudaEventRecord(b, static_cast<cudaStream_t>(stream));
+    pool->pending.push_back({kernel, a, b});
+  }
+  return rc;
+}
+
+int make_tmap(CUtensorMap* map, void* base, int num_blocks, int hkv, int head_dim) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled unavailable (driver too old?)");
+  const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * hkv * kBlockSize;
+  if (rows >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "pool too large for 32-bit TMA row coordinates");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(static_cast<int>(r)));
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_err.c_str(); }
+
+const char* pkv_version(void) { return "pkv 0.1 (sm_103a)"; }
+
+int pkv_device_sm_count(int* sms) {
+  if (!sms) return fail(PKV_EINVAL, "sms is NULL");
+  int dev = 0;
+  PKV_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  PKV_CUDA(cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+  return PKV_OK;
+}
+
+int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
+  if (!desc || !out) return fail(PKV_EINVAL, "desc/out is NULL");
+  *out = nullptr;
+  if (desc->num_blocks < 1 || desc->num_kv_heads < 1) return fail(PKV_EINVAL, "num_blocks and num_kv_heads must be >= 1");
+  if (desc->block_size != kBlockSize) return fail(PKV_EUNSUPPORTED, "block_size must be 16");
+  if (desc->head_dim != 64 && desc->head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (desc->dtype != PKV_DTYPE_BF16) return fail(PKV_EUNSUPPORTED, "only bf16 pools are supported");
+  if ((desc->k_storage == nullptr) != (desc->v_storage == nullptr))
+    return fail(PKV_EINVAL, "give both k_storage and v_storage or neither");
+  if (desc->k_storage && (!aligned16(desc->k_storage) || !aligned16(desc->v_storage)))
+    return fail(PKV_EINVAL, "pool storage must be 16-byte aligned");
+  auto* p = new pkv_pool();
+  p->num_blocks = desc->num_blocks;
+  p->block_size = desc->block_size;
+  p->num_kv_heads = desc->num_kv_heads;
+  p->head_dim = desc->head_dim;
+  auto cleanup = [p](int rc) {
+    if (p->owns) {
+      cudaFree(p->k);
+      cudaFree(p->v);
+    }
+    if (p->d_err) cudaFree(p->d_err);
+    delete p;
+    return rc;
+  };
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaGetDevice"));
+  e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaDeviceGetAttribute"));
+  const size_t bytes = static_cast<size_t>(desc->num_blocks) * desc->num_kv_heads * kBlockSize * desc->head_dim * 2;
+  if (desc->k_storage) {
+    p->k = desc->k_storage;
+    p->v = desc->v_storage;
+  } else {
+    p->owns = true;
+    if (cudaMalloc(&p->k, bytes) != cudaSuccess) { p->k = nullptr; return cleanup(fail(PKV_ENOMEM, "cudaMalloc K pool")); }
+    if (cudaMalloc(&p->v, bytes) != cudaSuccess) { p->v = nullptr; return cleanup(fail(PKV_ENOMEM, "cudaMalloc V pool")); }
+    if (cudaMemset(p->k, 0, bytes) != cudaSuccess || cudaMemset(p->v, 0, bytes) != cudaSuccess)
+      return cleanup(fail(PKV_ECUDA, "cudaMemset pool"));
+  }
+  if (cudaMalloc(&p->d_err, sizeof(unsigned)) != cudaSuccess) { p->d_err = nullptr; return cleanup(fail(PKV_ENOMEM, "cudaMalloc error word")); }
+  if (cudaMemset(p->d_err, 0, sizeof(unsigned)) != cudaSuccess) return cleanup(fail(PKV_ECUDA, "cudaMemset error word"));
+  int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim);
+  if (rc) return cleanup(rc);
+  rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim);
+  if (rc) return cleanup(rc);
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaDeviceSynchronize"));
+  *out = p;
+  return PKV_OK;
+}
+
+int pkv_pool_destroy(pkv_pool* pool) {
+  if (!pool) return PKV_OK;
+  cudaDeviceSynchronize();
+  if (pool->owns) {
+    cudaFree(pool->k);
+    cudaFree(pool->v);
+  }
+  cudaFree(pool->d_err);
+  for (auto& r : pool->pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : pool->ev_free) cudaEventDestroy(e);
+  delete pool;
+  return PKV_OK;
+}
+
+int pkv_pool_kv_ptrs(const pkv_pool* pool, void** k, void** v) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  if (k) *k = pool->k;
+  if (v) *v = pool->v;
+  return PKV_OK;
+}
+
+int pkv_append(pkv_pool* pool, const int32_t* block_tables, int max_blocks, int num_reqs, const int32_t* cu_q_lens,
+               const int32_t* positions, const void* k_new, const void* v_new, int num_tokens, void* stream) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  if (num_tokens < 0 || num_reqs < 0) return fail(PKV_EINVAL, "negative size");
+  if (num_tokens == 0) return PKV_OK;
+  if (num_reqs < 1 || max_blocks < 1) return fail(PKV_EINVAL, "num_reqs and max_blocks must be >= 1");
+  if (!block_tables || !cu_q_lens || !positions || !k_new || !v_new) return fail(PKV_EINVAL, "NULL device pointer");
+  if (!aligned16(k_new) || !aligned16(v_new)) return fail(PKV_EINVAL, "k_new / v_new must be 16-byte aligned");
+  if (static_cast<int64_t>(max_blocks) * kBlockSize > (1ll << 31)) return fail(PKV_EINVAL, "max_blocks too large");
+  PoolView pv = pool->view();
+  int rc = timed_launch(pool, 0, stream, [&] {
+    return launch_append(pv, pool->k, pool->v, block_tables, max_blocks, num_reqs, cu_q_lens, positions, k_new,
+                         v_new, num_tokens, stream);
+  });
+  if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "append launch");
+  return PKV_OK;
+}
+
+static int plan_for(pkv_pool* pool, int num_q_heads, int num_reqs, int num_tokens, int max_blocks,
+                    const pkv_host_meta* meta) {
+  if (!meta) return fail(PKV_EINVAL, "host_meta is NULL");
+  PlanParams pp{num_q_heads, pool->num_kv_heads, pool->head_dim, pool->num_sms, num_reqs, num_tokens, max_blocks};
+  const uint64_t sig = plan_signature(pp, *meta);
+  if (pool->plan.valid && pool->plan.signature == sig) return PKV_OK;
+  const char* err = "plan failed";
+  pool->plan.valid = false;
+  int rc = build_plan(pp, *meta, &pool->plan, &err);
+  if (rc) return fail(rc, err);
+  return PKV_OK;
+}
+
+int pkv_paged_attn_workspace_size(pkv_pool* pool, int num_q_heads, int num_reqs, int num_tokens,
+                                  const pkv_host_meta* host_meta, size_t* bytes) {
+  if (!pool || !bytes) return fail(PKV_EINVAL, "pool/bytes is NULL");
+  if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads) return fail(PKV_EINVAL, "num_q_heads must be a multiple of num_kv_heads");
+  if (num_reqs < 0 || num_tokens < 0) return fail(PKV_EINVAL, "negative size");
+  std::lock_guard<std::mutex> lk(pool->mu);
+  int rc = plan_for(pool, num_q_heads, num_reqs, num_tokens, 0, host_meta);
+  if (rc) return rc;
+  *bytes = pool->plan.total;
+  return PKV_OK;
+}
+
+int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t* q_positions,
+                   const int32_t* block_tables, int max_blocks, const int32_t* ctx_lens, const int32_t* cu_q_lens,
+                   int num_reqs, int num_tokens, const pkv_host_meta* host_meta, float scale, void* o, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  if (num_tokens < 0 || num_reqs < 0) return fail(PKV_EINVAL, "negative size");
+  if (num_tokens == 0) return PKV_OK;
+  if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads) return fail(PKV_EINVAL, "num_q_heads must be a multiple of num_kv_heads");
+  if (num_q_heads / pool->num_kv_heads > kTcRows) return fail(PKV_EUNSUPPORTED, "group size above 128");
+  if (num_reqs < 1 || max_blocks < 1) return fail(PKV_EINVAL, "num_reqs and max_blocks must be >= 1");
+  if (!q || !q_positions || !block_tables || !ctx_lens || !cu_q_lens || !o) return fail(PKV_EINVAL, "NULL device pointer");
+  if (!aligned16(q) || !aligned16(o)) return fail(PKV_EINVAL, "q and o must be 16-byte aligned");
+  if (!(scale > 0.f)) return fail(PKV_EINVAL, "scale must be positive");
+  std::lock_guard<std::mutex> lk(pool->mu);
+  int rc = plan_for(pool, num_q_heads, num_reqs, num_tokens, max_blocks, host_meta);
+  if (rc) return rc;
+  const Plan& pl = pool->plan;
+  if (!workspace || workspace_bytes < pl.total) return fail(PKV_EINVAL, "workspace missing or smaller than pkv_paged_attn_workspace_size()");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(PKV_EINVAL, "workspace must be 256-byte aligned");
+
+  // Upload the work lists (from pageable memory: the host buffer is free on return).
+  const size_t meta_bytes = pl.off_part_o;
+  pool->staging.assign(meta_bytes, 0);
+  if (!pl.decode.empty()) std::memcpy(pool->staging.data() + pl.off_decode, pl.decode.data(), pl.decode.size() * sizeof(WorkItem));
+  if (!pl.tc.empty()) std::memcpy(pool->staging.data() + pl.off_tc, pl.tc.data(), pl.tc.size() * sizeof(WorkItem));
+  if (!pl.merge.empty()) std::memcpy(pool->staging.data() + pl.off_merge, pl.merge.data(), pl.merge.size() * sizeof(MergeItem));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (meta_bytes) PKV_CUDA(cudaMemcpyAsync(ws, pool->staging.data(), meta_bytes, cudaMemcpyHostToDevice, s), "upload work list");
+
+  AttnArgs a;
+  a.pool = pool->view();
+  a.q = q;
+  a.num_q_heads = num_q_heads;
+  a.group = num_q_heads / pool->num_kv_heads;
+  a.q_positions = q_positions;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.ctx_lens = ctx_lens;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.o = o;
+  a.lse = lse;
+  a.part_o = reinterpret_cast<float*>(ws + pl.off_part_o);
+  a.part_lse = reinterpret_cast<float*>(ws + pl.off_part_lse);
+
+  const WorkItem* d_dec = reinterpret_cast<const WorkItem*>(ws + pl.off_decode);
+  const WorkItem* d_tc = reinterpret_cast<const WorkItem*>(ws + pl.off_tc);
+  const MergeItem* d_merge = reinterpret_cast<const MergeItem*>(ws + pl.off_merge);
+  if (!pl.tc.empty()) {
+    rc = timed_launch(pool, 2, stream, [&] {
+      return launch_tc(a, &pool->tmap_k, &pool->tmap_v, d_tc, static_cast<int>(pl.tc.size()), stream);
+    });
+    if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "tensor-core attention launch");
+  }
+  if (!pl.decode.empty()) {
+    rc = timed_launch(pool, 1, stream, [&] { return launch_decode(a, d_dec, static_cast<int>(pl.decode.size()), stream); });
+    if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "split-KV attention launch");
+  }
+  if (!pl.merge.empty()) {
+    rc = timed_launch(pool, 3, stream, [&] { return launch_merge(a, d_merge, static_cast<int>(pl.merge.size()), stream); });
+    if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "merge launch");
+  }
+  return PKV_OK;
+}
+
+int pkv_plan_inspect(int num_q_heads, int num_kv_heads, int head_dim, int num_sms, int num_reqs, int num_tokens,
+                     const pkv_host_meta* host_meta, pkv_work_desc* items, int max_items, int* num_items,
+                     pkv_plan_stats* stats) {
+  if (!host_meta || !num_items) return fail(PKV_EINVAL, "host_meta/num_items is NULL");
+  if (head_dim != 64 && head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
+  Plan plan;
+  const char* err = "plan failed";
+  PlanParams pp{num_q_heads, num_kv_heads, head_dim, num_sms, num_reqs, num_tokens, 0};
+  const int rc = build_plan(pp, *host_meta, &plan, &err);
+  if (rc) return fail(rc, err);
+  const int total = static_cast<int>(plan.decode.size() + plan.tc.size());
+  *num_items = total;
+  int k = 0;
+  for (int which = 0; which < 2; ++which)
+    for (const WorkItem& w : which == 0 ? plan.decode : plan.tc) {
+      if (items && k < max_items)
+        items[k] = pkv_work_desc{which + 1, w.req, w.kv_head, w.q_start, w.q_count, w.kv_start, w.kv_end, w.part};
+      ++k;
+    }
+  if (stats) *stats = plan.stats;
+  return PKV_OK;
+}
+
+int pkv_last_plan_stats(const pkv_pool* pool, pkv_plan_stats* out) {
+  if (!pool || !out) return fail(PKV_EINVAL, "pool/out is NULL");
+  if (!pool->plan.valid) return fail(PKV_EINVAL, "no plan built yet");
+  *out = pool->plan.stats;
+  return PKV_OK;
+}
+
+static int swap_impl(pkv_pool* pool, const int32_t* ids, int n, void* host, bool out, void* stream) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  if (n < 0) return fail(PKV_EINVAL, "negative count");
+  if (n == 0) return PKV_OK;
+  if (!ids || !host) return fail(PKV_EINVAL, "NULL block_ids or host buffer");
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= pool->num_blocks) return fail(PKV_EINVAL, "block id outside the pool");
+  const size_t blk = static_cast<size_t>(pool->num_kv_heads) * kBlockSize * pool->head_dim * 2;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* h = static_cast<uint8_t*>(host);
+  int i = 0;
+  while (i < n) {
+    int j = i + 1;
+    while (j < n && ids[j] == ids[j - 1] + 1) ++j;   // run of consecutive physical blocks
+    const size_t run = static_cast<size_t>(j - i);
+    for (int kv = 0; kv < 2; ++kv) {
+      uint8_t* dev = static_cast<uint8_t*>(kv == 0 ? pool->k : pool->v) + static_cast<size_t>(ids[i]) * blk;
+      uint8_t* hp = h + (static_cast<size_t>(i) * 2 + kv) * blk;
+      cudaError_t e = out ? cudaMemcpy2DAsync(hp, 2 * blk, dev, blk, blk, run, cudaMemcpyDeviceToHost, s)
+                          : cudaMemcpy2DAsync(dev, blk, hp, 2 * blk, blk, run, cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(e, out ? "swap out copy" : "swap in copy");
+    }
+    i = j;
+  }
+  return PKV_OK;
+}
+
+int pkv_swap_out(pkv_pool* pool, const int32_t* block_ids, int n, void* host_buf, void* stream) {
+  return swap_impl(pool, block_ids, n, host_buf, true, stream);
+}
+
+int pkv_swap_in(pkv_pool* pool, const int32_t* block_ids, int n, const void* host_buf, void* stream) {
+  return swap_impl(pool, block_ids, n, const_cast<void*>(host_buf), false, stream);
+}
+
+int pkv_check_device_errors(pkv_pool* pool, void* stream, unsigned* flags) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  PKV_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");
+  unsigned v = 0;
+  PKV_CUDA(cudaMemcpy(&v, pool->d_err, sizeof v, cudaMemcpyDeviceToHost), "read error word");
+  PKV_CUDA(cudaMemset(pool->d_err, 0, sizeof v), "clear error word");
+  if (flags) *flags = v;
+  if (v & PKV_DEVERR_TIMEOUT) return fail(PKV_ETIMEOUT, "a bounded wait inside a kernel ran out");
+  if (v) return fail(PKV_EDEVICE, "kernels skipped invalid block ids or positions");
+  return PKV_OK;
+}
+
+int pkv_profile_enable(pkv_pool* pool, int on) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  pool->prof_on = on != 0;
+  return PKV_OK;
+}
+
+int pkv_profile_read(pkv_pool* pool, pkv_profile* out, int reset) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  for (auto& r : pool->pending) {
+    PKV_CUDA(cudaEventSynchronize(r.b), "cudaEventSynchronize");
+    float ms = 0.f;
+    PKV_CUDA(cudaEventElapsedTime(&ms, r.a, r.b), "cudaEventElapsedTime");
+    pool->totals.launches[r.kernel] += 1;
+    pool->totals.total_ms[r.kernel] += ms;
+    pool->ev_free.push_back(r.a);
+    pool->ev_free.push_back(r.b);
+  }
+  pool->pending.clear();
+  if (out) *out = pool->totals;
+  if (reset) pool->totals = pkv_profile{};
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,357 @@
+// Split-KV paged attention for the decode regime (few query rows per KV head).
+//
+// One CTA runs one work item: a request, one KV head, up to kDecodeMaxRows
+// query rows (tokens x grouped query heads) and a range of key positions.
+// The item's KV blocks are streamed from HBM exactly once: each (block, KV
+// head) is one contiguous 16 x D bf16 chunk of the pool, fetched with a 1-D
+// bulk copy (cp.async.bulk) into a per-warp ring of shared-memory stages
+// tracked by mbarriers.  The four warps take blocks round-robin and keep their
+// own online-softmax state (running max m, sum l, fp32 accumulator); the CTA
+// merges the four states at the end and writes either the final O / LSE or a
+// split partial that the merge kernel combines by log-sum-exp (split-KV as in
+// "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM Serving on
+// Commodity GPUs", section 2; attention as in "Stateful Large Language Model
+// Serving with Pensieve", abstract).
+//
+// Arithmetic: scores in fp32 with scale*log2(e) folded into q, exp2 on the
+// SFU, fp32 accumulation; O rounded to bf16 once at the end.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+
+template <int D>
+struct DecodeSmem {
+  static constexpr int kChunk = kBlockSize * D * 2;            // bytes of one (block, head) of K or V
+  static constexpr int kStage = 2 * kChunk;                    // K then V
+  static constexpr int kRing = kWarps * kStages * kStage;
+  static constexpr int kMergeFloats = kWarps * kDecodeMaxRows * (D + 2);
+  static constexpr int kPBuf = kWarps * kDecodeMaxRows * kBlockSize * 4;
+  static constexpr int kBars = kWarps * kStages * 8;
+  static constexpr int kTotal = kRing + kMergeFloats * 4 + kPBuf + kBars + 16;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
+  using S = DecodeSmem<D>;
+  constexpr int kDPL = D / 32;   // head dims per lane
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  float* merge = reinterpret_cast<float*>(smem + S::kRing);
+  float* pbuf = merge + S::kMergeFloats;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(pbuf) + S::kPBuf);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + kWarps * kStages);
+
+  // Once any wait in this launch has given up, the remaining CTAs do nothing.
+  // (__syncthreads_or makes the decision the same for every thread of the CTA.)
+  if (__syncthreads_or((*reinterpret_cast<volatile unsigned*>(a.pool.err) & PKV_DEVERR_TIMEOUT) != 0)) return;
+  const WorkItem it = items[blockIdx.x];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.group;
+  const int rows = it.q_count * G;
+  const int Hkv = a.pool.num_kv_heads;
+  const int g = it.kv_head;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWarps * kStages; ++i) mbar_init(&bars[i], 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+
+  // Per-row query (pre-scaled by scale*log2 e) and position; rows >= `rows` are inert.
+  float q[kDecodeMaxRows][kDPL];
+  int qpos[kDecodeMaxRows];
+  int max_pos = -1;
+#pragma unroll
+  for (int r = 0; r < kDecodeMaxRows; ++r) {
+    qpos[r] = -1;
+#pragma unroll
+    for (int d = 0; d < kDPL; ++d) q[r][d] = 0.f;
+    if (r < rows) {
+      const int t = it.q_start + r / G;
+      const int h = g * G + r % G;
+      qpos[r] = __ldg(a.q_positions + t);
+      max_pos = max(max_pos, qpos[r]);
+      const uint16_t* src = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D + lane * kDPL;
+      if constexpr (kDPL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2*>(src);
+        q[r][0] = bf16lo_to_f32(v.x) * a.scale_log2;
+        q[r][1] = bf16hi_to_f32(v.x) * a.scale_log2;
+        q[r][2] = bf16lo_to_f32(v.y) * a.scale_log2;
+        q[r][3] = bf16hi_to_f32(v.y) * a.scale_log2;
+      } else {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
+        q[r][0] = bf16lo_to_f32(v) * a.scale_log2;
+        q[r][1] = bf16hi_to_f32(v) * a.scale_log2;
+      }
+    }
+  }
+  const int kv_end = min(it.kv_end, max_pos + 1);
+  const int blk0 = it.kv_start / kBlockSize;
+  const int nblk = kv_end > it.kv_start ? (kv_end - it.kv_start + kBlockSize - 1) / kBlockSize : 0;
+  const int nb_w = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;   // blocks of this warp
+
+  __syncthreads();
+
+  uint8_t* my_ring = ring + warp * kStages * S::kStage;
+  uint64_t* my_full = bars + warp * kStages;
+  float* my_p = pbuf + warp * kDecodeMaxRows * kBlockSize;
+  const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
+
+  // Physical block ids of this warp's iterations, 32 at a time (lane l holds iteration base+l).
+  auto load_ids = [&](int base) -> int {
+    const int i = base + lane;
+    int pb = -1;
+    if (i < nb_w) {
+      const int col = blk0 + warp + kWarps * i;
+      pb = col < a.max_blocks ? __ldg(bt_row + col) : -1;
+      if (pb < 0 || pb >= a.pool.num_blocks) {
+        atomicOr(a.pool.err, PKV_DEVERR_BLOCK_ID);
+        pb = -1;
+      }
+    }
+    return pb;
+  };
+  int ids_cur = load_ids(0), ids_next = load_ids(32), win = 0;
+
+  auto issue = [&](int j) {
+    // Only lane 0 issues; every lane evaluates the shuffle.
+    const int src_lane = j & 31;
+    const int pb = (j >> 5) == win ? __shfl_sync(0xffffffffu, ids_cur, src_lane)
+                                   : __shfl_sync(0xffffffffu, ids_next, src_lane);
+    if (lane == 0) {
+      const int st = j % kStages;
+      uint8_t* dst = my_ring + st * S::kStage;
+      if (pb >= 0) {
+        const int64_t off = (static_cast<int64_t>(pb) * Hkv + g) * S::kChunk;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&my_full[st], 2 * S::kChunk);
+        bulk_g2s(dst, static_cast<const uint8_t*>(a.pool.k) + off, S::kChunk, &my_full[st]);
+        bulk_g2s(dst + S::kChunk, static_cast<const uint8_t*>(a.pool.v) + off, S::kChunk, &my_full[st]);
+      } else {
+        mbar_arrive(&my_full[st]);   // invalid block: stage keeps stale data, error already flagged
+      }
+    }
+  };
+
+#pragma unroll
+  for (int s = 0; s < kStages; ++s)
+    if (s < nb_w) issue(s);
+
+  float m[kDecodeMaxRows], l[kDecodeMaxRows], acc[kDecodeMaxRows][kDPL];
+#pragma unroll
+  for (int r = 0; r < kDecodeMaxRows; ++r) {
+    m[r] = -CUDART_INF_F;
+    l[r] = 0.f;
+#pragma unroll
+    for (int d = 0; d < kDPL; ++d) acc[r][d] = 0.f;
+  }
+
+  int consumed = 0;
+  bool aborted = false;
+  for (int i = 0; i < nb_w; ++i) {
+    if ((i & 31) == 0 && i > 0) {   // slide the block-id window
+      ids_cur = ids_next;
+      win = i >> 5;
+      ids_next = load_ids(i + 32);
+    }
+    const int st = i % kStages;
+    if (!mbar_wait_warp(&my_full[st], (i / kStages) & 1, s_abort)) {
+      aborted = true;
+      break;
+    }
+    const uint8_t* kb = my_ring + st * S::kStage;
+    const uint8_t* vb = kb + S::kChunk;
+    const int key0 = (blk0 + warp + kWarps * i) * kBlockSize;
+
+    // q . k for 16 keys, this lane's dims.
+    float part[kDecodeMaxRows][kBlockSize];
+#pragma unroll
+    for (int k = 0; k < kBlockSize; ++k) {
+      float kf[kDPL];
+      if constexpr (kDPL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2*>(kb + (k * D + lane * kDPL) * 2);
+        kf[0] = bf16lo_to_f32(v.x); kf[1] = bf16hi_to_f32(v.x);
+        kf[2] = bf16lo_to_f32(v.y); kf[3] = bf16hi_to_f32(v.y);
+      } else {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(kb + (k * D + lane * kDPL) * 2);
+        kf[0] = bf16lo_to_f32(v); kf[1] = bf16hi_to_f32(v);
+      }
+#pragma unroll
+      for (int r = 0; r < kDecodeMaxRows; ++r) {
+        if (r < rows) {
+          float s = 0.f;
+#pragma unroll
+          for (int d = 0; d < kDPL; ++d) s = fmaf(q[r][d], kf[d], s);
+          part[r][k] = s;
+        }
+      }
+    }
+
+#pragma unroll
+    for (int r = 0; r < kDecodeMaxRows; ++r) {
+      if (r >= rows) break;
+      // Transpose-reduce the 16 partial dot products over the 32 lanes:
+      // afterwards lane holds the full score of key (lane >> 1).
+      float v8[8], v4[4], v2[2], v1;
+      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float send = b4 ? part[r][j] : part[r][j + 8];
+        const float keep = b4 ? part[r][j + 8] : part[r][j];
+        v8[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float send = b3 ? v8[j] : v8[j + 4];
+        const float keep = b3 ? v8[j + 4] : v8[j];
+        v4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float send = b2 ? v4[j] : v4[j + 2];
+        const float keep = b2 ? v4[j + 2] : v4[j];
+        v2[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+      {
+        const float send = b1 ? v2[0] : v2[1];
+        const float keep = b1 ? v2[1] : v2[0];
+        v1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+      float s = v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
+      const int key = key0 + (lane >> 1);
+      if (key > qpos[r] || key >= kv_end) s = -CUDART_INF_F;
+      float mx = s;
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_new = fmaxf(m[r], mx);
+      const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
+      const float alpha = fast_exp2(m[r] - m_use);
+      const float p = fast_exp2(s - m_use);
+      float ps = p;
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      l[r] = l[r] * alpha + ps;
+      m[r] = m_new;
+#pragma unroll
+      for (int d = 0; d < kDPL; ++d) acc[r][d] *= alpha;
+      if ((lane & 1) == 0) my_p[r * kBlockSize + (lane >> 1)] = p;
+    }
+    __syncwarp();
+
+    // acc += p . V for this lane's dims; keys at or past kv_end read as zero.
+#pragma unroll
+    for (int k = 0; k < kBlockSize; ++k) {
+      float vf[kDPL];
+      const bool live = key0 + k < kv_end;
+      if constexpr (kDPL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2*>(vb + (k * D + lane * kDPL) * 2);
+        vf[0] = bf16lo_to_f32(v.x); vf[1] = bf16hi_to_f32(v.x);
+        vf[2] = bf16lo_to_f32(v.y); vf[3] = bf16hi_to_f32(v.y);
+      } else {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(vb + (k * D + lane * kDPL) * 2);
+        vf[0] = bf16lo_to_f32(v); vf[1] = bf16hi_to_f32(v);
+      }
+#pragma unroll
+      for (int d = 0; d < kDPL; ++d) vf[d] = live ? vf[d] : 0.f;
+#pragma unroll
+      for (int r = 0; r < kDecodeMaxRows; ++r) {
+        if (r >= rows) break;
+        const float p = my_p[r * kBlockSize + k];
+#pragma unroll
+        for (int d = 0; d < kDPL; ++d) acc[r][d] = fmaf(p, vf[d], acc[r][d]);
+      }
+    }
+    __syncwarp();
+    consumed = i + 1;
+    if (i + kStages < nb_w) issue(i + kStages);
+  }
+
+  if (aborted) {
+    if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
+    *s_abort = 1;
+    // Let this warp's copies in flight land before the CTA's shared memory is released.
+    for (int j = consumed; j < min(nb_w, consumed + kStages); ++j)
+      (void)mbar_wait_warp(&my_full[j % kStages], (j / kStages) & 1, nullptr);
+  }
+
+  // Merge the four warps' (m, l, acc) states.
+  float* wm = merge + (warp * kDecodeMaxRows) * (D + 2);
+#pragma unroll
+  for (int r = 0; r < kDecodeMaxRows; ++r) {
+    if (r >= rows) break;
+    float* dst = wm + r * (D + 2);
+#pragma unroll
+    for (int d = 0; d < kDPL; ++d) dst[lane * kDPL + d] = acc[r][d];
+    if (lane == 0) {
+      dst[D] = m[r];
+      dst[D + 1] = l[r];
+    }
+  }
+  __syncthreads();
+
+  constexpr float kLn2 = 0.69314718055994530942f;
+  for (int idx = threadIdx.x; idx < rows * (D / 2); idx += blockDim.x) {
+    const int r = idx / (D / 2);
+    const int d = (idx % (D / 2)) * 2;
+    float mw[kWarps], mstar = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      mw[w] = merge[(w * kDecodeMaxRows + r) * (D + 2) + D];
+      mstar = fmaxf(mstar, mw[w]);
+    }
+    float lsum = 0.f, o0 = 0.f, o1 = 0.f;
+    if (mstar != -CUDART_INF_F) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float* src = merge + (w * kDecodeMaxRows + r) * (D + 2);
+        const float f = fast_exp2(mw[w] - mstar);
+        lsum += src[D + 1] * f;
+        o0 += src[d] * f;
+        o1 += src[d + 1] * f;
+      }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    o0 *= inv;
+    o1 *= inv;
+    const float lse = lsum > 0.f ? (mstar + fast_log2(lsum)) * kLn2 : -CUDART_INF_F;
+    const int t = it.q_start + r / G;
+    const int h = g * G + r % G;
+    if (it.part < 0) {
+      uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D + d);
+      *o = pack_bf16x2(o0, o1);
+      if (d == 0 && a.lse) a.lse[static_cast<int64_t>(t) * a.num_q_heads + h] = lse;
+    } else {
+      float2* o = reinterpret_cast<float2*>(a.part_o + static_cast<int64_t>(it.part + r) * D + d);
+      *o = make_float2(o0, o1);
+      if (d == 0) a.part_lse[it.part + r] = lse;
+    }
+  }
+}
+
+}  // namespace
+
+template <int D>
+static int launch_decode_d(const AttnArgs& a, const WorkItem* items, int n_items, void* stream) {
+  const int smem = DecodeSmem<D>::kTotal;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<D><<<n_items, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(a, items);
+  return cudaGetLastError();
+}
+
+int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream) {
+  if (n_items <= 0) return cudaSuccess;
+  if (a.pool.head_dim == 128) return launch_decode_d<128>(a, items, n_items, stream);
+  return launch_decode_d<64>(a, items, n_items, stream);
+}
+
+}  // namespace pkv

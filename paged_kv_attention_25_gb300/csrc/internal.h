@@ -1,0 +1,101 @@
+// Internal types shared by the host API, the planner and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;        // tokens per KV block
+constexpr int kDecodeMaxRows = 4;     // query rows (tokens x group) per split-KV item
+constexpr int kTcRows = 128;          // query rows per tensor-core tile (TMEM lanes)
+constexpr int kTcKeys = 64;           // keys per tensor-core KV tile (4 blocks)
+
+// One CTA of work.  Rows of an item are (token q_start + i, query head
+// kv_head*G + j) for i < q_count, j < G, numbered i*G + j.
+struct WorkItem {
+  int32_t req;
+  int32_t kv_head;
+  int32_t q_start;   // first token (index into [0, num_tokens))
+  int32_t q_count;   // tokens in the item
+  int32_t kv_start;  // first key position (multiple of the kernel's key tile)
+  int32_t kv_end;    // one past the last key position this item may read
+  int32_t part;      // -1: write O / LSE directly; else first fp32 partial row
+  int32_t pad;
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+// Log-sum-exp merge of `nsplit` partial results of one (token tile, KV head).
+// Partial row of split s and item row i: part_base + s * (q_count * G) + i.
+struct MergeItem {
+  int32_t q_start;
+  int32_t q_count;
+  int32_t kv_head;
+  int32_t nsplit;
+  int32_t part_base;
+  int32_t pad[3];
+};
+static_assert(sizeof(MergeItem) == 32, "MergeItem layout");
+
+struct PlanParams {
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int num_sms;
+  int num_reqs;
+  int num_tokens;
+  int max_blocks;   // block-table row length; 0 = not checked (host-only planning)
+};
+
+struct Plan {
+  std::vector<WorkItem> decode;   // split-KV CUDA-core kernel
+  std::vector<WorkItem> tc;       // tensor-core kernel
+  std::vector<MergeItem> merge;
+  int num_partial_rows = 0;
+  pkv_plan_stats stats{};
+  // Workspace layout (byte offsets, 256-aligned sections).
+  size_t off_decode = 0, off_tc = 0, off_merge = 0, off_part_o = 0, off_part_lse = 0, total = 0;
+  uint64_t signature = 0;
+  bool valid = false;
+};
+
+// Host planner.  Returns PKV_OK or PKV_EINVAL (message in *err).
+int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, const char** err);
+uint64_t plan_signature(const PlanParams& pp, const pkv_host_meta& meta);
+
+// Kernel launchers (defined in the .cu files); return cudaError_t as int.
+struct PoolView {
+  const void* k;
+  const void* v;
+  int num_blocks, num_kv_heads, head_dim;
+  unsigned* err;   // device error word
+};
+
+int launch_append(const PoolView& pool, void* kp, void* vp, const int32_t* bt, int max_blocks, int num_reqs,
+                  const int32_t* cu_q_lens, const int32_t* positions, const void* k_new, const void* v_new,
+                  int num_tokens, void* stream);
+
+struct AttnArgs {
+  PoolView pool;
+  const void* q;
+  int num_q_heads;
+  int group;             // num_q_heads / num_kv_heads
+  const int32_t* q_positions;
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* ctx_lens;
+  float scale_log2;      // scale * log2(e)
+  void* o;
+  float* lse;
+  float* part_o;         // [num_partial_rows][head_dim]
+  float* part_lse;       // [num_partial_rows]
+};
+
+int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream);
+int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const WorkItem* items, int n_items,
+              void* stream);
+int launch_merge(const AttnArgs& a, const MergeItem* items, int n_items, void* stream);
+
+}  // namespace pkv

@@ -1,0 +1,137 @@
+// Log-sum-exp merge of split-KV partials, and the paged KV append.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Merge: one warp per query row of a merge item.  Split s of row i holds
+// O_s (normalised, fp32) and LSE_s; the combined row is
+//   LSE = M + ln sum_s exp(LSE_s - M),  O = sum_s exp(LSE_s - LSE) O_s,
+// which equals attention over the union of the splits' key ranges (the
+// split-and-merge of "PersistentKV: Page-Aware Decode Scheduling for
+// Long-Context LLM Serving on Commodity GPUs", section 2).
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a, const MergeItem* __restrict__ items) {
+  constexpr int kDPL = D / 32;
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr float kLn2 = 0.69314718055994530942f;
+  const MergeItem mi = items[blockIdx.x];
+  const int G = a.group;
+  const int rows = mi.q_count * G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < rows; r += blockDim.x >> 5) {
+    float mx = -CUDART_INF_F;
+    for (int s = lane; s < mi.nsplit; s += 32) mx = fmaxf(mx, a.part_lse[mi.part_base + s * rows + r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float acc[kDPL];
+#pragma unroll
+    for (int d = 0; d < kDPL; ++d) acc[d] = 0.f;
+    float wsum = 0.f;
+    if (mx != -CUDART_INF_F) {
+      for (int s = 0; s < mi.nsplit; ++s) {
+        const int pr = mi.part_base + s * rows + r;
+        const float w = fast_exp2((a.part_lse[pr] - mx) * kLog2e);
+        wsum += w;
+        const float* src = a.part_o + static_cast<int64_t>(pr) * D + lane * kDPL;
+        if constexpr (kDPL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+          acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int t = mi.q_start + r / G;
+    const int h = mi.kv_head * G + r % G;
+    uint16_t* dst = static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D + lane * kDPL;
+    if constexpr (kDPL == 4) {
+      uint2 w;
+      w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(dst) = w;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0 && a.lse)
+      a.lse[static_cast<int64_t>(t) * a.num_q_heads + h] =
+          wsum > 0.f ? mx + fast_log2(wsum) * kLn2 : -CUDART_INF_F;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Append: every 16-byte chunk of a new K/V row goes to its slot
+//   pool[block_tables[r][p / 16]][g][p % 16][:]
+// (fixed-size blocks in non-contiguous memory, "LLM上下文缓存与状态复用机制的分析和探索",
+// section 3.1).  Consecutive threads copy consecutive chunks of one row, so both
+// the read of the new rows and the write into the block are coalesced.
+__global__ void __launch_bounds__(256) append_kernel(uint4* __restrict__ kp, uint4* __restrict__ vp, int num_blocks,
+                                                     int hkv, int chunks_per_row, const int32_t* __restrict__ bt,
+                                                     int max_blocks, int num_reqs, const int32_t* __restrict__ cu,
+                                                     const int32_t* __restrict__ pos, const uint4* __restrict__ k_new,
+                                                     const uint4* __restrict__ v_new, int num_tokens, unsigned* err) {
+  const int64_t total = static_cast<int64_t>(num_tokens) * hkv * chunks_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % chunks_per_row);
+    const int64_t row = i / chunks_per_row;   // t * hkv + g
+    const int g = static_cast<int>(row % hkv);
+    const int t = static_cast<int>(row / hkv);
+    int lo = 0, hi = num_reqs - 1;             // last r with cu[r] <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    const int p = __ldg(pos + t);
+    if (p < 0 || p >= max_blocks * kBlockSize) {
+      if (c == 0) atomicOr(err, PKV_DEVERR_POSITION);
+      continue;
+    }
+    const int pb = __ldg(bt + static_cast<int64_t>(lo) * max_blocks + p / kBlockSize);
+    if (pb < 0 || pb >= num_blocks) {
+      if (c == 0) atomicOr(err, PKV_DEVERR_BLOCK_ID);
+      continue;
+    }
+    const int64_t dst = ((static_cast<int64_t>(pb) * hkv + g) * kBlockSize + (p % kBlockSize)) * chunks_per_row + c;
+    kp[dst] = __ldg(k_new + i);
+    vp[dst] = __ldg(v_new + i);
+  }
+}
+
+}  // namespace
+
+int launch_merge(const AttnArgs& a, const MergeItem* items, int n_items, void* stream) {
+  if (n_items <= 0) return cudaSuccess;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a.pool.head_dim == 128) merge_kernel<128><<<n_items, 128, 0, s>>>(a, items);
+  else merge_kernel<64><<<n_items, 128, 0, s>>>(a, items);
+  return cudaGetLastError();
+}
+
+int launch_append(const PoolView& pool, void* kp, void* vp, const int32_t* bt, int max_blocks, int num_reqs,
+                  const int32_t* cu_q_lens, const int32_t* positions, const void* k_new, const void* v_new,
+                  int num_tokens, void* stream) {
+  if (num_tokens <= 0) return cudaSuccess;
+  const int cpr = pool.head_dim / 8;
+  const int64_t total = static_cast<int64_t>(num_tokens) * pool.num_kv_heads * cpr;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (total + 255) / 256;
+  const int grid = static_cast<int>(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+  append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(kp), static_cast<uint4*>(vp), pool.num_blocks, pool.num_kv_heads, cpr, bt, max_blocks,
+      num_reqs, cu_q_lens, positions, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), num_tokens,
+      pool.err);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

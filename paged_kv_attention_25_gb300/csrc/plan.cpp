@@ -1,0 +1,246 @@
+// Host worklist planner.
+//
+// Packs the ragged requests of one unified batch into CTA work items: one
+// compact list holding only real work, with no padding to a common length and
+// no launch per length bucket (the compact work queue of "PersistentKV:
+// Page-Aware Decode Scheduling for Long-Context LLM Serving on Commodity
+// GPUs", section 2), and long key ranges cut into partitions that run on
+// different SMs and are merged by log-sum-exp (the same page's split of one
+// long context into chapters).  Unlike that page, the split count is not a
+// constant: it is chosen from the batch's total work so that every kernel has
+// several items per CTA slot.
+//
+// Routing: a request whose query rows per KV head (q_len * G) fit in
+// kDecodeMaxRows goes to the CUDA-core split-KV kernel (HBM streaming, one
+// item per KV head); every other request goes to the tensor-core kernel in
+// tiles of at most 128 query rows.
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kDecodeCtasPerSm = 2;
+constexpr int kTcCtasPerSm = 2;
+constexpr int kItemsPerSlot = 8;        // target work items per CTA slot
+constexpr int kMinDecodeChunk = 16;     // blocks (256 keys) per split at least
+constexpr int kMinTcChunk = 4;          // 64-key tiles per split at least
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct QGroup {
+  int req;
+  int q_start;
+  int q_count;
+  int kv_len;   // keys the group can see: min(ctx, max position + 1)
+};
+
+}  // namespace
+
+uint64_t plan_signature(const PlanParams& pp, const pkv_host_meta& meta) {
+  uint64_t h = 1469598103934665603ull;
+  auto mix = [&h](const void* p, size_t n) {
+    const unsigned char* b = static_cast<const unsigned char*>(p);
+    for (size_t i = 0; i < n; ++i) {
+      h ^= b[i];
+      h *= 1099511628211ull;
+    }
+  };
+  mix(&pp, sizeof pp);
+  if (meta.cu_q_lens) mix(meta.cu_q_lens, sizeof(int32_t) * (pp.num_reqs + 1));
+  if (meta.ctx_lens) mix(meta.ctx_lens, sizeof(int32_t) * pp.num_reqs);
+  int has_pos = meta.q_positions != nullptr;
+  mix(&has_pos, sizeof has_pos);
+  if (has_pos) mix(meta.q_positions, sizeof(int32_t) * pp.num_tokens);
+  return h;
+}
+
+int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, const char** err) {
+  *plan = Plan();
+  const int R = pp.num_reqs, T = pp.num_tokens, Hq = pp.num_q_heads, Hkv = pp.num_kv_heads, D = pp.head_dim;
+  if (R < 0 || T < 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) {
+    *err = "plan: bad head counts or sizes";
+    return PKV_EINVAL;
+  }
+  const int G = Hq / Hkv;
+  if (G > kTcRows) {
+    *err = "plan: group size num_q_heads/num_kv_heads above 128";
+    return PKV_EINVAL;
+  }
+  if (!meta.cu_q_lens || !meta.ctx_lens) {
+    *err = "plan: host cu_q_lens and ctx_lens are required";
+    return PKV_EINVAL;
+  }
+  const int32_t* cu = meta.cu_q_lens;
+  const int32_t* ctx = meta.ctx_lens;
+  const int32_t* pos = meta.q_positions;
+  if (cu[0] != 0 || cu[R] != T) {
+    *err = "plan: cu_q_lens must start at 0 and end at num_tokens";
+    return PKV_EINVAL;
+  }
+  for (int r = 0; r < R; ++r) {
+    if (cu[r + 1] < cu[r]) {
+      *err = "plan: cu_q_lens must be nondecreasing";
+      return PKV_EINVAL;
+    }
+    if (ctx[r] < 0 || (cu[r + 1] > cu[r] && ctx[r] < 1)) {
+      *err = "plan: a request with query tokens needs ctx_len >= 1";
+      return PKV_EINVAL;
+    }
+    if (pp.max_blocks > 0 && static_cast<int64_t>(ctx[r]) > static_cast<int64_t>(pp.max_blocks) * kBlockSize) {
+      *err = "plan: ctx_len exceeds max_blocks * block_size";
+      return PKV_EINVAL;
+    }
+    if (pos) {
+      for (int t = cu[r]; t < cu[r + 1]; ++t)
+        if (pos[t] < 0 || pos[t] >= ctx[r]) {
+          *err = "plan: query position outside [0, ctx_len)";
+          return PKV_EINVAL;
+        }
+    }
+  }
+
+  // 1. Query groups: all tokens (split-KV route) or tiles of <= 128 rows.
+  std::vector<QGroup> dec_groups, tc_groups;
+  const int tq = kTcRows / G;  // tokens per tensor-core tile
+  for (int r = 0; r < R; ++r) {
+    const int n = cu[r + 1] - cu[r];
+    if (n == 0) continue;
+    auto kv_len_of = [&](int t0, int c) {
+      if (!pos) return static_cast<int>(ctx[r]);
+      int mx = 0;
+      for (int t = t0; t < t0 + c; ++t) mx = std::max(mx, static_cast<int>(pos[t]));
+      return std::min(static_cast<int>(ctx[r]), mx + 1);
+    };
+    if (n * G <= kDecodeMaxRows) {
+      dec_groups.push_back({r, cu[r], n, kv_len_of(cu[r], n)});
+      continue;
+    }
+    int t = cu[r];
+    const int end = cu[r + 1];
+    while (t < end) {
+      int c = 1;
+      // A tile holds consecutive tokens; with known positions it also stops at
+      // a jump in position (e.g. recomputed prefix [0,e) vs new tokens [c,..)).
+      while (c < tq && t + c < end) {
+        if (pos && pos[t + c] != pos[t + c - 1] + 1) break;
+        ++c;
+      }
+      tc_groups.push_back({r, t, c, kv_len_of(t, c)});
+      t += c;
+    }
+  }
+
+  // 2. Split sizes from the total work of each kernel.
+  int64_t dec_blocks = 0, tc_tiles = 0;
+  for (const auto& g : dec_groups) dec_blocks += ceil_div(g.kv_len, kBlockSize) * Hkv;
+  for (const auto& g : tc_groups) tc_tiles += ceil_div(g.kv_len, kTcKeys) * Hkv;
+  const int sms = std::max(1, pp.num_sms);
+  const int64_t dec_chunk = std::max<int64_t>(kMinDecodeChunk,
+                                              ceil_div(dec_blocks, int64_t(sms) * kDecodeCtasPerSm * kItemsPerSlot));
+  const int64_t tc_chunk = std::max<int64_t>(kMinTcChunk,
+                                             ceil_div(tc_tiles, int64_t(sms) * kTcCtasPerSm * kItemsPerSlot));
+
+  int part_rows = 0;
+  auto emit = [&](const QGroup& g, int unit_keys, int64_t chunk_units, std::vector<WorkItem>& out) {
+    const int rows = g.q_count * G;
+    const int64_t units = ceil_div(g.kv_len, unit_keys);
+    int nsplit = static_cast<int>(std::max<int64_t>(1, ceil_div(units, chunk_units)));
+    // Even split in whole units; no split is left empty.
+    const int64_t per = ceil_div(units, nsplit);
+    nsplit = static_cast<int>(ceil_div(units, per));
+    for (int kvh = 0; kvh < Hkv; ++kvh) {
+      int base = -1;
+      if (nsplit > 1) {
+        base = part_rows;
+        part_rows += nsplit * rows;
+        plan->merge.push_back({g.q_start, g.q_count, kvh, nsplit, base, {0, 0, 0}});
+      }
+      for (int s = 0; s < nsplit; ++s) {
+        const int64_t u0 = s * per;
+        const int64_t u1 = std::min(units, u0 + per);
+        WorkItem w;
+        w.req = g.req;
+        w.kv_head = kvh;
+        w.q_start = g.q_start;
+        w.q_count = g.q_count;
+        w.kv_start = static_cast<int32_t>(u0 * unit_keys);
+        w.kv_end = static_cast<int32_t>(std::min<int64_t>(g.kv_len, u1 * unit_keys));
+        w.part = nsplit > 1 ? base + s * rows : -1;
+        w.pad = 0;
+        if (w.kv_end <= w.kv_start) {   // cannot happen with an even split; keep a valid empty item
+          w.kv_end = w.kv_start;
+        }
+        out.push_back(w);
+      }
+    }
+  };
+  for (const auto& g : dec_groups) emit(g, kBlockSize, dec_chunk, plan->decode);
+  for (const auto& g : tc_groups) emit(g, kTcKeys, tc_chunk, plan->tc);
+
+  // 3. Longest items first, so that the tail of each launch is short.
+  auto longer = [](const WorkItem& a, const WorkItem& b) {
+    return (a.kv_end - a.kv_start) > (b.kv_end - b.kv_start);
+  };
+  std::stable_sort(plan->decode.begin(), plan->decode.end(), longer);
+  std::stable_sort(plan->tc.begin(), plan->tc.end(), longer);
+  plan->num_partial_rows = part_rows;
+
+  // 4. Statistics (algorithmic work; each (request, KV head) KV read once).
+  pkv_plan_stats& st = plan->stats;
+  st.num_decode_items = static_cast<int>(plan->decode.size());
+  st.num_tc_items = static_cast<int>(plan->tc.size());
+  st.num_merge_items = static_cast<int>(plan->merge.size());
+  st.num_partial_rows = part_rows;
+  std::vector<int> req_kv_dec(R, 0), req_kv_tc(R, 0);
+  for (const auto& g : dec_groups) req_kv_dec[g.req] = std::max(req_kv_dec[g.req], g.kv_len);
+  for (const auto& g : tc_groups) req_kv_tc[g.req] = std::max(req_kv_tc[g.req], g.kv_len);
+  const int64_t per_key = int64_t(2) * Hkv * D * 2;   // K and V, all KV heads, bf16
+  for (int r = 0; r < R; ++r) {
+    st.decode_kv_bytes += req_kv_dec[r] * per_key;
+    st.tc_kv_bytes += req_kv_tc[r] * per_key;
+  }
+  auto row_flops = [&](const std::vector<QGroup>& gs) {
+    int64_t f = 0;
+    for (const auto& g : gs)
+      for (int t = g.q_start; t < g.q_start + g.q_count; ++t) {
+        const int64_t vis = pos ? pos[t] + 1 : g.kv_len;
+        f += int64_t(4) * D * vis * Hq;
+      }
+    return f;
+  };
+  st.decode_flops = row_flops(dec_groups);
+  st.tc_flops = row_flops(tc_groups);
+  auto io_bytes = [&](const std::vector<QGroup>& gs) {
+    int64_t toks = 0;
+    for (const auto& g : gs) toks += g.q_count;
+    return toks * Hq * (int64_t(D) * 2 * 2 + 4);   // Q in, O out (bf16), LSE out (fp32)
+  };
+  st.decode_io_bytes = io_bytes(dec_groups);
+  st.tc_io_bytes = io_bytes(tc_groups);
+
+  // 5. Workspace layout.
+  size_t off = 0;
+  plan->off_decode = off;
+  off = align256(off + plan->decode.size() * sizeof(WorkItem));
+  plan->off_tc = off;
+  off = align256(off + plan->tc.size() * sizeof(WorkItem));
+  plan->off_merge = off;
+  off = align256(off + plan->merge.size() * sizeof(MergeItem));
+  plan->off_part_o = off;
+  off = align256(off + size_t(part_rows) * D * sizeof(float));
+  plan->off_part_lse = off;
+  off = align256(off + size_t(part_rows) * sizeof(float));
+  plan->total = std::max<size_t>(off, 256);
+  st.workspace_bytes = plan->total;
+  plan->signature = plan_signature(pp, meta);
+  plan->valid = true;
+  return PKV_OK;
+}
+
+}  // namespace pkv

@@ -327,3 +327,39 @@ def random_small(seed: int, *, num_q_heads: int = 4, num_kv_heads: int = 2, head
             reqs.append(_recompute(c, e, int(g.integers(0, max_q + 1))))
     return build_batch(f"random_small_{seed}", reqs, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                        head_dim=head_dim, pool_factor=1.5, seed=seed)
+
+
+# ---------------------------------------------------------------------------
+# Device copies (input marshalling only).
+# ---------------------------------------------------------------------------
+
+def bf16_tensor(bits: np.ndarray, device):
+    """A torch bfloat16 tensor holding the given bf16 bit patterns."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def upload(batch: Batch, device="cuda") -> dict:
+    """Device tensors of a batch's per-step inputs: q, k_new, v_new (bf16) and the int32 metadata."""
+    import torch
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+    return {
+        "q": bf16_tensor(batch.q, device),
+        "k_new": bf16_tensor(batch.k_new, device),
+        "v_new": bf16_tensor(batch.v_new, device),
+        "block_tables": i32(batch.block_tables),
+        "ctx_lens": i32(batch.ctx_lens),
+        "cu_q_lens": i32(batch.cu_q_lens),
+        "q_positions": i32(batch.q_positions),
+    }
+
+
+def fill_pool(batch: Batch, k_storage, v_storage):
+    """Write the batch's initial pool contents (used blocks; zeros elsewhere) into device storage."""
+    import torch
+    k_storage.zero_()
+    v_storage.zero_()
+    if batch.used_blocks.size:
+        idx = torch.from_numpy(batch.used_blocks.astype(np.int64)).to(k_storage.device)
+        k_storage[idx] = bf16_tensor(batch.k_used, k_storage.device)
+        v_storage[idx] = bf16_tensor(batch.v_used, v_storage.device)
