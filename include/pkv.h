@@ -186,6 +186,38 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
                    const pkv_host_meta* host_meta, float scale, void* o, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Paged attention for callers that cannot allocate device memory (a process
+ * whose device memory belongs to another framework's caching allocator, code
+ * inside an allocator or stream callback where allocating CUDA calls are not
+ * allowed, or a latency-critical loop that must not take cudaMalloc's
+ * implicit device-wide synchronisation).  The paper has no counterpart to this
+ * entry point.
+ *
+ * Same operation, arguments, results and errors as pkv_paged_attn, without
+ * the workspace: the work lists and split-KV partials live in one static
+ * device array of PKV_STATIC_SCRATCH_BYTES that every GPU loading this
+ * library holds until the process exits.  The call makes no cudaMalloc,
+ * cudaFree or other allocating call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current).  Make that first
+ *     call before any stream capture.
+ *   - A batch whose plan needs more scratch than PKV_STATIC_SCRATCH_BYTES is
+ *     rejected with PKV_EINVAL before anything is launched; use
+ *     pkv_paged_attn with a caller workspace for it.
+ *   - Every call uses the same array, which keeps the last call's contents.
+ *     Nothing in it is read before the same call writes it, so no clearing is
+ *     needed, but calls whose work overlaps on the GPU (on different streams,
+ *     or enqueued while an earlier one still runs elsewhere) race on it:
+ *     serialise them, e.g. on one stream.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int pkv_paged_attn_static(pkv_pool* pool, const void* q, int num_q_heads, const int32_t* q_positions,
+                          const int32_t* block_tables, int max_blocks, const int32_t* ctx_lens,
+                          const int32_t* cu_q_lens, int num_reqs, int num_tokens,
+                          const pkv_host_meta* host_meta, float scale, void* o, float* lse,
+                          void* stream);
+
 /* Statistics of the last plan built on this pool. */
 int pkv_last_plan_stats(const pkv_pool* pool, pkv_plan_stats* out);
 

@@ -12,6 +12,10 @@
 
 using namespace pkv;
 
+namespace pkv {
+int set_last_error(int code, const std::string& msg);
+}
+
 namespace {
 
 thread_local std::string g_err;
@@ -56,6 +60,8 @@ struct ProfRec {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+int pkv::set_last_error(int code, const std::string& msg) { return fail(code, msg); }
 
 struct pkv_pool {
   int num_blocks = 0, block_size = 0, num_kv_heads = 0, head_dim = 0;

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <string>
 #include <vector>
 
 #include "../../include/pkv.h"
@@ -60,6 +61,9 @@ struct Plan {
   uint64_t signature = 0;
   bool valid = false;
 };
+
+// Record `msg` as this thread's pkv_last_error() and return `code`.
+int set_last_error(int code, const std::string& msg);
 
 // Host planner.  Returns PKV_OK or PKV_EINVAL (message in *err).
 int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, const char** err);

@@ -38,7 +38,7 @@ KERNELS = ("append", "split_kv", "tensor_core", "merge")
 # Every symbol include/pkv.h declares (checked by the CPU test suite).
 EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_kv_ptrs", "pkv_append",
-    "pkv_paged_attn_workspace_size", "pkv_paged_attn", "pkv_last_plan_stats",
+    "pkv_paged_attn_workspace_size", "pkv_paged_attn", "pkv_paged_attn_static", "pkv_last_plan_stats",
     "pkv_plan_inspect", "pkv_swap_out", "pkv_swap_in", "pkv_check_device_errors",
     "pkv_profile_enable", "pkv_profile_read", "pkv_device_sm_count", "pkv_last_error",
     "pkv_version",
@@ -106,6 +106,7 @@ def load_library():
                                               ctypes.POINTER(ctypes.c_size_t)],
             "pkv_paged_attn": [P, P, I, P, P, I, P, P, I, I, ctypes.POINTER(pkv_host_meta), F, P, P, P,
                                ctypes.c_size_t, P],
+            "pkv_paged_attn_static": [P, P, I, P, P, I, P, P, I, I, ctypes.POINTER(pkv_host_meta), F, P, P, P],
             "pkv_last_plan_stats": [P, ctypes.POINTER(pkv_plan_stats)],
             "pkv_plan_inspect": [I, I, I, I, I, I, ctypes.POINTER(pkv_host_meta), ctypes.POINTER(pkv_work_desc),
                                  I, ctypes.POINTER(I), ctypes.POINTER(pkv_plan_stats)],
@@ -278,6 +279,38 @@ def pkv_paged_attn(pool: Pool, q, q_positions, block_tables, ctx_lens, cu_q_lens
                               block_tables.shape[1], _ptr(ctx_lens), _ptr(cu_q_lens), R, T, ctypes.byref(meta.c),
                               float(scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                               _stream(stream)))
+    return out, lse
+
+
+PKV_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def pkv_paged_attn_static(pool: Pool, q, q_positions, block_tables, ctx_lens, cu_q_lens, meta: HostMeta,
+                          scale: float, out=None, lse=None, stream=None, want_lse=True):
+    """pkv_paged_attn without a workspace, for callers that cannot allocate device memory.
+
+    The library keeps the work lists and split partials in a static device
+    array of PKV_STATIC_SCRATCH_BYTES; larger batches raise PkvError
+    (PKV_EINVAL).  Calls share that array, so calls that overlap on the GPU
+    race; run them on one stream.  The first call on a device should come
+    before any stream capture.  (This wrapper allocates `out` / `lse` with
+    torch only when they are not given.)
+    """
+    _dev_bf16(q, "q")
+    _dev_i32(q_positions, "q_positions")
+    _dev_i32(block_tables, "block_tables")
+    _dev_i32(ctx_lens, "ctx_lens")
+    _dev_i32(cu_q_lens, "cu_q_lens")
+    T, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _dev_bf16(out, "out")
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    _check(load_library().pkv_paged_attn_static(pool.handle, _ptr(q), Hq, _ptr(q_positions), _ptr(block_tables),
+                                                block_tables.shape[1], _ptr(ctx_lens), _ptr(cu_q_lens),
+                                                ctx_lens.shape[0], T, ctypes.byref(meta.c), float(scale), _ptr(out),
+                                                _ptr(lse), _stream(stream)))
     return out, lse
 
 
