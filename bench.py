@@ -264,10 +264,12 @@ def run_ours(args):
     main = torch.cuda.current_stream()
     side = torch.cuda.Stream(device=dev)
 
-    # Swap-out target: the history blocks of the conversation with the longest context
-    # among requests that are not appended into past their history (read-only this step).
+    # Swap-out target: the cached-history blocks (read-only in this step) of the
+    # conversation with the median context, i.e. one conversation moved to the
+    # CPU tier per step.
     q_lens = np.diff(batch.cu_q_lens)
-    r_swap = int(np.argmax(np.where(q_lens > 0, batch.ctx_lens, -1)))
+    cand = np.flatnonzero(q_lens > 0)
+    r_swap = int(cand[np.argsort(batch.ctx_lens[cand])[len(cand) // 2]])
     first_q = int(batch.q_positions[batch.cu_q_lens[r_swap]:batch.cu_q_lens[r_swap + 1]].min())
     swap_ids = batch.block_tables[r_swap, :max(1, first_q // 16)].astype(np.int32)
     swap_host = torch.empty((len(swap_ids), 2, batch.num_kv_heads, 16, D), dtype=torch.bfloat16).pin_memory()

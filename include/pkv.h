@@ -116,8 +116,8 @@ typedef struct {
 
 /* Accumulated device time per kernel family while profiling is on. */
 typedef struct {
-  int launches[4];          /* 0 append, 1 split-KV, 2 tensor-core, 3 merge */
-  double total_ms[4];
+  int launches[5];          /* 0 append, 1 split-KV, 2 tensor-core, 3 merge, 4 swap */
+  double total_ms[5];
 } pkv_profile;
 
 /* Create a KV block pool.  Allocates the pools (unless caller storage is
@@ -225,10 +225,13 @@ int pkv_last_plan_stats(const pkv_pool* pool, pkv_plan_stats* out);
  * CPU cache tier (Pensieve abstract: multi-tier GPU/CPU caching).  Copy n whole
  * physical blocks (all KV heads, K then V) from the pool to host memory laid
  * out [n][2][Hkv][B][D] (swap out), or back into the pool (swap in).
- * block_ids is a HOST array; host_buf should be pinned (cudaHostAlloc) for
- * the copies to be asynchronous and overlap with kernels on other streams.
- * Runs of consecutive ids are coalesced into one 2-D copy per pool.  Issue on
- * a side stream and record an event to overlap with attention.
+ * block_ids is a HOST array (copied into the launch; no upload).  With pinned
+ * host_buf (cudaHostAlloc / registered, 16-byte aligned) one kernel moves all
+ * blocks directly between HBM and host memory, asynchronously on `stream`;
+ * with pageable memory the library falls back to DMA copies (one 2-D copy
+ * per run of consecutive ids and pool), which the driver may serialise with
+ * the host.  Issue on a side stream and record an event to overlap with
+ * attention.
  * Errors: PKV_EINVAL for an id outside [0, num_blocks) (nothing is copied).
  */
 int pkv_swap_out(pkv_pool* pool, const int32_t* block_ids, int n, void* host_buf, void* stream);

@@ -74,6 +74,12 @@ struct pkv_pool {
   CUtensorMap tmap_v;
   std::mutex mu;
   Plan plan;
+  // Pinned, double-buffered staging for work-list uploads (allocated at
+  // creation; a work list larger than one slot goes through pageable memory).
+  static constexpr size_t kStagingBytes = size_t(4) << 20;
+  uint8_t* pinned[2] = {nullptr, nullptr};
+  cudaEvent_t pinned_done[2] = {nullptr, nullptr};
+  int pinned_slot = 0;
   std::vector<uint8_t> staging;
   // profiling
   bool prof_on = false;
@@ -168,6 +174,10 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
       cudaFree(p->v);
     }
     if (p->d_err) cudaFree(p->d_err);
+    for (int i = 0; i < 2; ++i) {
+      if (p->pinned[i]) cudaFreeHost(p->pinned[i]);
+      if (p->pinned_done[i]) cudaEventDestroy(p->pinned_done[i]);
+    }
     delete p;
     return rc;
   };
@@ -188,6 +198,17 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
   }
   if (cudaMalloc(&p->d_err, sizeof(unsigned)) != cudaSuccess) { p->d_err = nullptr; return cleanup(fail(PKV_ENOMEM, "cudaMalloc error word")); }
   if (cudaMemset(p->d_err, 0, sizeof(unsigned)) != cudaSuccess) return cleanup(fail(PKV_ECUDA, "cudaMemset error word"));
+  for (int i = 0; i < 2; ++i) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&p->pinned[i]), pkv_pool::kStagingBytes, cudaHostAllocDefault) !=
+        cudaSuccess) {
+      p->pinned[i] = nullptr;
+      return cleanup(fail(PKV_ENOMEM, "cudaHostAlloc staging"));
+    }
+    if (cudaEventCreateWithFlags(&p->pinned_done[i], cudaEventDisableTiming) != cudaSuccess) {
+      p->pinned_done[i] = nullptr;
+      return cleanup(fail(PKV_ECUDA, "cudaEventCreate staging"));
+    }
+  }
   int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim);
   if (rc) return cleanup(rc);
   rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim);
@@ -206,6 +227,10 @@ int pkv_pool_destroy(pkv_pool* pool) {
     cudaFree(pool->v);
   }
   cudaFree(pool->d_err);
+  for (int i = 0; i < 2; ++i) {
+    if (pool->pinned[i]) cudaFreeHost(pool->pinned[i]);
+    if (pool->pinned_done[i]) cudaEventDestroy(pool->pinned_done[i]);
+  }
   for (auto& r : pool->pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -285,15 +310,29 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   if (!workspace || workspace_bytes < pl.total) return fail(PKV_EINVAL, "workspace missing or smaller than pkv_paged_attn_workspace_size()");
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(PKV_EINVAL, "workspace must be 256-byte aligned");
 
-  // Upload the work lists (from pageable memory: the host buffer is free on return).
+  // Upload the work lists: through a pinned staging slot (asynchronous; the
+  // slot is reused only after its previous upload has completed), or for an
+  // unusually large list through pageable memory (free again on return).
   const size_t meta_bytes = pl.off_part_o;
-  pool->staging.assign(meta_bytes, 0);
-  if (!pl.decode.empty()) std::memcpy(pool->staging.data() + pl.off_decode, pl.decode.data(), pl.decode.size() * sizeof(WorkItem));
-  if (!pl.tc.empty()) std::memcpy(pool->staging.data() + pl.off_tc, pl.tc.data(), pl.tc.size() * sizeof(WorkItem));
-  if (!pl.merge.empty()) std::memcpy(pool->staging.data() + pl.off_merge, pl.merge.data(), pl.merge.size() * sizeof(MergeItem));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (meta_bytes) PKV_CUDA(cudaMemcpyAsync(ws, pool->staging.data(), meta_bytes, cudaMemcpyHostToDevice, s), "upload work list");
+  if (meta_bytes) {
+    uint8_t* host = nullptr;
+    const bool use_pinned = meta_bytes <= pkv_pool::kStagingBytes;
+    if (use_pinned) {
+      pool->pinned_slot ^= 1;
+      PKV_CUDA(cudaEventSynchronize(pool->pinned_done[pool->pinned_slot]), "staging slot wait");
+      host = pool->pinned[pool->pinned_slot];
+    } else {
+      pool->staging.assign(meta_bytes, 0);
+      host = pool->staging.data();
+    }
+    if (!pl.decode.empty()) std::memcpy(host + pl.off_decode, pl.decode.data(), pl.decode.size() * sizeof(WorkItem));
+    if (!pl.tc.empty()) std::memcpy(host + pl.off_tc, pl.tc.data(), pl.tc.size() * sizeof(WorkItem));
+    if (!pl.merge.empty()) std::memcpy(host + pl.off_merge, pl.merge.data(), pl.merge.size() * sizeof(MergeItem));
+    PKV_CUDA(cudaMemcpyAsync(ws, host, meta_bytes, cudaMemcpyHostToDevice, s), "upload work list");
+    if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], s), "staging slot record");
+  }
 
   AttnArgs a;
   a.pool = pool->view();
@@ -369,6 +408,18 @@ static int swap_impl(pkv_pool* pool, const int32_t* ids, int n, void* host, bool
     if (ids[i] < 0 || ids[i] >= pool->num_blocks) return fail(PKV_EINVAL, "block id outside the pool");
   const size_t blk = static_cast<size_t>(pool->num_kv_heads) * kBlockSize * pool->head_dim * 2;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Pinned (page-locked, device-mapped) host memory: one kernel moves every block.
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, host) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
+      attr.devicePointer != nullptr && (reinterpret_cast<uintptr_t>(attr.devicePointer) & 15u) == 0) {
+    const int rc = timed_launch(pool, 4, stream, [&] {
+      return launch_swap(pool->view(), pool->k, pool->v, attr.devicePointer, ids, n, out, pool->num_sms, stream);
+    });
+    if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "swap kernel launch");
+    return PKV_OK;
+  }
+  cudaGetLastError();   // clear a failed attribute query on pageable memory
+  // Pageable memory: DMA copies, one 2-D copy per run of consecutive block ids and pool.
   uint8_t* h = static_cast<uint8_t*>(host);
   int i = 0;
   while (i < n) {

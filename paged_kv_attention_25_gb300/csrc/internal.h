@@ -28,15 +28,19 @@ struct WorkItem {
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 
-// Log-sum-exp merge of `nsplit` partial results of one (token tile, KV head).
-// Partial row of split s and item row i: part_base + s * (q_count * G) + i.
+// Log-sum-exp merge of `nsplit` partial results of one (token tile, KV head),
+// for rows [row_begin, row_begin + row_count) of that tile (one CTA each).
+// Partial row of split s and tile row i: part_base + s * (q_count * G) + i.
+constexpr int kMergeRowsPerCta = 4;
 struct MergeItem {
   int32_t q_start;
   int32_t q_count;
   int32_t kv_head;
   int32_t nsplit;
   int32_t part_base;
-  int32_t pad[3];
+  int32_t row_begin;
+  int32_t row_count;
+  int32_t pad;
 };
 static_assert(sizeof(MergeItem) == 32, "MergeItem layout");
 
@@ -76,6 +80,15 @@ struct PoolView {
   int num_blocks, num_kv_heads, head_dim;
   unsigned* err;   // device error word
 };
+
+// Block ids of one swap launch, passed by value as a kernel parameter.
+constexpr int kSwapIdsPerLaunch = 2048;
+struct SwapIds {
+  int32_t id[kSwapIdsPerLaunch];
+};
+
+int launch_swap(const PoolView& pool, void* kp, void* vp, void* host_dev, const int32_t* ids, int n, bool to_host,
+                int num_sms, void* stream);
 
 int launch_append(const PoolView& pool, void* kp, void* vp, const int32_t* bt, int max_blocks, int num_reqs,
                   const int32_t* cu_q_lens, const int32_t* positions, const void* k_new, const void* v_new,

@@ -24,7 +24,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a, const Merg
   const int G = a.group;
   const int rows = mi.q_count * G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < rows; r += blockDim.x >> 5) {
+  if (warp < mi.row_count) {
+    const int r = mi.row_begin + warp;
     float mx = -CUDART_INF_F;
     for (int s = lane; s < mi.nsplit; s += 32) mx = fmaxf(mx, a.part_lse[mi.part_base + s * rows + r]);
 #pragma unroll
@@ -34,6 +35,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a, const Merg
     for (int d = 0; d < kDPL; ++d) acc[d] = 0.f;
     float wsum = 0.f;
     if (mx != -CUDART_INF_F) {
+#pragma unroll 4
       for (int s = 0; s < mi.nsplit; ++s) {
         const int pr = mi.part_base + s * rows + r;
         const float w = fast_exp2((a.part_lse[pr] - mx) * kLog2e);
@@ -111,8 +113,8 @@ __global__ void __launch_bounds__(256) append_kernel(uint4* __restrict__ kp, uin
 int launch_merge(const AttnArgs& a, const MergeItem* items, int n_items, void* stream) {
   if (n_items <= 0) return cudaSuccess;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (a.pool.head_dim == 128) merge_kernel<128><<<n_items, 128, 0, s>>>(a, items);
-  else merge_kernel<64><<<n_items, 128, 0, s>>>(a, items);
+  if (a.pool.head_dim == 128) merge_kernel<128><<<n_items, 32 * kMergeRowsPerCta, 0, s>>>(a, items);
+  else merge_kernel<64><<<n_items, 32 * kMergeRowsPerCta, 0, s>>>(a, items);
   return cudaGetLastError();
 }
 

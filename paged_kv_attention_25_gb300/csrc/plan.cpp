@@ -25,9 +25,15 @@ namespace {
 
 constexpr int kDecodeCtasPerSm = 2;
 constexpr int kTcCtasPerSm = 2;
-constexpr int kItemsPerSlot = 8;        // target work items per CTA slot
+// A split-KV partial is one fp32 row per query row (small next to the keys it
+// summarises), so split-KV items are cut to a quarter of the average per-slot
+// load; a tensor-core partial is a 128-row fp32 tile, so those items are cut
+// only when they exceed the average per-slot load (longest-first scheduling
+// then keeps the tail within about one item of the mean).
+constexpr int kDecodeSplitsPerSlot = 4;
+constexpr int kTcSplitsPerSlot = 1;
 constexpr int kMinDecodeChunk = 16;     // blocks (256 keys) per split at least
-constexpr int kMinTcChunk = 4;          // 64-key tiles per split at least
+constexpr int kMinTcChunk = 8;          // 64-key tiles (512 keys) per split at least
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -141,10 +147,11 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   for (const auto& g : dec_groups) dec_blocks += ceil_div(g.kv_len, kBlockSize) * Hkv;
   for (const auto& g : tc_groups) tc_tiles += ceil_div(g.kv_len, kTcKeys) * Hkv;
   const int sms = std::max(1, pp.num_sms);
-  const int64_t dec_chunk = std::max<int64_t>(kMinDecodeChunk,
-                                              ceil_div(dec_blocks, int64_t(sms) * kDecodeCtasPerSm * kItemsPerSlot));
-  const int64_t tc_chunk = std::max<int64_t>(kMinTcChunk,
-                                             ceil_div(tc_tiles, int64_t(sms) * kTcCtasPerSm * kItemsPerSlot));
+  const int64_t dec_chunk = std::max<int64_t>(
+      kMinDecodeChunk, ceil_div(dec_blocks, int64_t(sms) * kDecodeCtasPerSm * kDecodeSplitsPerSlot));
+  const int64_t tc_chunk =
+      std::max<int64_t>(kMinTcChunk, ceil_div(tc_tiles, int64_t(sms) * kTcCtasPerSm * kTcSplitsPerSlot));
+  int merge_groups = 0;
 
   int part_rows = 0;
   auto emit = [&](const QGroup& g, int unit_keys, int64_t chunk_units, std::vector<WorkItem>& out) {
@@ -159,7 +166,9 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
       if (nsplit > 1) {
         base = part_rows;
         part_rows += nsplit * rows;
-        plan->merge.push_back({g.q_start, g.q_count, kvh, nsplit, base, {0, 0, 0}});
+        ++merge_groups;
+        for (int r0 = 0; r0 < rows; r0 += kMergeRowsPerCta)
+          plan->merge.push_back({g.q_start, g.q_count, kvh, nsplit, base, r0, std::min(kMergeRowsPerCta, rows - r0), 0});
       }
       for (int s = 0; s < nsplit; ++s) {
         const int64_t u0 = s * per;
@@ -195,7 +204,7 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   pkv_plan_stats& st = plan->stats;
   st.num_decode_items = static_cast<int>(plan->decode.size());
   st.num_tc_items = static_cast<int>(plan->tc.size());
-  st.num_merge_items = static_cast<int>(plan->merge.size());
+  st.num_merge_items = merge_groups;
   st.num_partial_rows = part_rows;
   std::vector<int> req_kv_dec(R, 0), req_kv_tc(R, 0);
   for (const auto& g : dec_groups) req_kv_dec[g.req] = std::max(req_kv_dec[g.req], g.kv_len);

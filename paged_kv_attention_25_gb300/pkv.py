@@ -33,7 +33,7 @@ PKV_DEVERR_POSITION = 2
 PKV_DEVERR_TIMEOUT = 4
 PKV_DEVERR_INTERNAL = 8
 
-KERNELS = ("append", "split_kv", "tensor_core", "merge")
+KERNELS = ("append", "split_kv", "tensor_core", "merge", "swap")
 
 # Every symbol include/pkv.h declares (checked by the CPU test suite).
 EXPORTED = (
@@ -74,7 +74,7 @@ class pkv_plan_stats(ctypes.Structure):
 
 
 class pkv_profile(ctypes.Structure):
-    _fields_ = [("launches", ctypes.c_int * 4), ("total_ms", ctypes.c_double * 4)]
+    _fields_ = [("launches", ctypes.c_int * 5), ("total_ms", ctypes.c_double * 5)]
 
 
 class pkv_work_desc(ctypes.Structure):
@@ -377,7 +377,7 @@ def pkv_profile_enable(pool: Pool, on: bool = True):
 def pkv_profile_read(pool: Pool, reset: bool = False) -> dict:
     p = pkv_profile()
     _check(load_library().pkv_profile_read(pool.handle, ctypes.byref(p), 1 if reset else 0))
-    return {KERNELS[i]: {"launches": p.launches[i], "total_ms": p.total_ms[i]} for i in range(4)}
+    return {KERNELS[i]: {"launches": p.launches[i], "total_ms": p.total_ms[i]} for i in range(len(KERNELS))}
 
 
 def pkv_device_sm_count() -> int:
