@@ -35,6 +35,7 @@ constexpr int kStagesTc = 2;
 constexpr int kNK = kTcKeys;          // keys per tile (64)
 constexpr uint32_t kTmemCols = 256;   // S0 [0,64), S1 [64,128), O [128, 128+D)
 constexpr uint32_t kColO = 128;
+constexpr float kRescaleLog2 = 8.f;   // lazy O rescale threshold (log2 units)
 
 template <int D>
 struct TcSmem {
@@ -280,7 +281,14 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       float mx = s[0];
 #pragma unroll
       for (int c = 1; c < kNK; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m, mx * sl2);
+      // Lazy rescaling: rows keep their reference max m while the tile max stays
+      // within 2^kRescaleLog2 of it (P then stays <= 2^kRescaleLog2, fine for bf16
+      // and fp32 sums); O and l always share the same reference, so the result
+      // is exact.  The decision is per warp because TMEM loads and stores are
+      // warp-collective.
+      const float m_tile = mx * sl2;
+      const bool grow = __any_sync(0xffffffffu, m_tile > m + kRescaleLog2);
+      const float m_new = grow ? fmaxf(m, m_tile) : m;
       const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
       float rs = 0.f;
 #pragma unroll
@@ -288,21 +296,22 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         s[c] = fast_exp2(fmaf(s[c], sl2, -m_use));
         rs += s[c];
       }
-      const float alpha = fast_exp2(m - m_use);
+      const float alpha = grow ? fast_exp2(m - m_use) : 1.f;
       if (j > 0) {
         // PV of the previous tile must be done before P is overwritten and O rescaled.
         if (!mbar_wait_warp(&bars[kPvDone], (j - 1) & 1, s_abort)) { ok = false; break; }
         tc_fence_after();
-        // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it.
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        if (grow) {
 #pragma unroll
-          for (int c = 0; c < D; c += 16) {
-            float o[16];
+          for (int c = 0; c < D; c += 32) {
+            float o[32];
             tmem_ld16(tmem + lane_base + kColO + c, o);
+            tmem_ld16(tmem + lane_base + kColO + c + 16, o + 16);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] *= alpha;
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
             tmem_st16(tmem + lane_base + kColO + c, o);
+            tmem_st16(tmem + lane_base + kColO + c + 16, o + 16);
           }
           tmem_wait_st();
         }

@@ -299,12 +299,21 @@ def long_skewed_evict(seed: int = 5) -> Batch:
                        pool_factor=1.25, seed=seed)
 
 
+def decode_lognormal_small(seed: int = 3) -> Batch:
+    """The decode-only workload cut to 64 requests (about 3 GB of pool): a
+    profiling-size case whose KV still far exceeds L2."""
+    b = decode_lognormal(seed=seed, num_reqs=64)
+    b.name = "decode_lognormal_small"
+    return b
+
+
 WORKLOADS = {
     "tiny_mixed": tiny_mixed,
     "llama13b_mixed": llama13b_mixed,
     "decode_lognormal": decode_lognormal,
     "llama70b_gqa": llama70b_gqa,
     "long_skewed_evict": long_skewed_evict,
+    "decode_lognormal_small": decode_lognormal_small,
 }
 
 
