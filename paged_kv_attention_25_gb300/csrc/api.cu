@@ -81,6 +81,10 @@ struct pkv_pool {
   cudaEvent_t pinned_done[2] = {nullptr, nullptr};
   int pinned_slot = 0;
   std::vector<uint8_t> staging;
+  // The split-KV kernel runs on `side`, concurrently with the tensor-core
+  // kernel on the caller's stream (fork / join through the two events).
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
   // profiling
   bool prof_on = false;
   std::vector<cudaEvent_t> ev_free;
@@ -178,6 +182,9 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
       if (p->pinned[i]) cudaFreeHost(p->pinned[i]);
       if (p->pinned_done[i]) cudaEventDestroy(p->pinned_done[i]);
     }
+    if (p->side) cudaStreamDestroy(p->side);
+    if (p->fork) cudaEventDestroy(p->fork);
+    if (p->join) cudaEventDestroy(p->join);
     delete p;
     return rc;
   };
@@ -209,6 +216,13 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
       return cleanup(fail(PKV_ECUDA, "cudaEventCreate staging"));
     }
   }
+  if (cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess) {
+    p->side = nullptr;
+    return cleanup(fail(PKV_ECUDA, "cudaStreamCreate"));
+  }
+  if (cudaEventCreateWithFlags(&p->fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->join, cudaEventDisableTiming) != cudaSuccess)
+    return cleanup(fail(PKV_ECUDA, "cudaEventCreate fork/join"));
   int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim);
   if (rc) return cleanup(rc);
   rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim);
@@ -231,6 +245,9 @@ int pkv_pool_destroy(pkv_pool* pool) {
     if (pool->pinned[i]) cudaFreeHost(pool->pinned[i]);
     if (pool->pinned_done[i]) cudaEventDestroy(pool->pinned_done[i]);
   }
+  cudaStreamDestroy(pool->side);
+  cudaEventDestroy(pool->fork);
+  cudaEventDestroy(pool->join);
   for (auto& r : pool->pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -352,15 +369,30 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   const WorkItem* d_dec = reinterpret_cast<const WorkItem*>(ws + pl.off_decode);
   const WorkItem* d_tc = reinterpret_cast<const WorkItem*>(ws + pl.off_tc);
   const MergeItem* d_merge = reinterpret_cast<const MergeItem*>(ws + pl.off_merge);
+  // The two attention kernels are independent (disjoint outputs and workspace
+  // regions): with both present, the split-KV kernel (HBM-bound) runs on the
+  // pool's side stream next to the tensor-core kernel on the caller's stream.
+  const bool fork = !pl.tc.empty() && !pl.decode.empty();
+  void* dec_stream = stream;
+  if (fork) {
+    PKV_CUDA(cudaEventRecord(pool->fork, s), "fork record");
+    PKV_CUDA(cudaStreamWaitEvent(pool->side, pool->fork, 0), "fork wait");
+    dec_stream = pool->side;
+  }
+  if (!pl.decode.empty()) {
+    rc = timed_launch(pool, 1, dec_stream,
+                      [&] { return launch_decode(a, d_dec, static_cast<int>(pl.decode.size()), dec_stream); });
+    if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "split-KV attention launch");
+  }
   if (!pl.tc.empty()) {
     rc = timed_launch(pool, 2, stream, [&] {
       return launch_tc(a, &pool->tmap_k, &pool->tmap_v, d_tc, static_cast<int>(pl.tc.size()), stream);
     });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "tensor-core attention launch");
   }
-  if (!pl.decode.empty()) {
-    rc = timed_launch(pool, 1, stream, [&] { return launch_decode(a, d_dec, static_cast<int>(pl.decode.size()), stream); });
-    if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "split-KV attention launch");
+  if (fork) {
+    PKV_CUDA(cudaEventRecord(pool->join, pool->side), "join record");
+    PKV_CUDA(cudaStreamWaitEvent(s, pool->join, 0), "join wait");
   }
   if (!pl.merge.empty()) {
     rc = timed_launch(pool, 3, stream, [&] { return launch_merge(a, d_merge, static_cast<int>(pl.merge.size()), stream); });
@@ -385,7 +417,8 @@ int pkv_plan_inspect(int num_q_heads, int num_kv_heads, int head_dim, int num_sm
   for (int which = 0; which < 2; ++which)
     for (const WorkItem& w : which == 0 ? plan.decode : plan.tc) {
       if (items && k < max_items)
-        items[k] = pkv_work_desc{which + 1, w.req, w.kv_head, w.q_start, w.q_count, w.kv_start, w.kv_end, w.part};
+        items[k] = pkv_work_desc{which + 1, w.req,    w.kv_head, w.q_start, w.q_count,
+                                 w.kv_start, w.kv_end, w.part,     w.q_count2};
       ++k;
     }
   if (stats) *stats = plan.stats;

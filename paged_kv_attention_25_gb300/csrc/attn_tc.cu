@@ -4,22 +4,28 @@
 // non-contiguous memory" of "Stateful Large Language Model Serving with
 // Pensieve" (abstract), written for sm_103a.
 //
-// One CTA runs one work item: up to 128 query rows (tokens x grouped heads of
-// one KV head, one row per TMEM lane) against a range of key positions in
-// tiles of 64 keys (4 KV blocks).
+// One CTA (one per SM) runs one work item: two query tiles A and B of up to
+// 128 rows each (tokens x grouped heads of one KV head; one row per TMEM
+// lane) of the same request, against a range of key positions in tiles of
+// 128 keys (8 KV blocks).  Every K/V tile is fetched once and used by both
+// query tiles.
 //
-//   warp 4  producer: reads the block table and gathers each block's K and V
-//           (16 keys x 64 dims per TMA box, 128-byte swizzle) into a 2-stage
-//           shared-memory ring with cp.async.bulk.tensor;
-//   warp 5  MMA issuer: S = Q K^T (tcgen05.mma kind::f16, bf16 in, fp32 in
-//           TMEM, double-buffered) and O += P V (P from shared memory);
-//   warps 0-3 softmax: one query row per thread; read S from TMEM, apply the
-//           causal mask on absolute positions, online softmax in fp32 (exp2
-//           with scale*log2 e folded in), rescale O in TMEM when the running
-//           max grows, write P as bf16 into shared memory; epilogue O / l.
+//   warp 8     producer: reads the block table and gathers each block's K and
+//              V (16 keys x 64 dims per TMA box, 128-byte swizzle) into a
+//              shared-memory ring (cp.async.bulk.tensor, mbarrier tracked);
+//   warp 9     MMA issuer (one thread): S_X = Q_X K^T (tcgen05.mma kind::f16,
+//              M=128, N=128, bf16 in, fp32 accumulate in TMEM) and
+//              O_X += P_X V with P_X read from TMEM;
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one query row
+//              per thread; load S from TMEM, causal mask on absolute
+//              positions, online softmax in fp32 (exp2 with scale*log2 e
+//              folded in, lazy rescaling of O), P written back into TMEM as
+//              bf16 over its own S columns; epilogue O / l.
 //
-// Two CTAs fit on one SM (112 KB shared memory, 256 TMEM columns each), so
-// one CTA's softmax overlaps the other's tensor-core work.
+// The MMA issuer staggers the two tiles: PV and the next S of tile A run on
+// the tensor cores while tile B's softmax runs, and the other way round.
+//
+// TMEM: S_A [0,128)  S_B [128,256)  O_A [256, 256+D)  O_B [384, 384+D).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -30,36 +36,44 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kStagesTc = 2;
-constexpr int kNK = kTcKeys;          // keys per tile (64)
-constexpr uint32_t kTmemCols = 256;   // S0 [0,64), S1 [64,128), O [128, 128+D)
-constexpr uint32_t kColO = 128;
-constexpr float kRescaleLog2 = 8.f;   // lazy O rescale threshold (log2 units)
+constexpr int kThreads = 320;
+constexpr int kNK = kTcKeys;            // keys per tile (128)
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.f;     // lazy O rescale threshold (log2 units)
 
 template <int D>
 struct TcSmem {
   static constexpr int kHalves = D / 64;                 // 128-byte-wide column slabs
-  static constexpr int kQ = kTcRows * D * 2;             // [halves][128 rows][64]
-  static constexpr int kKV = kNK * D * 2;                // one stage of K (or V): [halves][64 keys][64]
-  static constexpr int kP = kTcRows * kNK * 2;           // [128 rows][64 keys]
-  static constexpr int kOffK = kQ;
-  static constexpr int kOffV = kOffK + kStagesTc * kKV;
-  static constexpr int kOffP = kOffV + kStagesTc * kKV;
-  static constexpr int kOffBar = kOffP + kP;
-  // barriers: k_full[2] k_empty[2] v_full[2] v_empty[2] q_full s_full[2] p_full pv_done drain
-  static constexpr int kNumBars = 14;
+  static constexpr int kStages = D == 128 ? 2 : 3;
+  static constexpr int kQ = kTcRows * D * 2;             // one query tile: [halves][128 rows][64]
+  static constexpr int kKV = kNK * D * 2;                // one stage of K (or V): [halves][128 keys][64]
+  static constexpr int kOffQ = 0;                        // tile A, then tile B
+  static constexpr int kOffK = 2 * kQ;
+  static constexpr int kOffV = kOffK + kStages * kKV;
+  static constexpr int kOffBar = kOffV + kStages * kKV;
+  static constexpr int kNumBars = 4 * kStages + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kTotal = kOffMisc + 32;
+  static constexpr int kTotal = kOffMisc + 64;
 };
 
-enum Bar { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kQFull = 8, kSFull = 9, kPFull = 11, kPvDone = 12, kDrain = 13 };
+// Barrier slots (the four rings first).
+template <int S>
+struct Bars {
+  static constexpr int kKFull = 0, kKEmpty = S, kVFull = 2 * S, kVEmpty = 3 * S;
+  static constexpr int kQ = 4 * S;          // + tile
+  static constexpr int kS = 4 * S + 2;      // + tile: S ready in TMEM
+  static constexpr int kP = 4 * S + 4;      // + tile: P written (128 arrivals)
+  static constexpr int kPv = 4 * S + 6;     // + tile: PV done
+  static constexpr int kDrain = 4 * S + 8;
+};
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                const WorkItem* __restrict__ items) {
   using S = TcSmem<D>;
+  using B = Bars<S::kStages>;
+  constexpr int kSt = S::kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {   // swizzle atoms need 1024-byte alignment
     if (threadIdx.x == 0) atomicOr(a.pool.err, PKV_DEVERR_INTERNAL);
@@ -70,67 +84,78 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   if (__syncthreads_or((*reinterpret_cast<volatile unsigned*>(a.pool.err) & PKV_DEVERR_TIMEOUT) != 0)) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
-  int* s_info = reinterpret_cast<int*>(smem + S::kOffMisc + 4);   // [0] max pos, [1] min pos
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 12);
+  int* s_pos = reinterpret_cast<int*>(smem + S::kOffMisc + 16);   // max A, min A, max B, min B
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 32);
 
   const WorkItem it = items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
-  const int rows = it.q_count * G;
   const int g = it.kv_head;
   const int Hkv = a.pool.num_kv_heads;
+  const int rows[2] = {it.q_count * G, it.q_count2 * G};
+  const int tok0[2] = {it.q_start, it.q_start + it.q_count};
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[kKFull + i], 1);    // k_full, k_empty
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[kVFull + i], 1);    // v_full, v_empty
-    mbar_init(&bars[kQFull], 128);
-    mbar_init(&bars[kSFull], 1);
-    mbar_init(&bars[kSFull + 1], 1);
-    mbar_init(&bars[kPFull], 128);
-    mbar_init(&bars[kPvDone], 1);
-    mbar_init(&bars[kDrain], 1);
-    s_info[0] = -1;
-    s_info[1] = 0x7fffffff;
+    for (int i = 0; i < 4 * kSt; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&bars[B::kQ], 128);
+    mbar_init(&bars[B::kQ + 1], 128);
+    mbar_init(&bars[B::kS], 1);
+    mbar_init(&bars[B::kS + 1], 1);
+    mbar_init(&bars[B::kP], 128);
+    mbar_init(&bars[B::kP + 1], 128);
+    mbar_init(&bars[B::kPv], 1);
+    mbar_init(&bars[B::kPv + 1], 1);
+    mbar_init(&bars[B::kDrain], 1);
+    s_pos[0] = -1;
+    s_pos[1] = 0x7fffffff;
+    s_pos[2] = -1;
+    s_pos[3] = 0x7fffffff;
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
-  const int row = threadIdx.x;   // meaningful for warps 0-3
+  const int X = (warp >> 2) & 1;            // query tile of a softmax warp (0 = A, 1 = B)
+  const int row = threadIdx.x & 127;        // its row within the tile
   int qpos = -1;
-  if (row < 128 && row < rows) qpos = __ldg(a.q_positions + it.q_start + row / G);
+  if (warp < 8 && row < rows[X]) qpos = __ldg(a.q_positions + tok0[X] + row / G);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (row < 128 && row < rows) {
-    atomicMax(&s_info[0], qpos);
-    atomicMin(&s_info[1], qpos);
+  if (warp < 8 && row < rows[X]) {
+    atomicMax(&s_pos[2 * X], qpos);
+    atomicMin(&s_pos[2 * X + 1], qpos);
   }
   __syncthreads();
   const uint32_t tmem = *s_tmem;
-  const int max_pos = s_info[0];
-  const int min_pos = s_info[1];
-  const int kv_end = min(it.kv_end, max_pos + 1);
-  const int ntiles = kv_end > it.kv_start ? (kv_end - it.kv_start + kNK - 1) / kNK : 0;
+  int ntile[2], min_pos[2];
+  int kv_end = it.kv_start;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int e = min(it.kv_end, s_pos[2 * t] + 1);          // keys tile t can see
+    ntile[t] = e > it.kv_start ? (e - it.kv_start + kNK - 1) / kNK : 0;
+    min_pos[t] = s_pos[2 * t + 1];
+    kv_end = max(kv_end, e);
+  }
+  const int ntiles = max(ntile[0], ntile[1]);
 
-  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sQ = smem_u32(smem + S::kOffQ);
   const uint32_t sK = smem_u32(smem + S::kOffK);
   const uint32_t sV = smem_u32(smem + S::kOffV);
-  const uint32_t sP = smem_u32(smem + S::kOffP);
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
     int j = 0;
     for (; j < ntiles; ++j) {
-      const int st = j % kStagesTc;
-      const uint32_t ph = (j / kStagesTc) & 1;
+      const int st = j % kSt;
+      const uint32_t ph = (j / kSt) & 1;
       const int key0 = it.kv_start + j * kNK;
       const int nkeys = min(kNK, kv_end - key0);
       const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;
@@ -146,88 +171,107 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const int nvalid = __popc(__ballot_sync(0xffffffffu, pb >= 0));
       const uint32_t bytes = static_cast<uint32_t>(nvalid) * S::kHalves * (kBlockSize * 128);
       const int y = (pb * Hkv + g) * kBlockSize;   // row of the 2-D pool view
-      if (!mbar_wait_warp(&bars[kKEmpty + st], ph ^ 1, s_abort)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull + st], bytes);
+      if (!mbar_wait_warp(&bars[B::kKEmpty + st], ph ^ 1, s_abort)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[B::kKFull + st], bytes);
       __syncwarp();
       if (pb >= 0) {
 #pragma unroll
         for (int hf = 0; hf < S::kHalves; ++hf)
           tma_load_2d(smem + S::kOffK + st * S::kKV + hf * (kNK * 128) + lane * (kBlockSize * 128), &tmap_k,
-                      hf * 64, y, &bars[kKFull + st]);
+                      hf * 64, y, &bars[B::kKFull + st]);
       }
-      if (!mbar_wait_warp(&bars[kVEmpty + st], ph ^ 1, s_abort)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[kVFull + st], bytes);
+      if (!mbar_wait_warp(&bars[B::kVEmpty + st], ph ^ 1, s_abort)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[B::kVFull + st], bytes);
       __syncwarp();
       if (pb >= 0) {
 #pragma unroll
         for (int hf = 0; hf < S::kHalves; ++hf)
           tma_load_2d(smem + S::kOffV + st * S::kKV + hf * (kNK * 128) + lane * (kBlockSize * 128), &tmap_v,
-                      hf * 64, y, &bars[kVFull + st]);
+                      hf * 64, y, &bars[B::kVFull + st]);
       }
     }
     if (j < ntiles) {   // gave up: flag it and let copies already issued land
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
       *s_abort = 1;
-      for (int i = max(0, j - kStagesTc); i < j; ++i) {
-        (void)mbar_wait(&bars[kKFull + i % kStagesTc], (i / kStagesTc) & 1, nullptr);
-        (void)mbar_wait(&bars[kVFull + i % kStagesTc], (i / kStagesTc) & 1, nullptr);
+      for (int i = max(0, j - kSt); i < j; ++i) {
+        (void)mbar_wait(&bars[B::kKFull + i % kSt], (i / kSt) & 1, nullptr);
+        (void)mbar_wait(&bars[B::kVFull + i % kSt], (i / kSt) & 1, nullptr);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = make_idesc_bf16(128, kNK, false);
     constexpr uint32_t idesc_o = make_idesc_bf16(128, D, true);
-    bool ok = mbar_wait_warp(&bars[kQFull], 0, s_abort);
-    auto issue_s = [&](int j) -> bool {
-      const int st = j % kStagesTc;
-      if (!mbar_wait_warp(&bars[kKFull + st], (j / kStagesTc) & 1, s_abort)) return false;
+    bool ok = mbar_wait_warp(&bars[B::kQ], 0, s_abort) && mbar_wait_warp(&bars[B::kQ + 1], 0, s_abort);
+    // S_t(j) = Q_t K(j)^T into TMEM columns [128 t, 128 t + 128).  The previous
+    // PV of tile t read P_t from those columns, so it must have completed.
+    auto issue_s = [&](int t, int j) -> bool {
+      const int st = j % kSt;
+      if (!mbar_wait_warp(&bars[B::kKFull + st], (j / kSt) & 1, s_abort)) return false;
+      if (j > 0 && !mbar_wait_warp(&bars[B::kPv + t], (j - 1) & 1, s_abort)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t d_tmem = tmem + (j & 1) * kNK;
+        const uint32_t q_base = sQ + t * S::kQ;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int hf = ks / 4, kk = ks % 4;
-          const uint64_t ad = make_sdesc_sw128(sQ + hf * (kTcRows * 128) + kk * 32, 16, 1024);
+          const uint64_t ad = make_sdesc_sw128(q_base + hf * (kTcRows * 128) + kk * 32, 16, 1024);
           const uint64_t bd = make_sdesc_sw128(sK + st * S::kKV + hf * (kNK * 128) + kk * 32, 16, 1024);
-          tc_mma(d_tmem, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+          tc_mma(tmem + t * 128, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&bars[kSFull + (j & 1)]);
-        tc_commit(&bars[kKEmpty + st]);
+        tc_commit(&bars[B::kS + t]);
       }
       __syncwarp();
       return true;
     };
-    if (ok && ntiles > 0) ok = issue_s(0);
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const int st = j % kStagesTc;
-      if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
-      if (!mbar_wait_warp(&bars[kPFull], j & 1, s_abort)) { ok = false; break; }
-      if (!mbar_wait_warp(&bars[kVFull + st], (j / kStagesTc) & 1, s_abort)) { ok = false; break; }
+    // O_t += P_t(j) V(j), P_t read from TMEM (bf16 packed in the first 64 columns of S_t).
+    auto issue_pv = [&](int t, int j) -> bool {
+      const int st = j % kSt;
+      if (!mbar_wait_warp(&bars[B::kP + t], j & 1, s_abort)) return false;
+      if (!mbar_wait_warp(&bars[B::kVFull + st], (j / kSt) & 1, s_abort)) return false;
       tc_fence_after();
-      const int key0 = it.kv_start + j * kNK;
-      const int nkeys = min(kNK, kv_end - key0);
-      if (nkeys < kNK) {
-        // Keys past the item's end: zero their V rows so that 0 * garbage cannot
-        // produce NaN in the tensor core (the pool's tail slots are not ours).
-        uint8_t* vst = smem + S::kOffV + st * S::kKV;
-        for (int idx = lane; idx < (kNK - nkeys) * S::kHalves * 8; idx += 32) {
-          const int hf = idx / ((kNK - nkeys) * 8);
-          const int rem = idx % ((kNK - nkeys) * 8);
-          const int key = nkeys + rem / 8, chunk = rem % 8;
-          *reinterpret_cast<uint4*>(vst + hf * (kNK * 128) + key * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
       if (lane == 0) {
 #pragma unroll
         for (int ks = 0; ks < kNK / 16; ++ks) {
-          const uint64_t ad = make_sdesc_sw128(sP + ks * 32, 16, 1024);
           const uint64_t bd = make_sdesc_sw128(sV + st * S::kKV + ks * (16 * 128), kNK * 128, 1024);
-          tc_mma(tmem + kColO, ad, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
         }
-        tc_commit(&bars[kPvDone]);
-        tc_commit(&bars[kVEmpty + st]);
+        tc_commit(&bars[B::kPv + t]);
+      }
+      __syncwarp();
+      return true;
+    };
+    // Keys past the item's end in its last tile: zero their V rows so that
+    // 0 * garbage cannot produce NaN in the tensor core.
+    auto zero_v_tail = [&](int j) -> bool {
+      const int st = j % kSt;
+      const int nkeys = min(kNK, kv_end - (it.kv_start + j * kNK));
+      if (nkeys >= kNK) return true;
+      if (!mbar_wait_warp(&bars[B::kVFull + st], (j / kSt) & 1, s_abort)) return false;
+      uint8_t* vst = smem + S::kOffV + st * S::kKV;
+      for (int idx = lane; idx < (kNK - nkeys) * S::kHalves * 8; idx += 32) {
+        const int hf = idx / ((kNK - nkeys) * 8);
+        const int rem = idx % ((kNK - nkeys) * 8);
+        const int key = nkeys + rem / 8, chunk = rem % 8;
+        *reinterpret_cast<uint4*>(vst + hf * (kNK * 128) + key * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      return true;
+    };
+    if (ok && ntile[0] > 0) ok = issue_s(0, 0);
+    if (ok && ntile[1] > 0) ok = issue_s(1, 0);
+    if (ok && ntiles > 0 && lane == 0) tc_commit(&bars[B::kKEmpty]);
+    __syncwarp();
+    for (int j = 0; ok && j < ntiles; ++j) {
+      if (j == ntiles - 1 && !(ok = zero_v_tail(j))) break;
+      if (j < ntile[0] && !(ok = issue_pv(0, j))) break;
+      if (j + 1 < ntile[0] && !(ok = issue_s(0, j + 1))) break;
+      if (j < ntile[1] && !(ok = issue_pv(1, j))) break;
+      if (j + 1 < ntile[1] && !(ok = issue_s(1, j + 1))) break;
+      if (lane == 0) {
+        if (j + 1 < ntiles) tc_commit(&bars[B::kKEmpty + (j + 1) % kSt]);
+        tc_commit(&bars[B::kVEmpty + j % kSt]);
       }
       __syncwarp();
     }
@@ -236,42 +280,46 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       *s_abort = 1;
     }
     // Drain: every MMA this thread issued has completed before TMEM is released.
-    if (lane == 0) tc_commit(&bars[kDrain]);
+    if (lane == 0) tc_commit(&bars[B::kDrain]);
     __syncwarp();
-    (void)mbar_wait_warp(&bars[kDrain], 0, nullptr);
+    (void)mbar_wait_warp(&bars[B::kDrain], 0, nullptr);
   } else {
-    // ------------------------------------------------------------ softmax / epilogue
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    // Q tile: row `row` = (token q_start + row / G, head g*G + row % G), swizzled K-major.
+    // ------------------------------------------------------------ softmax / epilogue of tile X
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t colS = X * 128, colO = 256 + X * 128;
+    const int nrows = rows[X];
+    const int nt = ntile[X];
+    // Q tile: row `row` = (token tok0[X] + row / G, head g*G + row % G), swizzled K-major.
     {
       const uint4* src = nullptr;
-      if (row < rows) {
-        const int t = it.q_start + row / G;
+      if (row < nrows) {
+        const int t = tok0[X] + row / G;
         const int h = g * G + row % G;
         src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
                                              (static_cast<int64_t>(t) * a.num_q_heads + h) * D);
       }
+      uint8_t* qt = smem + S::kOffQ + X * S::kQ;
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
         const int hf = c / 8, cc = c % 8;
-        *reinterpret_cast<uint4*>(smem + hf * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) * 16)) = v;
+        *reinterpret_cast<uint4*>(qt + hf * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) * 16)) = v;
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars[kQFull]);
+      mbar_arrive(&bars[B::kQ + X]);
     }
     const float sl2 = a.scale_log2;
     float m = -CUDART_INF_F, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
+    for (int j = 0; j < nt; ++j) {
       const int key0 = it.kv_start + j * kNK;
-      if (!mbar_wait_warp(&bars[kSFull + (j & 1)], (j >> 1) & 1, s_abort)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars[B::kS + X], j & 1, s_abort)) { ok = false; break; }
       tc_fence_after();
       float s[kNK];
 #pragma unroll
-      for (int c = 0; c < kNK; c += 16) tmem_ld16(tmem + lane_base + (j & 1) * kNK + c, s + c);
+      for (int c = 0; c < kNK; c += 16) tmem_ld16(tmem + lane_base + colS + c, s + c);
       tmem_wait_ld();
-      if (key0 + kNK - 1 > min_pos || key0 + kNK > kv_end) {
+      if (key0 + kNK - 1 > min_pos[X] || key0 + kNK > kv_end) {
 #pragma unroll
         for (int c = 0; c < kNK; ++c) {
           const int key = key0 + c;
@@ -291,71 +339,64 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const float m_new = grow ? fmaxf(m, m_tile) : m;
       const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
       float rs = 0.f;
+      uint32_t pk[kNK / 2];
 #pragma unroll
-      for (int c = 0; c < kNK; ++c) {
-        s[c] = fast_exp2(fmaf(s[c], sl2, -m_use));
-        rs += s[c];
+      for (int c = 0; c < kNK; c += 2) {
+        const float p0 = fast_exp2(fmaf(s[c], sl2, -m_use));
+        const float p1 = fast_exp2(fmaf(s[c + 1], sl2, -m_use));
+        rs += p0 + p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
       }
       const float alpha = grow ? fast_exp2(m - m_use) : 1.f;
-      if (j > 0) {
-        // PV of the previous tile must be done before P is overwritten and O rescaled.
-        if (!mbar_wait_warp(&bars[kPvDone], (j - 1) & 1, s_abort)) { ok = false; break; }
-        tc_fence_after();
-        if (grow) {
+      // The MMA issuer started S(j) only after PV(j-1) completed, so P may be
+      // written over S(j) and O rescaled right away.
 #pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            float o[32];
-            tmem_ld16(tmem + lane_base + kColO + c, o);
-            tmem_ld16(tmem + lane_base + kColO + c + 16, o + 16);
-            tmem_wait_ld();
+      for (int c = 0; c < kNK / 2; c += 16)
+        tmem_st16(tmem + lane_base + colS + c, reinterpret_cast<const float*>(pk + c));
+      if (grow && j > 0) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st16(tmem + lane_base + kColO + c, o);
-            tmem_st16(tmem + lane_base + kColO + c + 16, o + 16);
-          }
-          tmem_wait_st();
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          tmem_ld16(tmem + lane_base + colO + c, o);
+          tmem_ld16(tmem + lane_base + colO + c + 16, o + 16);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st16(tmem + lane_base + colO + c, o);
+          tmem_st16(tmem + lane_base + colO + c + 16, o + 16);
         }
       }
       l = l * alpha + rs;
       m = m_new;
-      // P row (bf16, K-major, 128-byte swizzle).
-#pragma unroll
-      for (int cc = 0; cc < kNK / 8; ++cc) {
-        uint4 v;
-        v.x = pack_bf16x2(s[cc * 8 + 0], s[cc * 8 + 1]);
-        v.y = pack_bf16x2(s[cc * 8 + 2], s[cc * 8 + 3]);
-        v.z = pack_bf16x2(s[cc * 8 + 4], s[cc * 8 + 5]);
-        v.w = pack_bf16x2(s[cc * 8 + 6], s[cc * 8 + 7]);
-        *reinterpret_cast<uint4*>(smem + S::kOffP + row * 128 + ((cc ^ (row & 7)) * 16)) = v;
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars[kPFull]);
+      mbar_arrive(&bars[B::kP + X]);
     }
-    if (ok && ntiles > 0) {
-      if (!mbar_wait_warp(&bars[kPvDone], (ntiles - 1) & 1, s_abort)) ok = false;
+    if (ok && nt > 0) {
+      if (!mbar_wait_warp(&bars[B::kPv + X], (nt - 1) & 1, s_abort)) ok = false;
       tc_fence_after();
     }
     if (!ok) {
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
       *s_abort = 1;
     }
-    // Epilogue.  `ok` is uniform across the four warps; the TMEM loads are
-    // executed by every thread, only the stores depend on the row being valid.
+    // Epilogue.  `ok` is uniform within a warp; the TMEM loads are executed by
+    // every thread of the warp, only the stores depend on the row being valid.
     if (ok) {
       constexpr float kLn2 = 0.69314718055994530942f;
-      const bool valid = row < rows;
+      const bool valid = row < nrows;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse = l > 0.f ? (m + fast_log2(l)) * kLn2 : -CUDART_INF_F;
-      const int t = it.q_start + (valid ? row / G : 0);
+      const int t = tok0[X] + (valid ? row / G : 0);
       const int h = g * G + row % G;
+      const int prow = it.part + (X == 0 ? row : rows[0] + row);
       uint4* dst_o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D);
-      float4* dst_p = it.part >= 0 ? reinterpret_cast<float4*>(a.part_o + static_cast<int64_t>(it.part + row) * D) : nullptr;
+      float4* dst_p = it.part >= 0 ? reinterpret_cast<float4*>(a.part_o + static_cast<int64_t>(prow) * D) : nullptr;
 #pragma unroll
       for (int c = 0; c < D; c += 16) {
         float o[16];
-        if (ntiles > 0) {
-          tmem_ld16(tmem + lane_base + kColO + c, o);
+        if (nt > 0) {
+          tmem_ld16(tmem + lane_base + colO + c, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -381,7 +422,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         if (it.part < 0) {
           if (a.lse) a.lse[static_cast<int64_t>(t) * a.num_q_heads + h] = lse;
         } else {
-          a.part_lse[it.part + row] = lse;
+          a.part_lse[prow] = lse;
         }
       }
     }
@@ -389,7 +430,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
