@@ -315,20 +315,34 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const int key0 = it.kv_start + j * kNK;
       if (!mbar_wait_warp(&bars[B::kS + X], j & 1, s_abort)) { ok = false; break; }
       tc_fence_after();
-      float s[kNK];
+      // Two passes over the S row in halves of 64 columns (TMEM reads are cheap;
+      // registers are not): pass 1 finds the row max, pass 2 exponentiates,
+      // sums and writes P (bf16) over the S columns it has consumed.  Max and
+      // sum use 8 independent partials: with two softmax warps per SM
+      // sub-partition, one long dependency chain would leave them latency-bound.
+      const bool need_mask = key0 + kNK - 1 > min_pos[X] || key0 + kNK > kv_end;
+      constexpr int kH = kNK / 2;
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < kNK; c += 16) tmem_ld16(tmem + lane_base + colS + c, s + c);
-      tmem_wait_ld();
-      if (key0 + kNK - 1 > min_pos[X] || key0 + kNK > kv_end) {
+      for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
 #pragma unroll
-        for (int c = 0; c < kNK; ++c) {
-          const int key = key0 + c;
-          if (key > qpos || key >= kv_end) s[c] = -CUDART_INF_F;
+      for (int half = 0; half < 2; ++half) {
+        float s[kH];
+#pragma unroll
+        for (int c = 0; c < kH; c += 16) tmem_ld16(tmem + lane_base + colS + half * kH + c, s + c);
+        tmem_wait_ld();
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < kH; ++c) {
+            const int key = key0 + half * kH + c;
+            if (key > qpos || key >= kv_end) s[c] = -CUDART_INF_F;
+          }
         }
-      }
-      float mx = s[0];
 #pragma unroll
-      for (int c = 1; c < kNK; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < kH; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // Lazy rescaling: rows keep their reference max m while the tile max stays
       // within 2^kRescaleLog2 of it (P then stays <= 2^kRescaleLog2, fine for bf16
       // and fp32 sums); O and l always share the same reference, so the result
@@ -338,21 +352,37 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const bool grow = __any_sync(0xffffffffu, m_tile > m + kRescaleLog2);
       const float m_new = grow ? fmaxf(m, m_tile) : m;
       const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-      float rs = 0.f;
-      uint32_t pk[kNK / 2];
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kNK; c += 2) {
-        const float p0 = fast_exp2(fmaf(s[c], sl2, -m_use));
-        const float p1 = fast_exp2(fmaf(s[c + 1], sl2, -m_use));
-        rs += p0 + p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
+      for (int half = 0; half < 2; ++half) {
+        float s[kH];
+#pragma unroll
+        for (int c = 0; c < kH; c += 16) tmem_ld16(tmem + lane_base + colS + half * kH + c, s + c);
+        tmem_wait_ld();
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < kH; ++c) {
+            const int key = key0 + half * kH + c;
+            if (key > qpos || key >= kv_end) s[c] = -CUDART_INF_F;
+          }
+        }
+        uint32_t pk[kH / 2];
+#pragma unroll
+        for (int c = 0; c < kH; c += 2) {
+          const float p0 = fast_exp2(fmaf(s[c], sl2, -m_use));
+          const float p1 = fast_exp2(fmaf(s[c + 1], sl2, -m_use));
+          rs8[(c >> 1) & 7] += p0 + p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
+        // P columns [half*32, half*32+32) lie inside S columns already read.
+#pragma unroll
+        for (int c = 0; c < kH / 2; c += 16)
+          tmem_st16(tmem + lane_base + colS + half * (kH / 2) + c, reinterpret_cast<const float*>(pk + c));
       }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       const float alpha = grow ? fast_exp2(m - m_use) : 1.f;
-      // The MMA issuer started S(j) only after PV(j-1) completed, so P may be
-      // written over S(j) and O rescaled right away.
-#pragma unroll
-      for (int c = 0; c < kNK / 2; c += 16)
-        tmem_st16(tmem + lane_base + colS + c, reinterpret_cast<const float*>(pk + c));
+      // The MMA issuer started S(j) only after PV(j-1) completed, so O may be
+      // rescaled right away.
       if (grow && j > 0) {
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
