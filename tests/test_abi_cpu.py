@@ -69,11 +69,7 @@ def check_plan(batch, num_sms=148):
     # Group items by (kernel, request, kv head, q_start, q_count).
     groups = {}
     for it in items:
-        key = (int(it["req"]), int(it["kv_head"]), int(it["q_start"]), int(it["q_count"]) + int(it["q_count2"]))
-        if int(it["kernel"]) == 1:
-            assert int(it["q_count2"]) == 0
-        else:
-            assert int(it["q_count"]) * G <= 128 and int(it["q_count2"]) * G <= 128
+        key = (int(it["req"]), int(it["kv_head"]), int(it["q_start"]), int(it["q_count"]))
         groups.setdefault(key, []).append(it)
     covered = np.zeros((batch.num_tokens, Hkv), np.int32)
     part_rows = []
@@ -86,7 +82,7 @@ def check_plan(batch, num_sms=148):
         if kern == 1:
             assert rows <= 4
         else:
-            assert rows <= 256
+            assert rows <= 128
         a, b = batch.cu_q_lens[r], batch.cu_q_lens[r + 1]
         assert a <= q0 and q0 + qc <= b
         covered[q0:q0 + qc, g] += 1
