@@ -163,22 +163,38 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
-    int j = 0;
-    for (; j < nt; ++j) {
-      const int st = j % kSt;
-      const uint32_t ph = (j / kSt) & 1;
-      const int key0 = it.kv_start + j * kNK;
-      const int nkeys = min(kNK, kv_end - key0);
-      const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;
+    // Block ids are read a window ahead: lane l holds the id of block
+    // (first block of the item) + 32 w + l, i.e. windows of four key tiles, and
+    // the next window is already in flight while the current one is used.
+    const int blk_first = it.kv_start / kBlockSize;
+    const int blk_end = (kv_end + kBlockSize - 1) / kBlockSize;
+    auto load_window = [&](int w) -> int {
+      const int col = blk_first + w * 32 + lane;
       int pb = -1;
-      if (lane < nblk) {
-        const int col = key0 / kBlockSize + lane;
+      if (col < blk_end) {
         pb = col < a.max_blocks ? __ldg(bt_row + col) : -1;
         if (pb < 0 || pb >= a.pool.num_blocks) {
           atomicOr(a.pool.err, PKV_DEVERR_BLOCK_ID);
           pb = -1;
         }
       }
+      return pb;
+    };
+    int ids_cur = load_window(0), ids_next = load_window(1), win = 0;
+    int j = 0;
+    for (; j < nt; ++j) {
+      const int st = j % kSt;
+      const uint32_t ph = (j / kSt) & 1;
+      if ((j >> 2) != win) {
+        win = j >> 2;
+        ids_cur = ids_next;
+        ids_next = load_window(win + 1);
+      }
+      const int key0 = it.kv_start + j * kNK;
+      const int nkeys = min(kNK, kv_end - key0);
+      const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;
+      int pb = __shfl_sync(0xffffffffu, ids_cur, (j & 3) * 8 + (lane & 7));
+      if (lane >= nblk) pb = -1;
       const int nvalid = __popc(__ballot_sync(0xffffffffu, pb >= 0));
       const uint32_t bytes = static_cast<uint32_t>(nvalid) * S::kHalves * (kBlockSize * 128);
       const int y = (pb * Hkv + g) * kBlockSize;   // row of the 2-D pool view
