@@ -250,9 +250,11 @@ int pkv_profile_enable(pkv_pool* pool, int on);
 int pkv_profile_read(pkv_pool* pool, pkv_profile* out, int reset);
 
 /* One planned work item, as reported by pkv_plan_inspect.  Rows of an item
- * are (token q_start + i, query head kv_head*G + j), i < q_count, j < G. */
+ * are (token q_start + i, query head kv_head*G + j), i < q_count + q_count2,
+ * j < G.  A tensor-core item holds two query tiles of at most 128 rows each:
+ * q_count tokens, then q_count2 tokens (0 if there is one tile). */
 typedef struct {
-  int32_t kernel;    /* 1: split-KV (CUDA cores), 2: tensor-core tile */
+  int32_t kernel;    /* 1: split-KV (CUDA cores), 2: tensor-core tile pair */
   int32_t req;
   int32_t kv_head;
   int32_t q_start;
@@ -260,6 +262,7 @@ typedef struct {
   int32_t kv_start;  /* key positions [kv_start, kv_end) */
   int32_t kv_end;
   int32_t part;      /* -1: writes O/LSE directly; else first partial row */
+  int32_t q_count2;
 } pkv_work_desc;
 
 /* Plan a batch on the host only (no device needed) and copy out its work

@@ -12,19 +12,22 @@ namespace pkv {
 constexpr int kBlockSize = 16;        // tokens per KV block
 constexpr int kDecodeMaxRows = 4;     // query rows (tokens x group) per split-KV item
 constexpr int kTcRows = 128;          // query rows per tensor-core tile (TMEM lanes)
-constexpr int kTcKeys = 128;          // keys per tensor-core KV tile (8 blocks)
+constexpr int kTcKeys = 64;           // keys per tensor-core KV tile (4 blocks)
 
 // One CTA of work.  Rows of an item are (token q_start + i, query head
-// kv_head*G + j) for i < q_count, j < G, numbered i*G + j.
+// kv_head*G + j) for i < q_count + q_count2, j < G, numbered i*G + j.  A
+// tensor-core item holds two query tiles: tokens [q_start, q_start+q_count)
+// and the q_count2 tokens after them (0 when there is one tile); a split-KV
+// item has q_count2 = 0.
 struct WorkItem {
   int32_t req;
   int32_t kv_head;
   int32_t q_start;   // first token (index into [0, num_tokens))
-  int32_t q_count;   // tokens in the item
+  int32_t q_count;   // tokens in the (first) tile
   int32_t kv_start;  // first key position (multiple of the kernel's key tile)
   int32_t kv_end;    // one past the last key position this item may read
   int32_t part;      // -1: write O / LSE directly; else first fp32 partial row
-  int32_t pad;
+  int32_t q_count2;  // tokens in the second tensor-core tile
 };
 static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
 

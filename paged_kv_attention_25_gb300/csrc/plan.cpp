@@ -33,7 +33,7 @@ constexpr int kTcCtasPerSm = 1;
 constexpr int kDecodeSplitsPerSlot = 4;
 constexpr int kTcSplitsPerSlot = 1;
 constexpr int kMinDecodeChunk = 16;     // blocks (256 keys) per split at least
-constexpr int kMinTcChunk = 4;          // 128-key tiles (512 keys) per split at least
+constexpr int kMinTcChunk = 8;          // 64-key tiles (512 keys) per split at least
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -42,8 +42,9 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 struct QGroup {
   int req;
   int q_start;
-  int q_count;
-  int kv_len;   // keys the group can see: min(ctx, max position + 1)
+  int q_count;   // tokens (of the first tile, for a tensor-core pair)
+  int kv_len;    // keys the group can see: min(ctx, max position + 1)
+  int q_count2;  // tokens of the second tensor-core tile (0: none)
 };
 
 }  // namespace
@@ -124,11 +125,12 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
       return std::min(static_cast<int>(ctx[r]), mx + 1);
     };
     if (n * G <= kDecodeMaxRows) {
-      dec_groups.push_back({r, cu[r], n, kv_len_of(cu[r], n)});
+      dec_groups.push_back({r, cu[r], n, kv_len_of(cu[r], n), 0});
       continue;
     }
     int t = cu[r];
     const int end = cu[r + 1];
+    std::vector<std::pair<int, int>> tiles;   // (first token, tokens)
     while (t < end) {
       int c = 1;
       // A tile holds consecutive tokens; with known positions it also stops at
@@ -138,15 +140,21 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
         if (pos && pos[t + c] != pos[t + c - 1] + 1) break;
         ++c;
       }
-      tc_groups.push_back({r, t, c, kv_len_of(t, c)});
+      tiles.push_back({t, c});
       t += c;
+    }
+    // Two consecutive tiles of a request share one CTA and every K/V tile it loads.
+    for (size_t i = 0; i < tiles.size(); i += 2) {
+      const int c0 = tiles[i].second;
+      const int c1 = i + 1 < tiles.size() ? tiles[i + 1].second : 0;
+      tc_groups.push_back({r, tiles[i].first, c0, kv_len_of(tiles[i].first, c0 + c1), c1});
     }
   }
 
   // 2. Split sizes from the total work of each kernel.
   int64_t dec_blocks = 0, tc_tiles = 0;
   for (const auto& g : dec_groups) dec_blocks += ceil_div(g.kv_len, kBlockSize) * Hkv;
-  for (const auto& g : tc_groups) tc_tiles += ceil_div(g.kv_len, kTcKeys) * Hkv;
+  for (const auto& g : tc_groups) tc_tiles += ceil_div(g.kv_len, kTcKeys) * Hkv;   // per tile pair
   const int sms = std::max(1, pp.num_sms);
   const int64_t dec_chunk = std::max<int64_t>(
       kMinDecodeChunk, ceil_div(dec_blocks, int64_t(sms) * kDecodeCtasPerSm * kDecodeSplitsPerSlot));
@@ -156,7 +164,7 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
 
   int part_rows = 0;
   auto emit = [&](const QGroup& g, int unit_keys, int64_t chunk_units, std::vector<WorkItem>& out) {
-    const int rows = g.q_count * G;
+    const int rows = (g.q_count + g.q_count2) * G;
     const int64_t units = ceil_div(g.kv_len, unit_keys);
     int nsplit = static_cast<int>(std::max<int64_t>(1, ceil_div(units, chunk_units)));
     // Even split in whole units; no split is left empty.
@@ -169,7 +177,8 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
         part_rows += nsplit * rows;
         ++merge_groups;
         for (int r0 = 0; r0 < rows; r0 += kMergeRowsPerCta)
-          plan->merge.push_back({g.q_start, g.q_count, kvh, nsplit, base, r0, std::min(kMergeRowsPerCta, rows - r0), 0});
+          plan->merge.push_back(
+            {g.q_start, g.q_count + g.q_count2, kvh, nsplit, base, r0, std::min(kMergeRowsPerCta, rows - r0), 0});
       }
       for (int s = 0; s < nsplit; ++s) {
         const int64_t u0 = s * per;
@@ -182,7 +191,7 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
         w.kv_start = static_cast<int32_t>(u0 * unit_keys);
         w.kv_end = static_cast<int32_t>(std::min<int64_t>(g.kv_len, u1 * unit_keys));
         w.part = nsplit > 1 ? base + s * rows : -1;
-        w.pad = 0;
+        w.q_count2 = g.q_count2;
         if (w.kv_end <= w.kv_start) {   // cannot happen with an even split; keep a valid empty item
           w.kv_end = w.kv_start;
         }
@@ -218,7 +227,7 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   auto row_flops = [&](const std::vector<QGroup>& gs) {
     int64_t f = 0;
     for (const auto& g : gs)
-      for (int t = g.q_start; t < g.q_start + g.q_count; ++t) {
+      for (int t = g.q_start; t < g.q_start + g.q_count + g.q_count2; ++t) {
         const int64_t vis = pos ? pos[t] + 1 : g.kv_len;
         f += int64_t(4) * D * vis * Hq;
       }
@@ -228,7 +237,7 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   st.tc_flops = row_flops(tc_groups);
   auto io_bytes = [&](const std::vector<QGroup>& gs) {
     int64_t toks = 0;
-    for (const auto& g : gs) toks += g.q_count;
+    for (const auto& g : gs) toks += g.q_count + g.q_count2;
     return toks * Hq * (int64_t(D) * 2 * 2 + 4);   // Q in, O out (bf16), LSE out (fp32)
   };
   st.decode_io_bytes = io_bytes(dec_groups);

@@ -79,7 +79,7 @@ class pkv_profile(ctypes.Structure):
 
 class pkv_work_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("kernel", "req", "kv_head", "q_start", "q_count", "kv_start", "kv_end", "part")]
+                ("kernel", "req", "kv_head", "q_start", "q_count", "kv_start", "kv_end", "part", "q_count2")]
 
 
 _lib = None

@@ -69,7 +69,11 @@ def check_plan(batch, num_sms=148):
     # Group items by (kernel, request, kv head, q_start, q_count).
     groups = {}
     for it in items:
-        key = (int(it["req"]), int(it["kv_head"]), int(it["q_start"]), int(it["q_count"]))
+        key = (int(it["req"]), int(it["kv_head"]), int(it["q_start"]), int(it["q_count"]) + int(it["q_count2"]))
+        if int(it["kernel"]) == 1:
+            assert int(it["q_count2"]) == 0
+        else:
+            assert int(it["q_count"]) * G <= 128 and int(it["q_count2"]) * G <= 128
         groups.setdefault(key, []).append(it)
     covered = np.zeros((batch.num_tokens, Hkv), np.int32)
     part_rows = []
@@ -82,13 +86,13 @@ def check_plan(batch, num_sms=148):
         if kern == 1:
             assert rows <= 4
         else:
-            assert rows <= 128
+            assert rows <= 256
         a, b = batch.cu_q_lens[r], batch.cu_q_lens[r + 1]
         assert a <= q0 and q0 + qc <= b
         covered[q0:q0 + qc, g] += 1
         kv_len = min(int(batch.ctx_lens[r]), int(batch.q_positions[q0:q0 + qc].max()) + 1)
         its = sorted(its, key=lambda i: int(i["kv_start"]))
-        unit = 16 if kern == 1 else 128
+        unit = 16 if kern == 1 else 64
         # splits tile [0, kv_len) exactly, in whole units
         assert int(its[0]["kv_start"]) == 0 and int(its[-1]["kv_end"]) == kv_len
         for x, y in zip(its[:-1], its[1:]):
