@@ -15,9 +15,10 @@
 //   warp 8     producer: reads the block table a window ahead and gathers each
 //              block's K and V (16 keys x 64 dims per TMA box, 128-byte
 //              swizzle) into a shared-memory ring (cp.async.bulk.tensor);
-//   warp 9     MMA issuer (one thread): S_t = Q_t K^T (tcgen05.mma kind::f16,
-//              M=128, N=64, bf16 in, fp32 accumulate in TMEM) and
-//              O_t += P_t V with P_t read from TMEM;
+//   warps 9,10 MMA issuers, one per query tile (a tcgen05.mma costs its
+//              issuing thread about a hundred cycles, and two issuing threads
+//              overlap): S_t = Q_t K^T (kind::f16, M=128, N=64, bf16 in, fp32
+//              accumulate in TMEM) and O_t += P_t V with P_t read from TMEM;
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one query row
 //              per thread.  Each thread loads its S row into registers and at
 //              once releases the S columns (so the next S MMA overlaps the rest
@@ -39,7 +40,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kNK = kTcKeys;            // keys per tile (64)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
@@ -55,7 +56,7 @@ struct TcSmem {
   static constexpr int kOffK = 2 * kQ;
   static constexpr int kOffV = kOffK + kStages * kKV;
   static constexpr int kOffBar = kOffV + kStages * kKV;
-  static constexpr int kNumBars = 4 * kStages + 11;
+  static constexpr int kNumBars = 4 * kStages + 13;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kTotal = kOffMisc + 64;
 };
@@ -68,7 +69,8 @@ struct Bars {
   static constexpr int kSFree = 4 * S + 4;  // + tile: S read into registers (128 arrivals)
   static constexpr int kP = 4 * S + 6;      // + tile: P written (128 arrivals)
   static constexpr int kPv = 4 * S + 8;     // + tile: PV done
-  static constexpr int kDrain = 4 * S + 10; // every MMA issued has completed
+  static constexpr int kDrain = 4 * S + 10; // + issuer: every MMA it issued has completed
+  static constexpr int kTail = 4 * S + 12;  // V rows past the item's end zeroed (issuer A -> B)
 };
 
 // 2^x on the FMA pipe, for x <= 2^kRescaleLog2: x = n + f with n = floor(x) and
@@ -114,7 +116,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   const int tok0[2] = {it.q_start, it.q_start + it.q_count};
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4 * kSt; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 4 * kSt; ++i) mbar_init(&bars[i], (i >= kSt && i < 2 * kSt) || i >= 3 * kSt ? 2 : 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[B::kQ + t], 128);
       mbar_init(&bars[B::kS + t], 1);
@@ -123,6 +125,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       mbar_init(&bars[B::kPv + t], 1);
     }
     mbar_init(&bars[B::kDrain], 1);
+    mbar_init(&bars[B::kDrain + 1], 1);
+    mbar_init(&bars[B::kTail], 1);
     s_pos[0] = -1;
     s_pos[1] = 0x7fffffff;
     s_pos[2] = -1;
@@ -233,58 +237,66 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         (void)mbar_wait(&bars[B::kVFull + i % kSt], (i / kSt) & 1, nullptr);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuer of query tile t
+    const int t = warp - 9;
+    const int nt_t = ntile[t];
     constexpr uint32_t idesc_s = make_idesc_bf16(128, kNK, false);
     constexpr uint32_t idesc_o = make_idesc_bf16(128, D, true);
-    bool ok = mbar_wait_warp(&bars[B::kQ], 0, s_abort) && mbar_wait_warp(&bars[B::kQ + 1], 0, s_abort);
-    // S_t(j) = Q_t K(j)^T into TMEM columns [64 t, 64 t + 64); the softmax of
-    // tile t has read S_t(j-1) into registers once it released the columns.
-    auto issue_s = [&](int t, int j) -> bool {
+    // Descriptors are built once; each MMA only advances the start-address
+    // field (bits 0-13, in 16-byte units) by a constant offset.
+    const uint64_t dq = make_sdesc_sw128(sQ + t * S::kQ, 16, 1024);
+    const uint64_t dk = make_sdesc_sw128(sK, 16, 1024);
+    const uint64_t dv = make_sdesc_sw128(sV, kNK * 128, 1024);
+    const uint32_t d_s = tmem + kColS + t * kNK, d_o = tmem + kColO + t * 128, a_p = tmem + kColP + t * (kNK / 2);
+    bool ok = mbar_wait_warp(&bars[B::kQ + t], 0, s_abort);
+    // S_t(j) = Q_t K(j)^T into this tile's S columns; the softmax has read
+    // S_t(j-1) into registers once it released them.
+    auto issue_s = [&](int j) -> bool {
       const int st = j % kSt;
       if (!mbar_wait_warp(&bars[B::kKFull + st], (j / kSt) & 1, s_abort)) return false;
       if (j > 0 && !mbar_wait_warp(&bars[B::kSFree + t], (j - 1) & 1, s_abort)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t q_base = sQ + t * S::kQ;
+        const uint64_t kst = dk + static_cast<uint64_t>((st * S::kKV) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int hf = ks / 4, kk = ks % 4;
-          const uint64_t ad = make_sdesc_sw128(q_base + hf * (kTcRows * 128) + kk * 32, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(sK + st * S::kKV + hf * (kNK * 128) + kk * 32, 16, 1024);
-          tc_mma(tmem + kColS + t * kNK, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+          tc_mma(d_s, dq + static_cast<uint64_t>((hf * (kTcRows * 128) + kk * 32) >> 4),
+                 kst + static_cast<uint64_t>((hf * (kNK * 128) + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
         }
         tc_commit(&bars[B::kS + t]);
       }
       __syncwarp();
       return true;
     };
-    // O_t += P_t(j) V(j), P_t in TMEM columns [128 + 32 t, 128 + 32 t + 32).
-    auto issue_pv = [&](int t, int j) -> bool {
+    // O_t += P_t(j) V(j).
+    auto issue_pv = [&](int j, bool wait_tail) -> bool {
       const int st = j % kSt;
       if (!mbar_wait_warp(&bars[B::kP + t], j & 1, s_abort)) return false;
       if (!mbar_wait_warp(&bars[B::kVFull + st], (j / kSt) & 1, s_abort)) return false;
+      if (wait_tail && !mbar_wait_warp(&bars[B::kTail], 0, s_abort)) return false;
       tc_fence_after();
       if (lane == 0) {
+        const uint64_t vst = dv + static_cast<uint64_t>((st * S::kKV) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < kNK / 16; ++ks) {
-          const uint64_t bd = make_sdesc_sw128(sV + st * S::kKV + ks * (16 * 128), kNK * 128, 1024);
-          tc_mma_ts(tmem + kColO + t * 128, tmem + kColP + t * (kNK / 2) + ks * 8, bd, idesc_o,
+        for (int ks = 0; ks < kNK / 16; ++ks)
+          tc_mma_ts(d_o, a_p + ks * 8, vst + static_cast<uint64_t>((ks * (16 * 128)) >> 4), idesc_o,
                     (j > 0 || ks > 0) ? 1u : 0u);
-        }
         tc_commit(&bars[B::kPv + t]);
       }
       __syncwarp();
       return true;
     };
-    // Keys past the item's end in its last tile: zero their V rows so that
-    // 0 * garbage cannot produce NaN in the tensor core.
+    // Keys past the item's end in its last tile: issuer A zeroes their V rows
+    // (so that 0 * garbage cannot produce NaN in the tensor core) before either
+    // tile's PV of that tile; issuer B waits for it.
+    const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
     auto zero_v_tail = [&](int j) -> bool {
       const int st = j % kSt;
-      const int nkeys = min(kNK, kv_end - (it.kv_start + j * kNK));
-      if (nkeys >= kNK) return true;
       if (!mbar_wait_warp(&bars[B::kVFull + st], (j / kSt) & 1, s_abort)) return false;
       uint8_t* vst = smem + S::kOffV + st * S::kKV;
+      const int nkeys = last_nkeys;
       for (int idx = lane; idx < (kNK - nkeys) * S::kHalves * 8; idx += 32) {
         const int hf = idx / ((kNK - nkeys) * 8);
         const int rem = idx % ((kNK - nkeys) * 8);
@@ -293,20 +305,20 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       }
       fence_proxy_async_smem();
       __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B::kTail]);
       return true;
     };
-    if (ok && ntile[0] > 0) ok = issue_s(0, 0);
-    if (ok && ntile[1] > 0) ok = issue_s(1, 0);
+    // Every issuer releases every K/V stage once (the empty barriers count two).
+    if (ok && nt_t > 0) ok = issue_s(0);
     if (ok && ntiles > 0 && lane == 0) tc_commit(&bars[B::kKEmpty]);
     __syncwarp();
     for (int j = 0; ok && j < ntiles; ++j) {
-      if (j + 1 < ntile[0] && !(ok = issue_s(0, j + 1))) break;
-      if (j + 1 < ntile[1] && !(ok = issue_s(1, j + 1))) break;
+      if (j + 1 < nt_t && !(ok = issue_s(j + 1))) break;
       if (lane == 0 && j + 1 < ntiles) tc_commit(&bars[B::kKEmpty + (j + 1) % kSt]);
       __syncwarp();
-      if (j == ntiles - 1 && !(ok = zero_v_tail(j))) break;
-      if (j < ntile[0] && !(ok = issue_pv(0, j))) break;
-      if (j < ntile[1] && !(ok = issue_pv(1, j))) break;
+      const bool last_partial = j == ntiles - 1 && last_nkeys < kNK;
+      if (t == 0 && last_partial && !(ok = zero_v_tail(j))) break;
+      if (j < nt_t && !(ok = issue_pv(j, t == 1 && last_partial))) break;
       if (lane == 0) tc_commit(&bars[B::kVEmpty + j % kSt]);
       __syncwarp();
     }
@@ -315,9 +327,9 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       *s_abort = 1;
     }
     // Drain: every MMA this thread issued has completed before TMEM is released.
-    if (lane == 0) tc_commit(&bars[B::kDrain]);
+    if (lane == 0) tc_commit(&bars[B::kDrain + t]);
     __syncwarp();
-    (void)mbar_wait_warp(&bars[B::kDrain], 0, nullptr);
+    (void)mbar_wait_warp(&bars[B::kDrain + t], 0, nullptr);
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue of tile X
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
