@@ -308,19 +308,32 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       if (lane == 0) mbar_arrive(&bars[B::kTail]);
       return true;
     };
-    // Every issuer releases every K/V stage once (the empty barriers count two).
+    // Every issuer releases every K/V stage once per tile (the empty barriers
+    // count two), and only after it has seen that tile land in the stage: an
+    // mbarrier does not keep phases apart, so a release for a later use of a
+    // stage must never arrive before the current use is complete.  An issuer
+    // with no work for a tile therefore still waits for the tile's full phase.
+    auto release_k = [&](int j, bool issued) -> bool {
+      if (!issued && !mbar_wait_warp(&bars[B::kKFull + j % kSt], (j / kSt) & 1, s_abort)) return false;
+      if (lane == 0) tc_commit(&bars[B::kKEmpty + j % kSt]);
+      __syncwarp();
+      return true;
+    };
+    auto release_v = [&](int j, bool issued) -> bool {
+      if (!issued && !mbar_wait_warp(&bars[B::kVFull + j % kSt], (j / kSt) & 1, s_abort)) return false;
+      if (lane == 0) tc_commit(&bars[B::kVEmpty + j % kSt]);
+      __syncwarp();
+      return true;
+    };
     if (ok && nt_t > 0) ok = issue_s(0);
-    if (ok && ntiles > 0 && lane == 0) tc_commit(&bars[B::kKEmpty]);
-    __syncwarp();
+    if (ok && ntiles > 0) ok = release_k(0, nt_t > 0);
     for (int j = 0; ok && j < ntiles; ++j) {
       if (j + 1 < nt_t && !(ok = issue_s(j + 1))) break;
-      if (lane == 0 && j + 1 < ntiles) tc_commit(&bars[B::kKEmpty + (j + 1) % kSt]);
-      __syncwarp();
+      if (j + 1 < ntiles && !(ok = release_k(j + 1, j + 1 < nt_t))) break;
       const bool last_partial = j == ntiles - 1 && last_nkeys < kNK;
       if (t == 0 && last_partial && !(ok = zero_v_tail(j))) break;
       if (j < nt_t && !(ok = issue_pv(j, t == 1 && last_partial))) break;
-      if (lane == 0) tc_commit(&bars[B::kVEmpty + j % kSt]);
-      __syncwarp();
+      if (!(ok = release_v(j, j < nt_t || (t == 0 && last_partial)))) break;
     }
     if (!ok) {
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
