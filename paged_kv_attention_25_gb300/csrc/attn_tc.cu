@@ -6,30 +6,30 @@
 //
 // One CTA (one per SM) runs one work item: two query tiles A and B of up to
 // 128 rows each (tokens x grouped heads of one KV head; one row per TMEM
-// lane) of the same request, against a range of key positions in tiles of 64
-// keys (4 KV blocks).  Each K/V tile is brought into shared memory once and
-// used by both query tiles: an SM can take in only a few tens of bytes per
-// clock from the memory system, so query rows per byte loaded is what bounds
-// this kernel.
+// lane) of the same request, against a range of key positions in tiles of
+// 128 keys (8 KV blocks).  Each K/V tile is brought into shared memory once
+// and used by both query tiles: an SM takes in only a few tens of bytes per
+// clock from the memory system, so query rows per byte loaded bound this
+// kernel next to the tensor cores.
 //
 //   warp 8     producer: reads the block table a window ahead and gathers each
 //              block's K and V (16 keys x 64 dims per TMA box, 128-byte
-//              swizzle) into a shared-memory ring (cp.async.bulk.tensor);
-//   warps 9,10 MMA issuers, one per query tile (a tcgen05.mma costs its
-//              issuing thread about a hundred cycles, and two issuing threads
-//              overlap): S_t = Q_t K^T (kind::f16, M=128, N=64, bf16 in, fp32
-//              accumulate in TMEM) and O_t += P_t V with P_t read from TMEM;
+//              swizzle) into shared-memory rings (cp.async.bulk.tensor); K
+//              runs one tile ahead of V;
+//   warp 9     MMA issuer: S_t = Q_t K^T (kind::f16, M=128, N=128 keys, bf16
+//              in, fp32 in TMEM) and O_t += P_t V with P_t read from TMEM, in
+//              the order PV_A(j) S_A(j+1) PV_B(j) S_B(j+1): tile B's softmax
+//              runs while the tensor pipe works on tile A and the other way
+//              round.  P_t(j) is written over S_t(j); S_t(j+1) may follow
+//              PV_t(j) at once because MMAs issued by one thread run in order;
 //   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B: one query row
-//              per thread.  Each thread loads its S row into registers and at
-//              once releases the S columns (so the next S MMA overlaps the rest
-//              of the softmax), applies the causal mask on absolute positions,
-//              runs the online softmax in fp32 (exp2 with scale*log2 e folded
-//              in; a quarter of the exponentials on the FMA pipe by a cubic,
-//              the rest on the SFU; lazy rescaling of O) and writes P as bf16
-//              into its own TMEM columns; epilogue O / l.
+//              per thread.  Each thread loads its 128 S values, applies the
+//              causal mask on absolute positions, runs the online softmax in
+//              fp32 (exp2 with scale*log2 e folded in, on the SFU; paired fp32
+//              FMA/add; lazy rescaling of O) and writes P as bf16 over S;
+//              epilogue O / l.
 //
-// TMEM columns: S_A [0,64)  S_B [64,128)  P_A [128,160)  P_B [160,192)
-//               O_A [256, 256+D)  O_B [384, 384+D).
+// TMEM columns: S_A/P_A [0,128)  S_B/P_B [128,256)  O_A [256,384)  O_B [384,512).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -40,51 +40,57 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 352;
-constexpr int kNK = kTcKeys;            // keys per tile (64)
+constexpr int kThreads = 320;
+constexpr int kNK = kTcKeys;            // keys per tile (128)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 256;
+constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;     // lazy O rescale threshold (log2 units)
 
 template <int D>
 struct TcSmem {
   static constexpr int kHalves = D / 64;                 // 128-byte-wide column slabs
-  static constexpr int kStages = D == 128 ? 4 : 6;
+  static constexpr int kKSt = D == 128 ? 3 : 4;          // K stages
+  static constexpr int kVSt = D == 128 ? 2 : 4;          // V stages
   static constexpr int kQ = kTcRows * D * 2;             // one query tile: [halves][128 rows][64]
-  static constexpr int kKV = kNK * D * 2;                // one stage of K (or V): [halves][64 keys][64]
+  static constexpr int kKV = kNK * D * 2;                // one stage of K (or V): [halves][128 keys][64]
   static constexpr int kOffQ = 0;                        // tile A, then tile B
   static constexpr int kOffK = 2 * kQ;
-  static constexpr int kOffV = kOffK + kStages * kKV;
-  static constexpr int kOffBar = kOffV + kStages * kKV;
-  static constexpr int kNumBars = 4 * kStages + 13;
+  static constexpr int kOffV = kOffK + kKSt * kKV;
+  static constexpr int kOffBar = kOffV + kVSt * kKV;
+  static constexpr int kNumBars = 2 * kKSt + 2 * kVSt + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kTotal = kOffMisc + 64;
 };
+static_assert(TcSmem<128>::kTotal <= 232448, "shared memory of the D=128 kernel");
 
-template <int S>
+template <int KS, int VS>
 struct Bars {
-  static constexpr int kKFull = 0, kKEmpty = S, kVFull = 2 * S, kVEmpty = 3 * S;
-  static constexpr int kQ = 4 * S;          // + tile: Q in shared memory (128 arrivals)
-  static constexpr int kS = 4 * S + 2;      // + tile: S ready in TMEM
-  static constexpr int kSFree = 4 * S + 4;  // + tile: S read into registers (128 arrivals)
-  static constexpr int kP = 4 * S + 6;      // + tile: P written (128 arrivals)
-  static constexpr int kPv = 4 * S + 8;     // + tile: PV done
-  static constexpr int kDrain = 4 * S + 10; // + issuer: every MMA it issued has completed
-  static constexpr int kTail = 4 * S + 12;  // V rows past the item's end zeroed (issuer A -> B)
+  static constexpr int kKFull = 0, kKEmpty = KS, kVFull = 2 * KS, kVEmpty = 2 * KS + VS;
+  static constexpr int kQ = 2 * KS + 2 * VS;   // + tile: Q in shared memory (128 arrivals)
+  static constexpr int kS = kQ + 2;            // + tile: S ready in TMEM
+  static constexpr int kP = kQ + 4;            // + tile: P written, O rescaled (128 arrivals)
+  static constexpr int kPv = kQ + 6;           // + tile: PV done
+  static constexpr int kDrain = kQ + 8;        // every MMA issued has completed
 };
 
-// 2^x on the FMA pipe, for x <= 2^kRescaleLog2: x = n + f with n = floor(x) and
-// f in [0,1); 2^f from a cubic fitted to minimise the relative error on [0,1)
-// (at most 7.5e-5, far below bf16's 2^-9), then n added to the exponent field.
-// Inputs below -126 give 0.
-__device__ __forceinline__ float exp2_poly(float x) {
-  const float n = floorf(x);
-  const float f = x - n;
-  float p = fmaf(f, 0.0780244991f, 0.2260672152f);
-  p = fmaf(p, f, 0.6958335042f);
-  p = fmaf(p, f, 0.9999251962f);
-  const int bits = __float_as_int(p) + (static_cast<int>(n) << 23);
-  return x < -126.f ? 0.f : __int_as_float(bits);
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (x0, x1) * s + (c, c) with one paired fp32 FMA.
+__device__ __forceinline__ void fma2(float& x0, float& x1, float s, float c) {
+  asm("{\n\t.reg .b64 p, q, r;\n\tmov.b64 p, {%0, %1};\n\tmov.b64 q, {%2, %2};\n\tmov.b64 r, {%3, %3};\n\t"
+      "fma.rn.f32x2 p, p, q, r;\n\tmov.b64 {%0, %1}, p;\n\t}"
+      : "+f"(x0), "+f"(x1) : "f"(s), "f"(c));
+}
+
+// (a0, a1) += (b0, b1) with one paired fp32 add.
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 p, q;\n\tmov.b64 p, {%0, %1};\n\tmov.b64 q, {%2, %3};\n\t"
+      "add.rn.f32x2 p, p, q;\n\tmov.b64 {%0, %1}, p;\n\t}"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
 }
 
 template <int D>
@@ -92,8 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                const WorkItem* __restrict__ items) {
   using S = TcSmem<D>;
-  using B = Bars<S::kStages>;
-  constexpr int kSt = S::kStages;
+  constexpr int kKSt = S::kKSt, kVSt = S::kVSt;
+  using B = Bars<kKSt, kVSt>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {   // swizzle atoms need 1024-byte alignment
     if (threadIdx.x == 0) atomicOr(a.pool.err, PKV_DEVERR_INTERNAL);
@@ -116,17 +122,21 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   const int tok0[2] = {it.q_start, it.q_start + it.q_count};
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4 * kSt; ++i) mbar_init(&bars[i], (i >= kSt && i < 2 * kSt) || i >= 3 * kSt ? 2 : 1);
+    for (int i = 0; i < kKSt; ++i) {
+      mbar_init(&bars[B::kKFull + i], 1);
+      mbar_init(&bars[B::kKEmpty + i], 1);
+    }
+    for (int i = 0; i < kVSt; ++i) {
+      mbar_init(&bars[B::kVFull + i], 1);
+      mbar_init(&bars[B::kVEmpty + i], 1);
+    }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[B::kQ + t], 128);
       mbar_init(&bars[B::kS + t], 1);
-      mbar_init(&bars[B::kSFree + t], 128);
       mbar_init(&bars[B::kP + t], 128);
       mbar_init(&bars[B::kPv + t], 1);
     }
     mbar_init(&bars[B::kDrain], 1);
-    mbar_init(&bars[B::kDrain + 1], 1);
-    mbar_init(&bars[B::kTail], 1);
     s_pos[0] = -1;
     s_pos[1] = 0x7fffffff;
     s_pos[2] = -1;
@@ -173,7 +183,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
-    constexpr int kBlk = kNK / kBlockSize;   // blocks per key tile (4)
+    constexpr int kBlk = kNK / kBlockSize;   // blocks per key tile (8)
     constexpr int kWin = 32 / kBlk;          // key tiles per window of 32 block ids
     // Block ids are read a window ahead: lane l holds the id of block
     // (first block of the item) + 32 w + l, and the next window is in flight
@@ -193,160 +203,158 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       return pb;
     };
     int ids_cur = load_window(0), ids_next = load_window(1), win = 0;
-    int j = 0;
-    for (; j < ntiles; ++j) {
-      const int st = j % kSt;
-      const uint32_t ph = (j / kSt) & 1;
+    // Row of the 2-D pool view of this lane's block in tile j (-1: none).
+    auto block_row = [&](int j) -> int {
       if (j / kWin != win) {
         win = j / kWin;
         ids_cur = ids_next;
         ids_next = load_window(win + 1);
       }
       const int key0 = it.kv_start + j * kNK;
-      const int nkeys = min(kNK, kv_end - key0);
-      const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;
+      const int nblk = (min(kNK, kv_end - key0) + kBlockSize - 1) / kBlockSize;
       int pb = __shfl_sync(0xffffffffu, ids_cur, (j % kWin) * kBlk + (lane % kBlk));
       if (lane >= nblk) pb = -1;
-      const int nvalid = __popc(__ballot_sync(0xffffffffu, pb >= 0));
+      return pb < 0 ? -1 : (pb * Hkv + g) * kBlockSize;
+    };
+    auto load = [&](int j, int y, bool is_k) -> bool {
+      const int nst = is_k ? kKSt : kVSt;
+      const int st = j % nst;
+      const uint32_t ph = (j / nst) & 1;
+      uint64_t* full = &bars[(is_k ? B::kKFull : B::kVFull) + st];
+      const int nvalid = __popc(__ballot_sync(0xffffffffu, y >= 0));
       const uint32_t bytes = static_cast<uint32_t>(nvalid) * S::kHalves * (kBlockSize * 128);
-      const int y = (pb * Hkv + g) * kBlockSize;   // row of the 2-D pool view
-      if (!mbar_wait_warp(&bars[B::kKEmpty + st], ph ^ 1, s_abort)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[B::kKFull + st], bytes);
+      if (!mbar_wait_warp(&bars[(is_k ? B::kKEmpty : B::kVEmpty) + st], ph ^ 1, s_abort)) return false;
+      if (lane == 0) mbar_arrive_expect_tx(full, bytes);
       __syncwarp();
-      if (pb >= 0) {
+      if (y >= 0) {
+        uint8_t* dst = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + lane * (kBlockSize * 128);
 #pragma unroll
         for (int hf = 0; hf < S::kHalves; ++hf)
-          tma_load_2d(smem + S::kOffK + st * S::kKV + hf * (kNK * 128) + lane * (kBlockSize * 128), &tmap_k,
-                      hf * 64, y, &bars[B::kKFull + st]);
+          tma_load_2d(dst + hf * (kNK * 128), is_k ? &tmap_k : &tmap_v, hf * 64, y, full);
       }
-      if (!mbar_wait_warp(&bars[B::kVEmpty + st], ph ^ 1, s_abort)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[B::kVFull + st], bytes);
-      __syncwarp();
-      if (pb >= 0) {
-#pragma unroll
-        for (int hf = 0; hf < S::kHalves; ++hf)
-          tma_load_2d(smem + S::kOffV + st * S::kKV + hf * (kNK * 128) + lane * (kBlockSize * 128), &tmap_v,
-                      hf * 64, y, &bars[B::kVFull + st]);
+      return true;
+    };
+    // K runs one tile ahead of V: K(j+1) is in flight while tile j's S, softmax and PV run.
+    bool ok = true;
+    int nk = 0, nv = 0;   // tiles whose K / V copies have been issued
+    int y_cur = ntiles > 0 ? block_row(0) : -1;
+    if (ntiles > 0 && (ok = load(0, y_cur, true))) nk = 1;
+    for (int j = 0; ok && j < ntiles; ++j) {
+      int y_next = -1;
+      if (j + 1 < ntiles) {
+        y_next = block_row(j + 1);
+        if (!(ok = load(j + 1, y_next, true))) break;
+        nk = j + 2;
       }
+      if (!(ok = load(j, y_cur, false))) break;
+      nv = j + 1;
+      y_cur = y_next;
     }
-    if (j < ntiles) {   // gave up: flag it and let copies already issued land
+    if (!ok) {   // gave up: flag it and let copies already issued land
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
       *s_abort = 1;
-      for (int i = max(0, j - kSt); i < j; ++i) {
-        (void)mbar_wait(&bars[B::kKFull + i % kSt], (i / kSt) & 1, nullptr);
-        (void)mbar_wait(&bars[B::kVFull + i % kSt], (i / kSt) & 1, nullptr);
-      }
+      for (int i = max(0, nk - kKSt); i < nk; ++i) (void)mbar_wait(&bars[B::kKFull + i % kKSt], (i / kKSt) & 1, nullptr);
+      for (int i = max(0, nv - kVSt); i < nv; ++i) (void)mbar_wait(&bars[B::kVFull + i % kVSt], (i / kVSt) & 1, nullptr);
     }
-  } else if (warp == 9 || warp == 10) {
-    // ------------------------------------------------------------ MMA issuer of query tile t
-    const int t = warp - 9;
-    const int nt_t = ntile[t];
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = make_idesc_bf16(128, kNK, false);
     constexpr uint32_t idesc_o = make_idesc_bf16(128, D, true);
     // Descriptors are built once; each MMA only advances the start-address
     // field (bits 0-13, in 16-byte units) by a constant offset.
-    const uint64_t dq = make_sdesc_sw128(sQ + t * S::kQ, 16, 1024);
     const uint64_t dk = make_sdesc_sw128(sK, 16, 1024);
     const uint64_t dv = make_sdesc_sw128(sV, kNK * 128, 1024);
-    const uint32_t d_s = tmem + kColS + t * kNK, d_o = tmem + kColO + t * 128, a_p = tmem + kColP + t * (kNK / 2);
-    bool ok = mbar_wait_warp(&bars[B::kQ + t], 0, s_abort);
-    // S_t(j) = Q_t K(j)^T into this tile's S columns; the softmax has read
-    // S_t(j-1) into registers once it released them.
-    auto issue_s = [&](int j) -> bool {
-      const int st = j % kSt;
-      if (!mbar_wait_warp(&bars[B::kKFull + st], (j / kSt) & 1, s_abort)) return false;
-      if (j > 0 && !mbar_wait_warp(&bars[B::kSFree + t], (j - 1) & 1, s_abort)) return false;
-      tc_fence_after();
+    bool ok = mbar_wait_warp(&bars[B::kQ], 0, s_abort) && mbar_wait_warp(&bars[B::kQ + 1], 0, s_abort);
+    const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
+    // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage).
+    auto issue_s = [&](int t, int j) {
       if (lane == 0) {
-        const uint64_t kst = dk + static_cast<uint64_t>((st * S::kKV) >> 4);
+        const uint64_t dq = make_sdesc_sw128(sQ + t * S::kQ, 16, 1024);
+        const uint64_t kd = dk + static_cast<uint64_t>(((j % kKSt) * S::kKV) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int hf = ks / 4, kk = ks % 4;
-          tc_mma(d_s, dq + static_cast<uint64_t>((hf * (kTcRows * 128) + kk * 32) >> 4),
-                 kst + static_cast<uint64_t>((hf * (kNK * 128) + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
+          tc_mma(tmem + t * kNK, dq + static_cast<uint64_t>((hf * (kTcRows * 128) + kk * 32) >> 4),
+                 kd + static_cast<uint64_t>((hf * (kNK * 128) + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
         }
         tc_commit(&bars[B::kS + t]);
       }
       __syncwarp();
-      return true;
     };
-    // O_t += P_t(j) V(j).
-    auto issue_pv = [&](int j, bool wait_tail) -> bool {
-      const int st = j % kSt;
-      if (!mbar_wait_warp(&bars[B::kP + t], j & 1, s_abort)) return false;
-      if (!mbar_wait_warp(&bars[B::kVFull + st], (j / kSt) & 1, s_abort)) return false;
-      if (wait_tail && !mbar_wait_warp(&bars[B::kTail], 0, s_abort)) return false;
-      tc_fence_after();
+    // O_t += P_t(j) V(j), P_t(j) from TMEM (over S_t(j)).
+    auto issue_pv = [&](int t, int j) {
       if (lane == 0) {
-        const uint64_t vst = dv + static_cast<uint64_t>((st * S::kKV) >> 4);
+        const uint64_t vd = dv + static_cast<uint64_t>(((j % kVSt) * S::kKV) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kNK / 16; ++ks)
-          tc_mma_ts(d_o, a_p + ks * 8, vst + static_cast<uint64_t>((ks * (16 * 128)) >> 4), idesc_o,
-                    (j > 0 || ks > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + kColO + t * 128, tmem + t * kNK + ks * 8, vd + static_cast<uint64_t>((ks * (16 * 128)) >> 4),
+                    idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
         tc_commit(&bars[B::kPv + t]);
       }
       __syncwarp();
-      return true;
     };
-    // Keys past the item's end in its last tile: issuer A zeroes their V rows
-    // (so that 0 * garbage cannot produce NaN in the tensor core) before either
-    // tile's PV of that tile; issuer B waits for it.
-    const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
-    auto zero_v_tail = [&](int j) -> bool {
-      const int st = j % kSt;
-      if (!mbar_wait_warp(&bars[B::kVFull + st], (j / kSt) & 1, s_abort)) return false;
-      uint8_t* vst = smem + S::kOffV + st * S::kKV;
-      const int nkeys = last_nkeys;
-      for (int idx = lane; idx < (kNK - nkeys) * S::kHalves * 8; idx += 32) {
-        const int hf = idx / ((kNK - nkeys) * 8);
-        const int rem = idx % ((kNK - nkeys) * 8);
-        const int key = nkeys + rem / 8, chunk = rem % 8;
-        *reinterpret_cast<uint4*>(vst + hf * (kNK * 128) + key * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+    // Each K/V stage is released once per tile, and only after its tile has
+    // landed: an mbarrier does not keep phases apart, so a release for a later
+    // use of a stage must never arrive before the current use is complete.
+    auto release = [&](int bar) {
+      if (lane == 0) tc_commit(&bars[bar]);
+      __syncwarp();
+    };
+    if (ok && ntiles > 0) {
+      if ((ok = mbar_wait_warp(&bars[B::kKFull], 0, s_abort))) {
+        tc_fence_after();
+        if (ntile[0] > 0) issue_s(0, 0);
+        if (ntile[1] > 0) issue_s(1, 0);
+        release(B::kKEmpty);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B::kTail]);
-      return true;
-    };
-    // Every issuer releases every K/V stage once per tile (the empty barriers
-    // count two), and only after it has seen that tile land in the stage: an
-    // mbarrier does not keep phases apart, so a release for a later use of a
-    // stage must never arrive before the current use is complete.  An issuer
-    // with no work for a tile therefore still waits for the tile's full phase.
-    auto release_k = [&](int j, bool issued) -> bool {
-      if (!issued && !mbar_wait_warp(&bars[B::kKFull + j % kSt], (j / kSt) & 1, s_abort)) return false;
-      if (lane == 0) tc_commit(&bars[B::kKEmpty + j % kSt]);
-      __syncwarp();
-      return true;
-    };
-    auto release_v = [&](int j, bool issued) -> bool {
-      if (!issued && !mbar_wait_warp(&bars[B::kVFull + j % kSt], (j / kSt) & 1, s_abort)) return false;
-      if (lane == 0) tc_commit(&bars[B::kVEmpty + j % kSt]);
-      __syncwarp();
-      return true;
-    };
-    if (ok && nt_t > 0) ok = issue_s(0);
-    if (ok && ntiles > 0) ok = release_k(0, nt_t > 0);
+    }
     for (int j = 0; ok && j < ntiles; ++j) {
-      if (j + 1 < nt_t && !(ok = issue_s(j + 1))) break;
-      if (j + 1 < ntiles && !(ok = release_k(j + 1, j + 1 < nt_t))) break;
-      const bool last_partial = j == ntiles - 1 && last_nkeys < kNK;
-      if (t == 0 && last_partial && !(ok = zero_v_tail(j))) break;
-      if (j < nt_t && !(ok = issue_pv(j, t == 1 && last_partial))) break;
-      if (!(ok = release_v(j, j < nt_t || (t == 0 && last_partial)))) break;
+      const bool next = j + 1 < ntiles;   // then at least one tile issues S(j+1) below
+      bool k_next = false;                // K(j+1) seen in its stage
+      if (!(ok = mbar_wait_warp(&bars[B::kVFull + j % kVSt], (j / kVSt) & 1, s_abort))) break;
+      if (j == ntiles - 1 && last_nkeys < kNK) {
+        // Keys past the item's end in its last tile: zero their V rows so that
+        // 0 * stale data cannot produce NaN in the tensor core.
+        uint8_t* vst = smem + S::kOffV + (j % kVSt) * S::kKV;
+        for (int idx = lane; idx < (kNK - last_nkeys) * S::kHalves * 8; idx += 32) {
+          const int hf = idx / ((kNK - last_nkeys) * 8);
+          const int rem = idx % ((kNK - last_nkeys) * 8);
+          const int key = last_nkeys + rem / 8, chunk = rem % 8;
+          *reinterpret_cast<uint4*>(vst + hf * (kNK * 128) + key * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (j < ntile[t]) {
+          if (!(ok = mbar_wait_warp(&bars[B::kP + t], j & 1, s_abort))) break;
+          tc_fence_after();
+          issue_pv(t, j);
+          if (j + 1 < ntile[t]) {
+            if (!k_next && !(ok = mbar_wait_warp(&bars[B::kKFull + (j + 1) % kKSt], ((j + 1) / kKSt) & 1, s_abort)))
+              break;
+            k_next = true;
+            tc_fence_after();
+            issue_s(t, j + 1);
+          }
+        }
+      }
+      if (!ok) break;
+      if (next) release(B::kKEmpty + (j + 1) % kKSt);
+      release(B::kVEmpty + j % kVSt);
     }
     if (!ok) {
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
       *s_abort = 1;
     }
-    // Drain: every MMA this thread issued has completed before TMEM is released.
-    if (lane == 0) tc_commit(&bars[B::kDrain + t]);
-    __syncwarp();
-    (void)mbar_wait_warp(&bars[B::kDrain + t], 0, nullptr);
+    // Drain: every MMA issued has completed before TMEM is released.
+    release(B::kDrain);
+    (void)mbar_wait_warp(&bars[B::kDrain], 0, nullptr);
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue of tile X
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t colS = kColS + X * kNK, colP = kColP + X * (kNK / 2), colO = kColO + X * 128;
+    const uint32_t colS = X * kNK, colO = kColO + X * 128;
     const int nrows = rows[X];
     const int nt = ntile[X];
     // Q tile: row `row` = (token tok0[X] + row / G, head g*G + row % G), swizzled K-major.
@@ -379,9 +387,6 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
 #pragma unroll
       for (int c = 0; c < kNK; c += 16) tmem_ld16(tmem + lane_base + colS + c, s + c);
       tmem_wait_ld();
-      // S is in registers: its TMEM columns may take the next S right away.
-      tc_fence_before();
-      mbar_arrive(&bars[B::kSFree + X]);
       if (key0 + kNK - 1 > min_pos[X] || key0 + kNK > kv_end) {
 #pragma unroll
         for (int c = 0; c < kNK; ++c) {
@@ -389,15 +394,14 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           if (key > qpos || key >= kv_end) s[c] = -CUDART_INF_F;
         }
       }
-      // Row max and sum as 8 independent partials (one long dependency chain
-      // would leave the softmax warps latency-bound).
+      // Row max as 8 independent partials of 3-input maxima (one long
+      // dependency chain would leave the softmax warps latency-bound).
       float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(s[2 * k], s[2 * k + 1]);
 #pragma unroll
-      for (int c = 8; c < kNK; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int c = 16; c < kNK; c += 2) mx8[(c >> 1) & 7] = max3f(mx8[(c >> 1) & 7], s[c], s[c + 1]);
+      const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       // Lazy rescaling: rows keep their reference max m while the tile max stays
       // within 2^kRescaleLog2 of it (P then stays <= 2^kRescaleLog2, fine for bf16
       // and fp32 sums); O and l always share the same reference, so the result
@@ -406,29 +410,26 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const float m_tile = mx * sl2;
       const bool grow = __any_sync(0xffffffffu, m_tile > m + kRescaleLog2);
       const float m_new = grow ? fmaxf(m, m_tile) : m;
-      const float m_use = m_new == -CUDART_INF_F ? 0.f : m_new;
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[kNK / 2];
+      const float neg_m = m_new == -CUDART_INF_F ? 0.f : -m_new;
+      float rs0[4] = {0.f, 0.f, 0.f, 0.f}, rs1[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(s * scale * log2 e - m) as bf16, written over S 32 keys at a
+      // time (16 columns); S columns are all in registers already.
 #pragma unroll
-      for (int c = 0; c < kNK; c += 2) {
-        const float x0 = fmaf(s[c], sl2, -m_use);
-        const float x1 = fmaf(s[c + 1], sl2, -m_use);
-        // A quarter of the exponentials on the FMA pipe, the rest on the SFU.
-        const float p0 = fast_exp2(x0);
-        const float p1 = (c & 2) ? exp2_poly(x1) : fast_exp2(x1);
-        rs8[(c >> 1) & 7] += p0 + p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
-      }
-      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-      const float alpha = grow ? fast_exp2(m - m_use) : 1.f;
-      // PV(j-1) read the P columns and accumulated O: wait for it before
-      // writing P(j) and rescaling O.
-      if (j > 0) {
-        if (!mbar_wait_warp(&bars[B::kPv + X], (j - 1) & 1, s_abort)) { ok = false; break; }
-        tc_fence_after();
-      }
+      for (int cc = 0; cc < kNK; cc += 32) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < kNK / 2; c += 16) tmem_st16(tmem + lane_base + colP + c, reinterpret_cast<const float*>(pk + c));
+        for (int c = cc; c < cc + 32; c += 2) {
+          float x0 = s[c], x1 = s[c + 1];
+          fma2(x0, x1, sl2, neg_m);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          add2(rs0[(c >> 1) & 3], rs1[(c >> 1) & 3], p0, p1);
+          pk[(c - cc) / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tmem + lane_base + colS + cc / 2, reinterpret_cast<const float*>(pk));
+      }
+      const float rsum = ((rs0[0] + rs1[0]) + (rs0[1] + rs1[1])) + ((rs0[2] + rs1[2]) + (rs0[3] + rs1[3]));
+      const float alpha = grow ? fast_exp2(m + neg_m) : 1.f;
+      // O(j-1) is complete (S(j) was issued after PV(j-1) finished).
       if (grow && j > 0) {
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
@@ -442,7 +443,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           tmem_st16(tmem + lane_base + colO + c + 16, o + 16);
         }
       }
-      l = l * alpha + rs;
+      l = l * alpha + rsum;
       m = m_new;
       tmem_wait_st();
       tc_fence_before();

@@ -12,7 +12,7 @@ namespace pkv {
 constexpr int kBlockSize = 16;        // tokens per KV block
 constexpr int kDecodeMaxRows = 4;     // query rows (tokens x group) per split-KV item
 constexpr int kTcRows = 128;          // query rows per tensor-core tile (TMEM lanes)
-constexpr int kTcKeys = 64;           // keys per tensor-core KV tile (4 blocks)
+constexpr int kTcKeys = 128;          // keys per tensor-core KV tile (8 blocks)
 
 // One CTA of work.  Rows of an item are (token q_start + i, query head
 // kv_head*G + j) for i < q_count + q_count2, j < G, numbered i*G + j.  A

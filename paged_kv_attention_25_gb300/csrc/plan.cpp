@@ -33,7 +33,7 @@ constexpr int kTcCtasPerSm = 1;
 constexpr int kDecodeSplitsPerSlot = 4;
 constexpr int kTcSplitsPerSlot = 1;
 constexpr int kMinDecodeChunk = 16;     // blocks (256 keys) per split at least
-constexpr int kMinTcChunk = 8;          // 64-key tiles (512 keys) per split at least
+constexpr int kMinTcChunk = 4;          // 128-key tiles (512 keys) per split at least
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -92,7 +92,7 @@ def check_plan(batch, num_sms=148):
         covered[q0:q0 + qc, g] += 1
         kv_len = min(int(batch.ctx_lens[r]), int(batch.q_positions[q0:q0 + qc].max()) + 1)
         its = sorted(its, key=lambda i: int(i["kv_start"]))
-        unit = 16 if kern == 1 else 64
+        unit = 16 if kern == 1 else 128
         # splits tile [0, kv_len) exactly, in whole units
         assert int(its[0]["kv_start"]) == 0 and int(its[-1]["kv_end"]) == kv_len
         for x, y in zip(its[:-1], its[1:]):
