@@ -263,6 +263,10 @@ typedef struct {
   int32_t kv_end;
   int32_t part;      /* -1: writes O/LSE directly; else first partial row */
   int32_t q_count2;
+  int32_t pos_max0;  /* query-position bounds of the first tile (the whole */
+  int32_t pos_min0;  /* split-KV item) and of the second tile: exact with  */
+  int32_t pos_max1;  /* host positions, else [0, ctx_len - 1]; an empty    */
+  int32_t pos_min1;  /* tile has pos_max -1                                 */
 } pkv_work_desc;
 
 /* Plan a batch on the host only (no device needed) and copy out its work

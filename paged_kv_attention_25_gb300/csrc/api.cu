@@ -417,8 +417,10 @@ int pkv_plan_inspect(int num_q_heads, int num_kv_heads, int head_dim, int num_sm
   for (int which = 0; which < 2; ++which)
     for (const WorkItem& w : which == 0 ? plan.decode : plan.tc) {
       if (items && k < max_items)
-        items[k] = pkv_work_desc{which + 1, w.req,    w.kv_head, w.q_start, w.q_count,
-                                 w.kv_start, w.kv_end, w.part,     w.q_count2};
+        items[k] = pkv_work_desc{which + 1,     w.req,          w.kv_head,      w.q_start,
+                                 w.q_count,     w.kv_start,     w.kv_end,       w.part,
+                                 w.q_count2,    w.pos_max[0],   w.pos_min[0],   w.pos_max[1],
+                                 w.pos_min[1]};
       ++k;
     }
   if (stats) *stats = plan.stats;

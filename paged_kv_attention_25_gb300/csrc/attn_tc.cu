@@ -105,15 +105,17 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     if (threadIdx.x == 0) atomicOr(a.pool.err, PKV_DEVERR_INTERNAL);
     return;
   }
-  // Once any wait in this launch has given up, the remaining CTAs do nothing.
-  // (__syncthreads_or makes the decision the same for every thread of the CTA.)
-  if (__syncthreads_or((*reinterpret_cast<volatile unsigned*>(a.pool.err) & PKV_DEVERR_TIMEOUT) != 0)) return;
+  // The work item and the launch's error word are read together: every global
+  // round trip before the first K/V copy is paid by every CTA.  Once any wait
+  // in this launch has given up, the remaining CTAs do nothing
+  // (__syncthreads_or makes the decision the same for every thread).
+  const WorkItem it = items[blockIdx.x];
+  const unsigned err0 = *reinterpret_cast<volatile unsigned*>(a.pool.err);
+  if (__syncthreads_or((err0 & PKV_DEVERR_TIMEOUT) != 0)) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
-  int* s_pos = reinterpret_cast<int*>(smem + S::kOffMisc + 16);   // max A, min A, max B, min B
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 32);
 
-  const WorkItem it = items[blockIdx.x];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
   const int g = it.kv_head;
@@ -137,10 +139,6 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       mbar_init(&bars[B::kPv + t], 1);
     }
     mbar_init(&bars[B::kDrain], 1);
-    s_pos[0] = -1;
-    s_pos[1] = 0x7fffffff;
-    s_pos[2] = -1;
-    s_pos[3] = 0x7fffffff;
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -154,27 +152,58 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   }
   const int X = (warp >> 2) & 1;            // query tile of a softmax warp (0 = A, 1 = B)
   const int row = threadIdx.x & 127;        // its row within the tile (TMEM lane)
-  int qpos = -1;
-  if (warp < 8 && row < rows[X]) qpos = __ldg(a.q_positions + tok0[X] + row / G);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp < 8 && row < rows[X]) {
-    atomicMax(&s_pos[2 * X], qpos);
-    atomicMin(&s_pos[2 * X + 1], qpos);
-  }
-  __syncthreads();
-  const uint32_t tmem = *s_tmem;
+  // Key range of each tile from the planner's position bounds, so that the
+  // block-table reads need not wait for the device positions.
   int ntile[2], min_pos[2];
   int kv_end = it.kv_start;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int e = min(it.kv_end, s_pos[2 * t] + 1);          // keys tile t can see
+    const int e = min(it.kv_end, it.pos_max[t] + 1);        // keys tile t can see
     ntile[t] = e > it.kv_start ? (e - it.kv_start + kNK - 1) / kNK : 0;
-    min_pos[t] = s_pos[2 * t + 1];
+    min_pos[t] = it.pos_min[t];
     kv_end = max(kv_end, e);
   }
   const int ntiles = max(ntile[0], ntile[1]);
+  // Round trips that only need the item are issued before the barrier: the
+  // producer's first two windows of block ids, the softmax threads' query
+  // position and query row.
+  const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
+  const int blk_first = it.kv_start / kBlockSize;
+  const int blk_end = (kv_end + kBlockSize - 1) / kBlockSize;
+  auto load_window = [&](int w) -> int {   // lane l: id of block blk_first + 32 w + l (-1: none)
+    const int col = blk_first + w * 32 + lane;
+    int pb = -1;
+    if (col < blk_end) {
+      pb = col < a.max_blocks ? __ldg(bt_row + col) : -1;
+      if (pb < 0 || pb >= a.pool.num_blocks) {
+        atomicOr(a.pool.err, PKV_DEVERR_BLOCK_ID);
+        pb = -1;
+      }
+    }
+    return pb;
+  };
+  int ids_cur = -1, ids_next = -1;
+  if (warp == 8) {
+    ids_cur = load_window(0);
+    ids_next = load_window(1);
+  }
+  int qpos = -1;
+  uint4 qrow[D / 8];
+  if (warp < 8) {
+    const uint4* src = nullptr;
+    if (row < rows[X]) {
+      const int t = tok0[X] + row / G;
+      qpos = __ldg(a.q_positions + t);
+      src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
+                                           (static_cast<int64_t>(t) * a.num_q_heads + g * G + row % G) * D);
+    }
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) qrow[c] = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
 
   const uint32_t sQ = smem_u32(smem + S::kOffQ);
   const uint32_t sK = smem_u32(smem + S::kOffK);
@@ -182,27 +211,12 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
     constexpr int kBlk = kNK / kBlockSize;   // blocks per key tile (8)
     constexpr int kWin = 32 / kBlk;          // key tiles per window of 32 block ids
     // Block ids are read a window ahead: lane l holds the id of block
     // (first block of the item) + 32 w + l, and the next window is in flight
     // while the current one is used.
-    const int blk_first = it.kv_start / kBlockSize;
-    const int blk_end = (kv_end + kBlockSize - 1) / kBlockSize;
-    auto load_window = [&](int w) -> int {
-      const int col = blk_first + w * 32 + lane;
-      int pb = -1;
-      if (col < blk_end) {
-        pb = col < a.max_blocks ? __ldg(bt_row + col) : -1;
-        if (pb < 0 || pb >= a.pool.num_blocks) {
-          atomicOr(a.pool.err, PKV_DEVERR_BLOCK_ID);
-          pb = -1;
-        }
-      }
-      return pb;
-    };
-    int ids_cur = load_window(0), ids_next = load_window(1), win = 0;
+    int win = 0;
     // Row of the 2-D pool view of this lane's block in tile j (-1: none).
     auto block_row = [&](int j) -> int {
       if (j / kWin != win) {
@@ -359,19 +373,11 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     const int nt = ntile[X];
     // Q tile: row `row` = (token tok0[X] + row / G, head g*G + row % G), swizzled K-major.
     {
-      const uint4* src = nullptr;
-      if (row < nrows) {
-        const int t = tok0[X] + row / G;
-        const int h = g * G + row % G;
-        src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
-                                             (static_cast<int64_t>(t) * a.num_q_heads + h) * D);
-      }
       uint8_t* qt = smem + S::kOffQ + X * S::kQ;
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
         const int hf = c / 8, cc = c % 8;
-        *reinterpret_cast<uint4*>(qt + hf * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) * 16)) = v;
+        *reinterpret_cast<uint4*>(qt + hf * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) * 16)) = qrow[c];
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars[B::kQ + X]);

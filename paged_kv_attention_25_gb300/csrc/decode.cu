@@ -50,10 +50,13 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(pbuf) + S::kPBuf);
   volatile int* s_abort = reinterpret_cast<volatile int*>(bars + kWarps * kStages);
 
-  // Once any wait in this launch has given up, the remaining CTAs do nothing.
-  // (__syncthreads_or makes the decision the same for every thread of the CTA.)
-  if (__syncthreads_or((*reinterpret_cast<volatile unsigned*>(a.pool.err) & PKV_DEVERR_TIMEOUT) != 0)) return;
+  // The work item and the launch's error word are read together: every global
+  // round trip before the first copy is paid by every CTA.  Once any wait in
+  // this launch has given up, the remaining CTAs do nothing (__syncthreads_or
+  // makes the decision the same for every thread).
   const WorkItem it = items[blockIdx.x];
+  const unsigned err0 = *reinterpret_cast<volatile unsigned*>(a.pool.err);
+  if (__syncthreads_or((err0 & PKV_DEVERR_TIMEOUT) != 0)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
   const int rows = it.q_count * G;
@@ -69,7 +72,6 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
   // Per-row query (pre-scaled by scale*log2 e) and position; rows >= `rows` are inert.
   float q[kDecodeMaxRows][kDPL];
   int qpos[kDecodeMaxRows];
-  int max_pos = -1;
 #pragma unroll
   for (int r = 0; r < kDecodeMaxRows; ++r) {
     qpos[r] = -1;
@@ -79,7 +81,6 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
       const int t = it.q_start + r / G;
       const int h = g * G + r % G;
       qpos[r] = __ldg(a.q_positions + t);
-      max_pos = max(max_pos, qpos[r]);
       const uint16_t* src = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D + lane * kDPL;
       if constexpr (kDPL == 4) {
         const uint2 v = *reinterpret_cast<const uint2*>(src);
@@ -94,12 +95,12 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
       }
     }
   }
-  const int kv_end = min(it.kv_end, max_pos + 1);
+  // Key range from the planner's position bound (the device positions only
+  // mask), so that the block-table reads need not wait for them.
+  const int kv_end = min(it.kv_end, it.pos_max[0] + 1);
   const int blk0 = it.kv_start / kBlockSize;
   const int nblk = kv_end > it.kv_start ? (kv_end - it.kv_start + kBlockSize - 1) / kBlockSize : 0;
   const int nb_w = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;   // blocks of this warp
-
-  __syncthreads();
 
   uint8_t* my_ring = ring + warp * kStages * S::kStage;
   uint64_t* my_full = bars + warp * kStages;
@@ -121,6 +122,7 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
     return pb;
   };
   int ids_cur = load_ids(0), ids_next = load_ids(32), win = 0;
+  __syncthreads();   // barrier initialisation visible (the id loads above are already in flight)
 
   auto issue = [&](int j) {
     // Only lane 0 issues; every lane evaluates the shuffle.

@@ -28,8 +28,13 @@ struct WorkItem {
   int32_t kv_end;    // one past the last key position this item may read
   int32_t part;      // -1: write O / LSE directly; else first fp32 partial row
   int32_t q_count2;  // tokens in the second tensor-core tile
+  // Query-position bounds of tile 0 (the whole item for split-KV) and tile 1:
+  // exact when the host knows the positions, else [0, ctx_len - 1].  The
+  // kernels size their key range with them before the device positions land.
+  int32_t pos_max[2];
+  int32_t pos_min[2];
 };
-static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+static_assert(sizeof(WorkItem) == 48, "WorkItem layout");
 
 // Log-sum-exp merge of `nsplit` partial results of one (token tile, KV head),
 // for rows [row_begin, row_begin + row_count) of that tile (one CTA each).

@@ -45,6 +45,7 @@ struct QGroup {
   int q_count;   // tokens (of the first tile, for a tensor-core pair)
   int kv_len;    // keys the group can see: min(ctx, max position + 1)
   int q_count2;  // tokens of the second tensor-core tile (0: none)
+  int pos_max[2], pos_min[2];   // position bounds of the tile(s)
 };
 
 }  // namespace
@@ -124,8 +125,28 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
       for (int t = t0; t < t0 + c; ++t) mx = std::max(mx, static_cast<int>(pos[t]));
       return std::min(static_cast<int>(ctx[r]), mx + 1);
     };
+    // Position bounds of tokens [t0, t0 + c): exact with host positions, else
+    // the whole context (masking then uses the device positions).
+    auto bounds = [&](int t0, int c, int* mx, int* mn) {
+      if (c == 0) {
+        *mx = -1;
+        *mn = 0;
+      } else if (!pos) {
+        *mx = static_cast<int>(ctx[r]) - 1;
+        *mn = 0;
+      } else {
+        *mx = -1;
+        *mn = 0x7fffffff;
+        for (int t = t0; t < t0 + c; ++t) {
+          *mx = std::max(*mx, static_cast<int>(pos[t]));
+          *mn = std::min(*mn, static_cast<int>(pos[t]));
+        }
+      }
+    };
     if (n * G <= kDecodeMaxRows) {
-      dec_groups.push_back({r, cu[r], n, kv_len_of(cu[r], n), 0});
+      QGroup q{r, cu[r], n, kv_len_of(cu[r], n), 0, {-1, -1}, {0, 0}};
+      bounds(cu[r], n, &q.pos_max[0], &q.pos_min[0]);
+      dec_groups.push_back(q);
       continue;
     }
     int t = cu[r];
@@ -147,7 +168,10 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
     for (size_t i = 0; i < tiles.size(); i += 2) {
       const int c0 = tiles[i].second;
       const int c1 = i + 1 < tiles.size() ? tiles[i + 1].second : 0;
-      tc_groups.push_back({r, tiles[i].first, c0, kv_len_of(tiles[i].first, c0 + c1), c1});
+      QGroup q{r, tiles[i].first, c0, kv_len_of(tiles[i].first, c0 + c1), c1, {-1, -1}, {0, 0}};
+      bounds(tiles[i].first, c0, &q.pos_max[0], &q.pos_min[0]);
+      bounds(tiles[i].first + c0, c1, &q.pos_max[1], &q.pos_min[1]);
+      tc_groups.push_back(q);
     }
   }
 
@@ -192,6 +216,10 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
         w.kv_end = static_cast<int32_t>(std::min<int64_t>(g.kv_len, u1 * unit_keys));
         w.part = nsplit > 1 ? base + s * rows : -1;
         w.q_count2 = g.q_count2;
+        for (int t = 0; t < 2; ++t) {
+          w.pos_max[t] = g.pos_max[t];
+          w.pos_min[t] = g.pos_min[t];
+        }
         if (w.kv_end <= w.kv_start) {   // cannot happen with an even split; keep a valid empty item
           w.kv_end = w.kv_start;
         }

@@ -79,7 +79,8 @@ class pkv_profile(ctypes.Structure):
 
 class pkv_work_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("kernel", "req", "kv_head", "q_start", "q_count", "kv_start", "kv_end", "part", "q_count2")]
+                ("kernel", "req", "kv_head", "q_start", "q_count", "kv_start", "kv_end", "part", "q_count2",
+                 "pos_max0", "pos_min0", "pos_max1", "pos_min1")]
 
 
 _lib = None

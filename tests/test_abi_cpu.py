@@ -75,6 +75,14 @@ def check_plan(batch, num_sms=148):
         else:
             assert int(it["q_count"]) * G <= 128 and int(it["q_count2"]) * G <= 128
         groups.setdefault(key, []).append(it)
+        # position bounds of each tile: exact, since the host knows the positions
+        q0, c0, c1 = int(it["q_start"]), int(it["q_count"]), int(it["q_count2"])
+        for t0, c, mx, mn in ((q0, c0, it["pos_max0"], it["pos_min0"]), (q0 + c0, c1, it["pos_max1"], it["pos_min1"])):
+            if c == 0:
+                assert int(mx) == -1
+            else:
+                assert int(mx) == int(batch.q_positions[t0:t0 + c].max())
+                assert int(mn) == int(batch.q_positions[t0:t0 + c].min())
     covered = np.zeros((batch.num_tokens, Hkv), np.int32)
     part_rows = []
     dec_bytes = tc_bytes = 0
@@ -174,3 +182,5 @@ def test_planner_without_host_positions_covers_whole_context(lib):
         its = items[items["req"] == r]
         if len(its):
             assert its["kv_end"].max() == b.ctx_lens[r]
+            # unknown positions: bounds cover the whole context
+            assert (its["pos_max0"] == b.ctx_lens[r] - 1).all() and (its["pos_min0"] == 0).all()
