@@ -25,7 +25,7 @@ namespace pkv {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 
 template <int D>
 struct DecodeSmem {
@@ -39,7 +39,7 @@ struct DecodeSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 3)
 decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
   using S = DecodeSmem<D>;
   constexpr int kDPL = D / 32;   // head dims per lane

@@ -23,7 +23,7 @@ namespace pkv {
 
 namespace {
 
-constexpr int kDecodeCtasPerSm = 2;
+constexpr int kDecodeCtasPerSm = 3;
 constexpr int kTcCtasPerSm = 1;
 // A split-KV partial is one fp32 row per query row (small next to the keys it
 // summarises), so split-KV items are cut to a quarter of the average per-slot
