@@ -394,11 +394,10 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       for (int c = 0; c < kNK; c += 16) tmem_ld16(tmem + lane_base + colS + c, s + c);
       tmem_wait_ld();
       if (key0 + kNK - 1 > min_pos[X] || key0 + kNK > kv_end) {
+        // The row sees keys [0, min(qpos + 1, kv_end)): a prefix of the tile.
+        const int lim = min(qpos + 1, kv_end) - key0;
 #pragma unroll
-        for (int c = 0; c < kNK; ++c) {
-          const int key = key0 + c;
-          if (key > qpos || key >= kv_end) s[c] = -CUDART_INF_F;
-        }
+        for (int c = 0; c < kNK; ++c) s[c] = c < lim ? s[c] : -CUDART_INF_F;
       }
       // Row max as 8 independent partials of 3-input maxima (one long
       // dependency chain would leave the softmax warps latency-bound).

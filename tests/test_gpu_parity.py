@@ -198,6 +198,30 @@ def test_peaky_scores_select_one_value():
     assert float(o.float().abs().mean()) > 0.3
 
 
+@pytest.mark.parametrize("G", [1, 8])
+def test_nan_in_slots_past_the_context_does_not_leak(G):
+    """Pool slots no request may see (unused blocks, and the slots past each context in its last
+    block) hold NaN: masked keys must contribute exactly nothing (a 0 * NaN product in the split-KV
+    FMAs or the tensor-core PV would spread NaN to every row of the tile)."""
+    batch = wl.random_small(21 + G, num_q_heads=2 * G, num_kv_heads=2, head_dim=128, num_reqs=8, max_ctx=700,
+                            max_q=150)
+    run = GpuRun(batch)
+    nan = float("nan")
+    unused = torch.from_numpy(np.setdiff1d(np.arange(batch.num_blocks), batch.used_blocks)).long().cuda()
+    for pool in (run.pool.k, run.pool.v):
+        pool[unused] = nan
+        for r in range(batch.num_reqs):
+            c = int(batch.ctx_lens[r])
+            if c % 16:
+                pool[int(batch.block_tables[r, c // 16]), :, c % 16:, :] = nan
+    o, lse = run.step()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    kp, vp = oracle_pools(batch)
+    O, L = oracle.paged_attn(batch.q, kp, vp, batch.block_tables, batch.ctx_lens, batch.cu_q_lens,
+                             batch.q_positions, batch.scale)
+    assert_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O, L, batch.name)
+
+
 def test_zero_tokens_is_a_no_op():
     batch = wl.tiny_mixed(1)
     run = GpuRun(batch)
