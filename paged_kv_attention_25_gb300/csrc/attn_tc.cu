@@ -49,8 +49,8 @@ constexpr float kRescaleLog2 = 8.f;     // lazy O rescale threshold (log2 units)
 template <int D>
 struct TcSmem {
   static constexpr int kHalves = D / 64;                 // 128-byte-wide column slabs
-  static constexpr int kKSt = D == 128 ? 3 : 4;          // K stages
-  static constexpr int kVSt = D == 128 ? 2 : 4;          // V stages
+  static constexpr int kKSt = D == 128 ? 2 : 4;          // K stages
+  static constexpr int kVSt = D == 128 ? 3 : 4;          // V stages (the PV copies bound the pair period)
   static constexpr int kQ = kTcRows * D * 2;             // one query tile: [halves][128 rows][64]
   static constexpr int kKV = kNK * D * 2;                // one stage of K (or V): [halves][128 keys][64]
   static constexpr int kOffQ = 0;                        // tile A, then tile B
