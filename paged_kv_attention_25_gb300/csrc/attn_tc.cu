@@ -12,10 +12,11 @@
 // clock from the memory system, so query rows per byte loaded bound this
 // kernel next to the tensor cores.
 //
-//   warp 8     producer: reads the block table a window ahead and gathers each
-//              block's K and V (16 keys x 64 dims per TMA box, 128-byte
-//              swizzle) into shared-memory rings (cp.async.bulk.tensor); K
-//              runs one tile ahead of V;
+//   warps 8,10 producers of K and of V: read the block table a window ahead
+//              and gather each block's K (warp 8) or V (warp 10) (16 keys x 64
+//              dims per TMA box, 128-byte swizzle) into shared-memory rings
+//              (cp.async.bulk.tensor), 2 K and 3 V stages; separate warps so
+//              that neither stream waits behind the other's free stages;
 //   warp 9     MMA issuer: S_t = Q_t K^T (kind::f16, M=128, N=128 keys, bf16
 //              in, fp32 in TMEM) and O_t += P_t V with P_t read from TMEM, in
 //              the order PV_A(j) S_A(j+1) PV_B(j) S_B(j+1): tile B's softmax
@@ -40,7 +41,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kNK = kTcKeys;            // keys per tile (128)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
@@ -183,7 +184,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     return pb;
   };
   int ids_cur = -1, ids_next = -1;
-  if (warp == 8) {
+  if (warp == 8 || warp == 10) {
     ids_cur = load_window(0);
     ids_next = load_window(1);
   }
@@ -209,8 +210,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   const uint32_t sK = smem_u32(smem + S::kOffK);
   const uint32_t sV = smem_u32(smem + S::kOffV);
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ producers: warp 8 K, warp 10 V
     constexpr int kBlk = kNK / kBlockSize;   // blocks per key tile (8)
     constexpr int kWin = 32 / kBlk;          // key tiles per window of 32 block ids
     // Block ids are read a window ahead: lane l holds the id of block
@@ -248,27 +249,22 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       }
       return true;
     };
-    // K runs one tile ahead of V: K(j+1) is in flight while tile j's S, softmax and PV run.
+    // K and V stream from two warps, so that neither waits behind the
+    // other's free stages: a K stage frees when its S MMAs finish, a V stage
+    // only when both tiles' PV on it have finished.
+    const bool is_k = warp == 8;
+    const int nst = is_k ? kKSt : kVSt;
     bool ok = true;
-    int nk = 0, nv = 0;   // tiles whose K / V copies have been issued
-    int y_cur = ntiles > 0 ? block_row(0) : -1;
-    if (ntiles > 0 && (ok = load(0, y_cur, true))) nk = 1;
-    for (int j = 0; ok && j < ntiles; ++j) {
-      int y_next = -1;
-      if (j + 1 < ntiles) {
-        y_next = block_row(j + 1);
-        if (!(ok = load(j + 1, y_next, true))) break;
-        nk = j + 2;
-      }
-      if (!(ok = load(j, y_cur, false))) break;
-      nv = j + 1;
-      y_cur = y_next;
+    int nl = 0;   // tiles whose copies this warp has issued
+    for (int j = 0; j < ntiles; ++j) {
+      if (!(ok = load(j, block_row(j), is_k))) break;
+      nl = j + 1;
     }
     if (!ok) {   // gave up: flag it and let copies already issued land
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
       *s_abort = 1;
-      for (int i = max(0, nk - kKSt); i < nk; ++i) (void)mbar_wait(&bars[B::kKFull + i % kKSt], (i / kKSt) & 1, nullptr);
-      for (int i = max(0, nv - kVSt); i < nv; ++i) (void)mbar_wait(&bars[B::kVFull + i % kVSt], (i / kVSt) & 1, nullptr);
+      for (int i = max(0, nl - nst); i < nl; ++i)
+        (void)mbar_wait(&bars[(is_k ? B::kKFull : B::kVFull) + i % nst], (i / nst) & 1, nullptr);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
