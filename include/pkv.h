@@ -177,6 +177,10 @@ int pkv_paged_attn_workspace_size(pkv_pool* pool, int num_q_heads, int num_reqs,
  * workspace: device memory of at least pkv_paged_attn_workspace_size() bytes,
  * 256-byte aligned, owned by the caller and not used by other work in flight.
  * The split-KV partials and the uploaded work list live there.
+ * Streams: when the batch has both split-KV and tensor-core work, the split-KV
+ * kernel runs on a stream owned by the pool, ordered after the work already
+ * on `stream` (event) and joined back into `stream` before the merge; every
+ * effect of the call is complete once `stream` passes the point after it.
  * num_tokens == 0 is a no-op.  Errors: PKV_EINVAL for bad shapes, a workspace
  * that is too small, or host metadata that is inconsistent.
  */
@@ -227,7 +231,9 @@ int pkv_last_plan_stats(const pkv_pool* pool, pkv_plan_stats* out);
  * out [n][2][Hkv][B][D] (swap out), or back into the pool (swap in).
  * block_ids is a HOST array (copied into the launch; no upload).  With pinned
  * host_buf (cudaHostAlloc / registered, 16-byte aligned) one kernel moves all
- * blocks directly between HBM and host memory, asynchronously on `stream`;
+ * blocks directly between HBM and host memory, asynchronously on `stream`,
+ * on a few SMs only (8 CTAs out, 24 in: enough to saturate the CPU-GPU link,
+ * so that it can run beside attention kernels);
  * with pageable memory the library falls back to DMA copies (one 2-D copy
  * per run of consecutive ids and pool), which the driver may serialise with
  * the host.  Issue on a side stream and record an event to overlap with
