@@ -347,6 +347,10 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
     if (!pl.decode.empty()) std::memcpy(host + pl.off_decode, pl.decode.data(), pl.decode.size() * sizeof(WorkItem));
     if (!pl.tc.empty()) std::memcpy(host + pl.off_tc, pl.tc.data(), pl.tc.size() * sizeof(WorkItem));
     if (!pl.merge.empty()) std::memcpy(host + pl.off_merge, pl.merge.data(), pl.merge.size() * sizeof(MergeItem));
+    if (!pl.merge_dec.empty()) {
+      std::memcpy(host + pl.off_merge_dec, pl.merge_dec.data(), pl.merge_dec.size() * sizeof(MergeItem));
+      std::memset(host + pl.off_merge_cnt, 0, pl.merge_dec.size() * sizeof(int32_t));
+    }
     PKV_CUDA(cudaMemcpyAsync(ws, host, meta_bytes, cudaMemcpyHostToDevice, s), "upload work list");
     if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], s), "staging slot record");
   }
@@ -365,6 +369,8 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   a.lse = lse;
   a.part_o = reinterpret_cast<float*>(ws + pl.off_part_o);
   a.part_lse = reinterpret_cast<float*>(ws + pl.off_part_lse);
+  a.merge_dec = reinterpret_cast<const MergeItem*>(ws + pl.off_merge_dec);
+  a.merge_cnt = reinterpret_cast<int*>(ws + pl.off_merge_cnt);
 
   const WorkItem* d_dec = reinterpret_cast<const WorkItem*>(ws + pl.off_decode);
   const WorkItem* d_tc = reinterpret_cast<const WorkItem*>(ws + pl.off_tc);

@@ -8,7 +8,8 @@
 // tracked by mbarriers.  The four warps take blocks round-robin and keep their
 // own online-softmax state (running max m, sum l, fp32 accumulator); the CTA
 // merges the four states at the end and writes either the final O / LSE or a
-// split partial that the merge kernel combines by log-sum-exp (split-KV as in
+// split partial; the last split of a group to finish combines the group's
+// partials by log-sum-exp (split-KV as in
 // "PersistentKV: Page-Aware Decode Scheduling for Long-Context LLM Serving on
 // Commodity GPUs", section 2; attention as in "Stateful Large Language Model
 // Serving with Pensieve", abstract).
@@ -19,6 +20,7 @@
 #include <math_constants.h>
 
 #include "internal.h"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace pkv {
@@ -335,6 +337,27 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
       float2* o = reinterpret_cast<float2*>(a.part_o + static_cast<int64_t>(it.part + r) * D + d);
       *o = make_float2(o0, o1);
       if (d == 0) a.part_lse[it.part + r] = lse;
+    }
+  }
+
+  // Split group: count this split as done; the split that completes the count
+  // merges the group.  The barrier orders the CTA's partial writes before
+  // thread 0's device-scope fence and count (release); the merging CTA's
+  // thread 0 fences after the count (acquire) before the barrier that lets
+  // the other warps read the partials.
+  if (it.part >= 0 && it.merge_id >= 0) {
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const int last = atomicAdd(a.merge_cnt + it.merge_id, 1) == a.merge_dec[it.merge_id].nsplit - 1;
+      if (last) __threadfence();
+      s_last = last;
+    }
+    __syncthreads();
+    if (s_last) {
+      const MergeItem mi = a.merge_dec[it.merge_id];
+      if (warp < mi.row_count) merge_row<D>(a, mi, mi.row_begin + warp, lane);
     }
   }
 }

@@ -19,22 +19,26 @@ constexpr int kTcKeys = 128;          // keys per tensor-core KV tile (8 blocks)
 // tensor-core item holds two query tiles: tokens [q_start, q_start+q_count)
 // and the q_count2 tokens after them (0 when there is one tile); a split-KV
 // item has q_count2 = 0.
-struct WorkItem {
+struct alignas(16) WorkItem {
   int32_t req;
   int32_t kv_head;
   int32_t q_start;   // first token (index into [0, num_tokens))
-  int32_t q_count;   // tokens in the (first) tile
+  int16_t q_count;   // tokens in the (first) tile (<= 128)
+  int16_t q_count2;  // tokens in the second tensor-core tile (<= 128)
   int32_t kv_start;  // first key position (multiple of the kernel's key tile)
   int32_t kv_end;    // one past the last key position this item may read
   int32_t part;      // -1: write O / LSE directly; else first fp32 partial row
-  int32_t q_count2;  // tokens in the second tensor-core tile
+  // Split-KV item of a split group: index of the group's merge item in the
+  // fused list (the group's last split to finish merges it); else -1.
+  int32_t merge_id;
   // Query-position bounds of tile 0 (the whole item for split-KV) and tile 1:
   // exact when the host knows the positions, else [0, ctx_len - 1].  The
   // kernels size their key range with them before the device positions land.
   int32_t pos_max[2];
   int32_t pos_min[2];
 };
-static_assert(sizeof(WorkItem) == 48, "WorkItem layout");
+static_assert(sizeof(WorkItem) == 48, "WorkItem layout: three 16-byte loads");
+static_assert(kTcRows <= 32767, "token counts of a tile fit 16 bits");
 
 // Log-sum-exp merge of `nsplit` partial results of one (token tile, KV head),
 // for rows [row_begin, row_begin + row_count) of that tile (one CTA each).
@@ -65,11 +69,12 @@ struct PlanParams {
 struct Plan {
   std::vector<WorkItem> decode;   // split-KV CUDA-core kernel
   std::vector<WorkItem> tc;       // tensor-core kernel
-  std::vector<MergeItem> merge;
+  std::vector<MergeItem> merge;        // merged by the merge kernel (tensor-core groups)
+  std::vector<MergeItem> merge_dec;    // merged inside the split-KV kernel
   int num_partial_rows = 0;
   pkv_plan_stats stats{};
   // Workspace layout (byte offsets, 256-aligned sections).
-  size_t off_decode = 0, off_tc = 0, off_merge = 0, off_part_o = 0, off_part_lse = 0, total = 0;
+  size_t off_decode = 0, off_tc = 0, off_merge = 0, off_merge_dec = 0, off_merge_cnt = 0, off_part_o = 0, off_part_lse = 0, total = 0;
   uint64_t signature = 0;
   bool valid = false;
 };
@@ -116,6 +121,8 @@ struct AttnArgs {
   float* lse;
   float* part_o;         // [num_partial_rows][head_dim]
   float* part_lse;       // [num_partial_rows]
+  const MergeItem* merge_dec;   // merge items of split-KV groups (merged by their last split)
+  int* merge_cnt;               // splits finished per such item (zeroed by the work-list upload)
 };
 
 int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream);

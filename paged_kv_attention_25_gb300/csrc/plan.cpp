@@ -187,7 +187,9 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   int merge_groups = 0;
 
   int part_rows = 0;
-  auto emit = [&](const QGroup& g, int unit_keys, int64_t chunk_units, std::vector<WorkItem>& out) {
+  // fused: the group's last split merges it inside the split-KV kernel (rows
+  // fit one merge item); else the merge kernel does.
+  auto emit = [&](const QGroup& g, int unit_keys, int64_t chunk_units, std::vector<WorkItem>& out, bool fused) {
     const int rows = (g.q_count + g.q_count2) * G;
     const int64_t units = ceil_div(g.kv_len, unit_keys);
     int nsplit = static_cast<int>(std::max<int64_t>(1, ceil_div(units, chunk_units)));
@@ -195,14 +197,15 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
     const int64_t per = ceil_div(units, nsplit);
     nsplit = static_cast<int>(ceil_div(units, per));
     for (int kvh = 0; kvh < Hkv; ++kvh) {
-      int base = -1;
+      int base = -1, merge_id = -1;
       if (nsplit > 1) {
         base = part_rows;
         part_rows += nsplit * rows;
         ++merge_groups;
+        std::vector<MergeItem>& ml = fused ? plan->merge_dec : plan->merge;
+        if (fused) merge_id = static_cast<int>(ml.size());
         for (int r0 = 0; r0 < rows; r0 += kMergeRowsPerCta)
-          plan->merge.push_back(
-            {g.q_start, g.q_count + g.q_count2, kvh, nsplit, base, r0, std::min(kMergeRowsPerCta, rows - r0), 0});
+          ml.push_back({g.q_start, g.q_count + g.q_count2, kvh, nsplit, base, r0, std::min(kMergeRowsPerCta, rows - r0), 0});
       }
       for (int s = 0; s < nsplit; ++s) {
         const int64_t u0 = s * per;
@@ -211,11 +214,12 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
         w.req = g.req;
         w.kv_head = kvh;
         w.q_start = g.q_start;
-        w.q_count = g.q_count;
+        w.q_count = static_cast<int16_t>(g.q_count);
         w.kv_start = static_cast<int32_t>(u0 * unit_keys);
         w.kv_end = static_cast<int32_t>(std::min<int64_t>(g.kv_len, u1 * unit_keys));
         w.part = nsplit > 1 ? base + s * rows : -1;
-        w.q_count2 = g.q_count2;
+        w.q_count2 = static_cast<int16_t>(g.q_count2);
+        w.merge_id = merge_id;
         for (int t = 0; t < 2; ++t) {
           w.pos_max[t] = g.pos_max[t];
           w.pos_min[t] = g.pos_min[t];
@@ -227,8 +231,9 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
       }
     }
   };
-  for (const auto& g : dec_groups) emit(g, kBlockSize, dec_chunk, plan->decode);
-  for (const auto& g : tc_groups) emit(g, kTcKeys, tc_chunk, plan->tc);
+  static_assert(kDecodeMaxRows <= kMergeRowsPerCta, "a split-KV group is one merge item");
+  for (const auto& g : dec_groups) emit(g, kBlockSize, dec_chunk, plan->decode, true);
+  for (const auto& g : tc_groups) emit(g, kTcKeys, tc_chunk, plan->tc, false);
 
   // 3. Longest items first, so that the tail of each launch is short.
   auto longer = [](const WorkItem& a, const WorkItem& b) {
@@ -279,6 +284,10 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   off = align256(off + plan->tc.size() * sizeof(WorkItem));
   plan->off_merge = off;
   off = align256(off + plan->merge.size() * sizeof(MergeItem));
+  plan->off_merge_dec = off;
+  off = align256(off + plan->merge_dec.size() * sizeof(MergeItem));
+  plan->off_merge_cnt = off;   // counters, uploaded as zeros with the work lists
+  off = align256(off + plan->merge_dec.size() * sizeof(int32_t));
   plan->off_part_o = off;
   off = align256(off + size_t(part_rows) * D * sizeof(float));
   plan->off_part_lse = off;
