@@ -127,16 +127,52 @@ int timed_launch(pkv_pool* pool, int kernel, void* stream, F&& fn) {
 int make_tmap(CUtensorMap* map, void* base, int num_blocks, int hkv, int head_dim) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled unavailable (driver too old?)");
-  const cuuint64_t rows = static_cast<cuuint64_t>(num_blocks) * hkv * kBlockSize;
-  if (rows >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "pool too large for 32-bit TMA row coordinates");
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), rows};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+  const cuuint64_t chunks = static_cast<cuuint64_t>(num_blocks) * hkv;   // (block, head) chunks of 16 x D
+  if (chunks * kBlockSize >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "pool too large for 32-bit TMA coordinates");
+  CUresult r;
+  if (head_dim == 128) {
+    // One (block, head) chunk per copy, 16 rows x 256 bytes, landing as
+    // [8-row group][64-column half][8 rows][128 bytes]: the 4-D view
+    // (column within a half, row within a group, half, group) with strides
+    // (2, 256, 128, 2048) bytes.  Each 1024-byte [8 rows][128 bytes] piece is
+    // one 128-byte-swizzle atom of the MMA operand.
+    cuuint64_t dims[4] = {64, 8, 2, chunks * 2};
+    cuuint64_t strides[3] = {256, 128, 2048};
+    cuuint32_t box[4] = {64, 8, 2, 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // D = 64: a chunk is 16 rows of 128 bytes, already one column slab.
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), chunks * kBlockSize};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t estr[2] = {1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(static_cast<int>(r)));
+  return PKV_OK;
+}
+
+// Q viewed as [T][Hq][D] (bf16) for the tensor-core kernel's query tiles: a
+// box of 64 columns x G heads (one KV head's group) x the tile's tokens lands
+// as a [row][128 bytes] slab with 128-byte swizzle; tokens past T read zeros.
+int make_q_tmap(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads, int head_dim, int group,
+                int* box_tokens) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled unavailable (driver too old?)");
+  const int bt = std::min(kTcRows / group, num_tokens);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_q_heads),
+                        static_cast<cuuint64_t>(num_tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2, static_cast<cuuint64_t>(num_q_heads) * head_dim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(bt)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled failed: " + std::to_string(static_cast<int>(r)));
+  if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled (q) failed: " + std::to_string(static_cast<int>(r)));
+  *box_tokens = bt;
   return PKV_OK;
 }
 
@@ -371,6 +407,12 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   a.part_lse = reinterpret_cast<float*>(ws + pl.off_part_lse);
   a.merge_dec = reinterpret_cast<const MergeItem*>(ws + pl.off_merge_dec);
   a.merge_cnt = reinterpret_cast<int*>(ws + pl.off_merge_cnt);
+  a.q_box_tokens = 0;
+  CUtensorMap tmap_q;
+  if (!pl.tc.empty()) {
+    rc = make_q_tmap(&tmap_q, q, num_tokens, num_q_heads, pool->head_dim, a.group, &a.q_box_tokens);
+    if (rc) return rc;
+  }
 
   const WorkItem* d_dec = reinterpret_cast<const WorkItem*>(ws + pl.off_decode);
   const WorkItem* d_tc = reinterpret_cast<const WorkItem*>(ws + pl.off_tc);
@@ -392,7 +434,7 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   }
   if (!pl.tc.empty()) {
     rc = timed_launch(pool, 2, stream, [&] {
-      return launch_tc(a, &pool->tmap_k, &pool->tmap_v, d_tc, static_cast<int>(pl.tc.size()), stream);
+      return launch_tc(a, &pool->tmap_k, &pool->tmap_v, &tmap_q, d_tc, static_cast<int>(pl.tc.size()), stream);
     });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "tensor-core attention launch");
   }

@@ -13,10 +13,10 @@
 // kernel next to the tensor cores.
 //
 //   warps 8,10 producers of K and of V: read the block table a window ahead
-//              and gather each block's K (warp 8) or V (warp 10) (16 keys x 64
-//              dims per TMA box, 128-byte swizzle) into shared-memory rings
-//              (cp.async.bulk.tensor), 2 K and 3 V stages; separate warps so
-//              that neither stream waits behind the other's free stages;
+//              and gather each block's K (warp 8) or V (warp 10) into
+//              shared-memory rings (cp.async.bulk.tensor, one 16 x D box per
+//              block, 128-byte swizzle), 2 K and 3 V stages; separate warps
+//              so that neither stream waits behind the other's free stages;
 //   warp 9     MMA issuer: S_t = Q_t K^T (kind::f16, M=128, N=128 keys, bf16
 //              in, fp32 in TMEM) and O_t += P_t V with P_t read from TMEM, in
 //              the order PV_A(j) S_A(j+1) PV_B(j) S_B(j+1): tile B's softmax
@@ -53,7 +53,13 @@ struct TcSmem {
   static constexpr int kKSt = D == 128 ? 2 : 4;          // K stages
   static constexpr int kVSt = D == 128 ? 3 : 4;          // V stages (the PV copies bound the pair period)
   static constexpr int kQ = kTcRows * D * 2;             // one query tile: [halves][128 rows][64]
-  static constexpr int kKV = kNK * D * 2;                // one stage of K (or V): [halves][128 keys][64]
+  // One stage of K (or V), 128 keys: [8-key group][half][8 keys][64 columns],
+  // each [8][64] piece a 1024-byte swizzle atom; one TMA box fills the two
+  // groups of a block.  kGS: bytes between 8-key groups; kHS: between halves.
+  static constexpr int kKV = kNK * D * 2;
+  static constexpr int kGS = kHalves * 1024;
+  static constexpr int kHS = 1024;
+  static constexpr int kBlkBytes = 2 * kGS;              // one block (16 keys) of a stage
   static constexpr int kOffQ = 0;                        // tile A, then tile B
   static constexpr int kOffK = 2 * kQ;
   static constexpr int kOffV = kOffK + kKSt * kKV;
@@ -67,10 +73,10 @@ static_assert(TcSmem<128>::kTotal <= 232448, "shared memory of the D=128 kernel"
 template <int KS, int VS>
 struct Bars {
   static constexpr int kKFull = 0, kKEmpty = KS, kVFull = 2 * KS, kVEmpty = 2 * KS + VS;
-  static constexpr int kQ = 2 * KS + 2 * VS;   // + tile: Q in shared memory (128 arrivals)
+  static constexpr int kQ = 2 * KS + 2 * VS;   // + tile: Q in shared memory (TMA)
   static constexpr int kS = kQ + 2;            // + tile: S ready in TMEM
   static constexpr int kP = kQ + 4;            // + tile: P written, O rescaled (128 arrivals)
-  static constexpr int kPv = kQ + 6;           // + tile: PV done
+  static constexpr int kPv = kQ + 6;           // + tile: the tile's last PV done
   static constexpr int kDrain = kQ + 8;        // every MMA issued has completed
 };
 
@@ -97,7 +103,7 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-               const WorkItem* __restrict__ items) {
+               const __grid_constant__ CUtensorMap tmap_q, const WorkItem* __restrict__ items) {
   using S = TcSmem<D>;
   constexpr int kKSt = S::kKSt, kVSt = S::kVSt;
   using B = Bars<kKSt, kVSt>;
@@ -134,7 +140,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       mbar_init(&bars[B::kVEmpty + i], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars[B::kQ + t], 128);
+      mbar_init(&bars[B::kQ + t], 1);
       mbar_init(&bars[B::kS + t], 1);
       mbar_init(&bars[B::kP + t], 128);
       mbar_init(&bars[B::kPv + t], 1);
@@ -142,6 +148,22 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     mbar_init(&bars[B::kDrain], 1);
     *s_abort = 0;
     fence_mbar_init();
+    // Both query tiles by TMA, first of all copies: rows (token, head) of the
+    // tile land as [half][row][64 columns] (rows past the tile are other
+    // tokens' rows or zeros, computed and never stored).
+    prefetch_tmap(&tmap_q);
+    const uint32_t qbytes = static_cast<uint32_t>(D * 2 * G * a.q_box_tokens);
+    for (int t = 0; t < 2; ++t) {
+      if (rows[t] > 0) {
+        mbar_arrive_expect_tx(&bars[B::kQ + t], qbytes);
+        uint8_t* qt = smem + S::kOffQ + t * S::kQ;
+#pragma unroll
+        for (int hf = 0; hf < S::kHalves; ++hf)
+          tma_load_3d(qt + hf * (kTcRows * 128), &tmap_q, hf * 64, g * G, tok0[t], &bars[B::kQ + t]);
+      } else {
+        mbar_arrive(&bars[B::kQ + t]);
+      }
+    }
   }
   if (warp == 8 && lane == 0) {
     prefetch_tmap(&tmap_k);
@@ -166,8 +188,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   }
   const int ntiles = max(ntile[0], ntile[1]);
   // Round trips that only need the item are issued before the barrier: the
-  // producer's first two windows of block ids, the softmax threads' query
-  // position and query row.
+  // producer's first two windows of block ids and the softmax threads' query
+  // positions.
   const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
   const int blk_first = it.kv_start / kBlockSize;
   const int blk_end = (kv_end + kBlockSize - 1) / kBlockSize;
@@ -189,18 +211,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     ids_next = load_window(1);
   }
   int qpos = -1;
-  uint4 qrow[D / 8];
-  if (warp < 8) {
-    const uint4* src = nullptr;
-    if (row < rows[X]) {
-      const int t = tok0[X] + row / G;
-      qpos = __ldg(a.q_positions + t);
-      src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q) +
-                                           (static_cast<int64_t>(t) * a.num_q_heads + g * G + row % G) * D);
-    }
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) qrow[c] = src ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-  }
+  if (warp < 8 && row < rows[X]) qpos = __ldg(a.q_positions + tok0[X] + row / G);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -218,8 +229,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     // (first block of the item) + 32 w + l, and the next window is in flight
     // while the current one is used.
     int win = 0;
-    // Row of the 2-D pool view of this lane's block in tile j (-1: none).
-    auto block_row = [&](int j) -> int {
+    // (block, head) chunk index of this lane's block in tile j (-1: none).
+    auto block_chunk = [&](int j) -> int {
       if (j / kWin != win) {
         win = j / kWin;
         ids_cur = ids_next;
@@ -229,7 +240,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const int nblk = (min(kNK, kv_end - key0) + kBlockSize - 1) / kBlockSize;
       int pb = __shfl_sync(0xffffffffu, ids_cur, (j % kWin) * kBlk + (lane % kBlk));
       if (lane >= nblk) pb = -1;
-      return pb < 0 ? -1 : (pb * Hkv + g) * kBlockSize;
+      return pb < 0 ? -1 : pb * Hkv + g;
     };
     auto load = [&](int j, int y, bool is_k) -> bool {
       const int nst = is_k ? kKSt : kVSt;
@@ -242,10 +253,11 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       if (lane == 0) mbar_arrive_expect_tx(full, bytes);
       __syncwarp();
       if (y >= 0) {
-        uint8_t* dst = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + lane * (kBlockSize * 128);
-#pragma unroll
-        for (int hf = 0; hf < S::kHalves; ++hf)
-          tma_load_2d(dst + hf * (kNK * 128), is_k ? &tmap_k : &tmap_v, hf * 64, y, full);
+        uint8_t* dst = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + lane * S::kBlkBytes;
+        if constexpr (D == 128)
+          tma_load_4d(dst, is_k ? &tmap_k : &tmap_v, 0, 0, 0, 2 * y, full);
+        else
+          tma_load_2d(dst, is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, full);
       }
       return true;
     };
@@ -257,7 +269,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     bool ok = true;
     int nl = 0;   // tiles whose copies this warp has issued
     for (int j = 0; j < ntiles; ++j) {
-      if (!(ok = load(j, block_row(j), is_k))) break;
+      if (!(ok = load(j, block_chunk(j), is_k))) break;
       nl = j + 1;
     }
     if (!ok) {   // gave up: flag it and let copies already issued land
@@ -272,8 +284,10 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     constexpr uint32_t idesc_o = make_idesc_bf16(128, D, true);
     // Descriptors are built once; each MMA only advances the start-address
     // field (bits 0-13, in 16-byte units) by a constant offset.
-    const uint64_t dk = make_sdesc_sw128(sK, 16, 1024);
-    const uint64_t dv = make_sdesc_sw128(sV, kNK * 128, 1024);
+    // K: K-major, 8-key groups kGS apart; V: MN-major, 64-dim halves kHS
+    // apart (leading offset) and 8-key groups kGS apart (stride offset).
+    const uint64_t dk = make_sdesc_sw128(sK, 16, S::kGS);
+    const uint64_t dv = make_sdesc_sw128(sV, S::kHS, S::kGS);
     bool ok = mbar_wait_warp(&bars[B::kQ], 0, s_abort) && mbar_wait_warp(&bars[B::kQ + 1], 0, s_abort);
     const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
     // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage).
@@ -285,7 +299,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         for (int ks = 0; ks < D / 16; ++ks) {
           const int hf = ks / 4, kk = ks % 4;
           tc_mma(tmem + t * kNK, dq + static_cast<uint64_t>((hf * (kTcRows * 128) + kk * 32) >> 4),
-                 kd + static_cast<uint64_t>((hf * (kNK * 128) + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
+                 kd + static_cast<uint64_t>((hf * S::kHS + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
         }
         tc_commit(&bars[B::kS + t]);
       }
@@ -297,9 +311,11 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         const uint64_t vd = dv + static_cast<uint64_t>(((j % kVSt) * S::kKV) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kNK / 16; ++ks)
-          tc_mma_ts(tmem + kColO + t * 128, tmem + t * kNK + ks * 8, vd + static_cast<uint64_t>((ks * (16 * 128)) >> 4),
+          tc_mma_ts(tmem + kColO + t * 128, tmem + t * kNK + ks * 8, vd + static_cast<uint64_t>((ks * 2 * S::kGS) >> 4),
                     idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-        tc_commit(&bars[B::kPv + t]);
+        // Only the epilogue waits for PV: earlier PVs are covered by the next
+        // S commit of the tile (the tensor pipe completes one thread's MMAs in order).
+        if (j == ntile[t] - 1) tc_commit(&bars[B::kPv + t]);
       }
       __syncwarp();
     };
@@ -330,7 +346,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           const int hf = idx / ((kNK - last_nkeys) * 8);
           const int rem = idx % ((kNK - last_nkeys) * 8);
           const int key = last_nkeys + rem / 8, chunk = rem % 8;
-          *reinterpret_cast<uint4*>(vst + hf * (kNK * 128) + key * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vst + (key / 8) * S::kGS + hf * S::kHS + (key % 8) * 128 + chunk * 16) =
+              make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -367,17 +384,6 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     const uint32_t colS = X * kNK, colO = kColO + X * 128;
     const int nrows = rows[X];
     const int nt = ntile[X];
-    // Q tile: row `row` = (token tok0[X] + row / G, head g*G + row % G), swizzled K-major.
-    {
-      uint8_t* qt = smem + S::kOffQ + X * S::kQ;
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const int hf = c / 8, cc = c % 8;
-        *reinterpret_cast<uint4*>(qt + hf * (kTcRows * 128) + row * 128 + ((cc ^ (row & 7)) * 16)) = qrow[c];
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars[B::kQ + X]);
-    }
     const float sl2 = a.scale_log2;
     float m = -CUDART_INF_F, l = 0.f;
     bool ok = true;
@@ -451,7 +457,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       mbar_arrive(&bars[B::kP + X]);
     }
     if (ok && nt > 0) {
-      if (!mbar_wait_warp(&bars[B::kPv + X], (nt - 1) & 1, s_abort)) ok = false;
+      if (!mbar_wait_warp(&bars[B::kPv + X], 0, s_abort)) ok = false;
       tc_fence_after();
     }
     if (!ok) {
@@ -470,29 +476,35 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const int prow = it.part + (X == 0 ? row : rows[0] + row);
       uint4* dst_o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D);
       float4* dst_p = it.part >= 0 ? reinterpret_cast<float4*>(a.part_o + static_cast<int64_t>(prow) * D) : nullptr;
+      // O in 64-column batches: four TMEM loads in flight per wait.
 #pragma unroll
-      for (int c = 0; c < D; c += 16) {
-        float o[16];
+      for (int c0 = 0; c0 < D; c0 += 64) {
+        float ob[64];
         if (nt > 0) {
-          tmem_ld16(tmem + lane_base + colO + c, o);
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) tmem_ld16(tmem + lane_base + colO + c0 + c, ob + c);
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = 0.f;
+          for (int e = 0; e < 64; ++e) ob[e] = 0.f;
         }
         if (valid) {
-          if (it.part < 0) {
-            uint4 w0, w1;
-            w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);   w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-            w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);   w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-            w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);   w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
-            w1.z = pack_bf16x2(o[12] * inv, o[13] * inv); w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-            dst_o[c / 8] = w0;
-            dst_o[c / 8 + 1] = w1;
-          } else {
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-              dst_p[(c + e) / 4] = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+          for (int c = 0; c < 64; c += 16) {
+            const float* o = ob + c;
+            if (it.part < 0) {
+              uint4 w0, w1;
+              w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);   w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+              w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);   w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+              w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);   w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
+              w1.z = pack_bf16x2(o[12] * inv, o[13] * inv); w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
+              dst_o[(c0 + c) / 8] = w0;
+              dst_o[(c0 + c) / 8 + 1] = w1;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; e += 4)
+                dst_p[(c0 + c + e) / 4] = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+            }
           }
         }
       }
@@ -506,6 +518,12 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     }
   }
 
+  // The query-tile copies have landed before shared memory is released (at
+  // once unless a wait above gave up before the issuer saw them).
+  if (threadIdx.x == 0) {
+    (void)mbar_wait(&bars[B::kQ], 0, nullptr);
+    (void)mbar_wait(&bars[B::kQ + 1], 0, nullptr);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {
@@ -517,22 +535,23 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
 }  // namespace
 
 template <int D>
-static int launch_tc_d(const AttnArgs& a, const CUtensorMap* tk, const CUtensorMap* tv, const WorkItem* items,
-                       int n_items, void* stream) {
+static int launch_tc_d(const AttnArgs& a, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
+                       const WorkItem* items, int n_items, void* stream) {
   const int smem = TcSmem<D>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tc_attn_kernel<D><<<n_items, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, *tk, *tv, items);
+  tc_attn_kernel<D><<<n_items, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, *tk, *tv, *tq, items);
   return cudaGetLastError();
 }
 
-int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const WorkItem* items, int n_items,
-              void* stream) {
+int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const void* tmap_q, const WorkItem* items,
+              int n_items, void* stream) {
   if (n_items <= 0) return cudaSuccess;
   const CUtensorMap* tk = static_cast<const CUtensorMap*>(tmap_k);
   const CUtensorMap* tv = static_cast<const CUtensorMap*>(tmap_v);
-  if (a.pool.head_dim == 128) return launch_tc_d<128>(a, tk, tv, items, n_items, stream);
-  return launch_tc_d<64>(a, tk, tv, items, n_items, stream);
+  const CUtensorMap* tq = static_cast<const CUtensorMap*>(tmap_q);
+  if (a.pool.head_dim == 128) return launch_tc_d<128>(a, tk, tv, tq, items, n_items, stream);
+  return launch_tc_d<64>(a, tk, tv, tq, items, n_items, stream);
 }
 
 }  // namespace pkv

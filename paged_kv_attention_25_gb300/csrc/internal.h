@@ -123,11 +123,14 @@ struct AttnArgs {
   float* part_lse;       // [num_partial_rows]
   const MergeItem* merge_dec;   // merge items of split-KV groups (merged by their last split)
   int* merge_cnt;               // splits finished per such item (zeroed by the work-list upload)
+  int q_box_tokens;             // tokens per query-tile copy of the tensor-core kernel's Q tensor map
 };
 
 int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream);
-int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const WorkItem* items, int n_items,
-              void* stream);
+// tmap_q: Q viewed as [T][Hq][D] with a (64, G, q_box_tokens) box (128-byte
+// swizzle), built per call by make_q_tmap.
+int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const void* tmap_q, const WorkItem* items,
+              int n_items, void* stream);
 int launch_merge(const AttnArgs& a, const MergeItem* items, int n_items, void* stream);
 
 }  // namespace pkv
