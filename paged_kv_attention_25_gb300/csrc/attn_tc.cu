@@ -64,7 +64,7 @@ struct TcSmem {
   static constexpr int kOffK = 2 * kQ;
   static constexpr int kOffV = kOffK + kKSt * kKV;
   static constexpr int kOffBar = kOffV + kVSt * kKV;
-  static constexpr int kNumBars = 2 * kKSt + 2 * kVSt + 9;
+  static constexpr int kNumBars = 3 * kKSt + 2 * kVSt + 7;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kTotal = kOffMisc + 64;
 };
@@ -72,12 +72,14 @@ static_assert(TcSmem<128>::kTotal <= 232448, "shared memory of the D=128 kernel"
 
 template <int KS, int VS>
 struct Bars {
-  static constexpr int kKFull = 0, kKEmpty = KS, kVFull = 2 * KS, kVEmpty = 2 * KS + VS;
-  static constexpr int kQ = 2 * KS + 2 * VS;   // + tile: Q in shared memory (TMA)
-  static constexpr int kS = kQ + 2;            // + tile: S ready in TMEM
-  static constexpr int kP = kQ + 4;            // + tile: P written, O rescaled (128 arrivals)
-  static constexpr int kPv = kQ + 6;           // + tile: the tile's last PV done
-  static constexpr int kDrain = kQ + 8;        // every MMA issued has completed
+  // S of query tile t from K stage s ready in TMEM: kS + t * KS + s.  The same
+  // commit frees the K stage once the stage's last S (tile B's, where B has
+  // that key tile) has completed, so K stages need no release of their own.
+  static constexpr int kKFull = 0, kS = KS, kVFull = 3 * KS, kVEmpty = 3 * KS + VS;
+  static constexpr int kQ = 3 * KS + 2 * VS;   // + tile: Q in shared memory (TMA)
+  static constexpr int kP = kQ + 2;            // + tile: P written, O rescaled (128 arrivals)
+  static constexpr int kPv = kQ + 4;           // + tile: the tile's last PV done
+  static constexpr int kDrain = kQ + 6;        // every MMA issued has completed
 };
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -133,7 +135,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKSt; ++i) {
       mbar_init(&bars[B::kKFull + i], 1);
-      mbar_init(&bars[B::kKEmpty + i], 1);
+      mbar_init(&bars[B::kS + i], 1);
+      mbar_init(&bars[B::kS + kKSt + i], 1);
     }
     for (int i = 0; i < kVSt; ++i) {
       mbar_init(&bars[B::kVFull + i], 1);
@@ -141,7 +144,6 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[B::kQ + t], 1);
-      mbar_init(&bars[B::kS + t], 1);
       mbar_init(&bars[B::kP + t], 128);
       mbar_init(&bars[B::kPv + t], 1);
     }
@@ -249,7 +251,12 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       uint64_t* full = &bars[(is_k ? B::kKFull : B::kVFull) + st];
       const int nvalid = __popc(__ballot_sync(0xffffffffu, y >= 0));
       const uint32_t bytes = static_cast<uint32_t>(nvalid) * S::kHalves * (kBlockSize * 128);
-      if (!mbar_wait_warp(&bars[(is_k ? B::kKEmpty : B::kVEmpty) + st], ph ^ 1, s_abort)) return false;
+      // Free stage: V after the release that follows its tile's PVs; K after
+      // the S commit of the tile that last read it (j - nst), i.e. tile B's
+      // where B reaches that key tile, else tile A's.  Before a stage's first
+      // use, parity 1 of a fresh barrier passes at once.
+      const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile[1] ? kKSt : 0) + st : B::kVEmpty + st;
+      if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort)) return false;
       if (lane == 0) mbar_arrive_expect_tx(full, bytes);
       __syncwarp();
       if (y >= 0) {
@@ -301,7 +308,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           tc_mma(tmem + t * kNK, dq + static_cast<uint64_t>((hf * (kTcRows * 128) + kk * 32) >> 4),
                  kd + static_cast<uint64_t>((hf * S::kHS + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
         }
-        tc_commit(&bars[B::kS + t]);
+        tc_commit(&bars[B::kS + t * kKSt + j % kKSt]);
       }
       __syncwarp();
     };
@@ -319,9 +326,10 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       }
       __syncwarp();
     };
-    // Each K/V stage is released once per tile, and only after its tile has
+    // Each V stage is released once per tile, and only after its tile has
     // landed: an mbarrier does not keep phases apart, so a release for a later
     // use of a stage must never arrive before the current use is complete.
+    // (A K stage is freed by the S commits, which follow its landing.)
     auto release = [&](int bar) {
       if (lane == 0) tc_commit(&bars[bar]);
       __syncwarp();
@@ -331,11 +339,9 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         tc_fence_after();
         if (ntile[0] > 0) issue_s(0, 0);
         if (ntile[1] > 0) issue_s(1, 0);
-        release(B::kKEmpty);
       }
     }
     for (int j = 0; ok && j < ntiles; ++j) {
-      const bool next = j + 1 < ntiles;   // then at least one tile issues S(j+1) below
       bool k_next = false;                // K(j+1) seen in its stage
       if (!(ok = mbar_wait_warp(&bars[B::kVFull + j % kVSt], (j / kVSt) & 1, s_abort))) break;
       if (j == ntiles - 1 && last_nkeys < kNK) {
@@ -368,7 +374,6 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         }
       }
       if (!ok) break;
-      if (next) release(B::kKEmpty + (j + 1) % kKSt);
       release(B::kVEmpty + j % kVSt);
     }
     if (!ok) {
@@ -389,7 +394,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int key0 = it.kv_start + j * kNK;
-      if (!mbar_wait_warp(&bars[B::kS + X], j & 1, s_abort)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars[B::kS + X * kKSt + j % kKSt], (j / kKSt) & 1, s_abort)) { ok = false; break; }
       tc_fence_after();
       float s[kNK];
 #pragma unroll
