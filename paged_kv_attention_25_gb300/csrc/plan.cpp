@@ -25,12 +25,16 @@ namespace {
 
 constexpr int kDecodeCtasPerSm = 3;
 constexpr int kTcCtasPerSm = 1;
-// A split-KV partial is one fp32 row per query row (small next to the keys it
-// summarises), so split-KV items are cut to a quarter of the average per-slot
-// load; a tensor-core partial is a 128-row fp32 tile, so those items are cut
-// only when they exceed the average per-slot load (longest-first scheduling
-// then keeps the tail within about one item of the mean).
+// Split-KV items are cut to 1/s of the average per-slot load, with s the
+// smallest of 1..kDecodeSplitsPerSlot that still yields kDecodeMinWaves waves
+// of items (so that longest-first scheduling can balance the slots); every
+// extra split costs a CTA's fixed latency and a partial merge, and occupies
+// SMs the tensor-core kernel is waiting for.  A tensor-core partial is a
+// 128-row fp32 tile, so those items are cut only when they exceed the average
+// per-slot load (longest-first scheduling then keeps the tail within about
+// one item of the mean).
 constexpr int kDecodeSplitsPerSlot = 4;
+constexpr int kDecodeMinWaves = 2;
 constexpr int kTcSplitsPerSlot = 1;
 constexpr int kMinDecodeChunk = 16;     // blocks (256 keys) per split at least
 constexpr int kMinTcChunk = 4;          // 128-key tiles (512 keys) per split at least
@@ -180,8 +184,25 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   for (const auto& g : dec_groups) dec_blocks += ceil_div(g.kv_len, kBlockSize) * Hkv;
   for (const auto& g : tc_groups) tc_tiles += ceil_div(g.kv_len, kTcKeys) * Hkv;   // per tile pair
   const int sms = std::max(1, pp.num_sms);
-  const int64_t dec_chunk = std::max<int64_t>(
-      kMinDecodeChunk, ceil_div(dec_blocks, int64_t(sms) * kDecodeCtasPerSm * kDecodeSplitsPerSlot));
+  const int64_t dec_slots = int64_t(sms) * kDecodeCtasPerSm;
+  auto dec_chunk_for = [&](int s) { return std::max<int64_t>(kMinDecodeChunk, ceil_div(dec_blocks, dec_slots * s)); };
+  auto dec_items_for = [&](int64_t chunk) {   // the split-KV item count emit() will produce
+    int64_t n = 0;
+    for (const auto& g : dec_groups) {
+      const int64_t units = std::max<int64_t>(1, ceil_div(g.kv_len, kBlockSize));
+      const int64_t per = ceil_div(units, std::max<int64_t>(1, ceil_div(units, chunk)));
+      n += std::max<int64_t>(1, ceil_div(units, per)) * Hkv;
+    }
+    return n;
+  };
+  int64_t dec_chunk = dec_chunk_for(kDecodeSplitsPerSlot);
+  for (int s = 1; s < kDecodeSplitsPerSlot; ++s) {
+    const int64_t c = dec_chunk_for(s);
+    if (dec_items_for(c) >= kDecodeMinWaves * dec_slots) {
+      dec_chunk = c;
+      break;
+    }
+  }
   const int64_t tc_chunk =
       std::max<int64_t>(kMinTcChunk, ceil_div(tc_tiles, int64_t(sms) * kTcCtasPerSm * kTcSplitsPerSlot));
   int merge_groups = 0;
