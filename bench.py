@@ -276,15 +276,17 @@ def run_ours(args):
     swap_ids = batch.block_tables[r_swap, :max(1, first_q // 16)].astype(np.int32)
     swap_host = torch.empty((len(swap_ids), 2, batch.num_kv_heads, 16, D), dtype=torch.bfloat16).pin_memory()
     swap_bytes = swap_host.numel() * 2
-    appended = torch.cuda.Event()
+    begun = torch.cuda.Event()
     swapped = torch.cuda.Event()
 
+    # The swap-out moves cached history that this step's append does not
+    # write, so it starts with the step, beside the append.
     def step():
-        pkv.pkv_append(pool, d["block_tables"], d["cu_q_lens"], d["q_positions"], d["k_new"], d["v_new"])
-        appended.record(main)
-        side.wait_event(appended)
+        begun.record(main)
+        side.wait_event(begun)
         pkv.pkv_swap_out(pool, swap_ids, swap_host, stream=side)
         swapped.record(side)
+        pkv.pkv_append(pool, d["block_tables"], d["cu_q_lens"], d["q_positions"], d["k_new"], d["v_new"])
         pkv.pkv_paged_attn(pool, d["q"], d["q_positions"], d["block_tables"], d["ctx_lens"], d["cu_q_lens"],
                            meta, batch.scale, out=out, lse=lse, workspace=ws)
         main.wait_event(swapped)
@@ -371,11 +373,11 @@ def run_ours(args):
         di, (o_s, l_s) = dev_in[s], outs[s]
         main.wait_event(in_ready[s])
         main.wait_event(out_read[s])
-        pkv.pkv_append(pool, di["block_tables"], di["cu_q_lens"], di["q_positions"], di["k_new"], di["v_new"])
-        appended.record(main)
-        side.wait_event(appended)
+        begun.record(main)
+        side.wait_event(begun)
         pkv.pkv_swap_out(pool, swap_ids, swap_host, stream=side)
         swapped.record(side)
+        pkv.pkv_append(pool, di["block_tables"], di["cu_q_lens"], di["q_positions"], di["k_new"], di["v_new"])
         pkv.pkv_paged_attn(pool, di["q"], di["q_positions"], di["block_tables"], di["ctx_lens"], di["cu_q_lens"],
                            meta_e, batch.scale, out=o_s, lse=l_s, workspace=ws)
         main.wait_event(swapped)

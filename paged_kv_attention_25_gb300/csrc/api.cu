@@ -85,6 +85,12 @@ struct pkv_pool {
   // kernel on the caller's stream (fork / join through the two events).
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  // Work-list uploads run on `copy`, ordered only after the previous call's
+  // kernels (ws_free), so that they overlap the caller's work queued before
+  // the attention call (the append, typically); the kernels wait on up_done.
+  cudaStream_t copy = nullptr;
+  cudaEvent_t up_done = nullptr, ws_free = nullptr;
+
   // profiling
   bool prof_on = false;
   std::vector<cudaEvent_t> ev_free;
@@ -221,6 +227,9 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
     if (p->side) cudaStreamDestroy(p->side);
     if (p->fork) cudaEventDestroy(p->fork);
     if (p->join) cudaEventDestroy(p->join);
+    if (p->copy) cudaStreamDestroy(p->copy);
+    if (p->up_done) cudaEventDestroy(p->up_done);
+    if (p->ws_free) cudaEventDestroy(p->ws_free);
     delete p;
     return rc;
   };
@@ -259,6 +268,14 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
   if (cudaEventCreateWithFlags(&p->fork, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->join, cudaEventDisableTiming) != cudaSuccess)
     return cleanup(fail(PKV_ECUDA, "cudaEventCreate fork/join"));
+  if (cudaStreamCreateWithFlags(&p->copy, cudaStreamNonBlocking) != cudaSuccess) {
+    p->copy = nullptr;
+    return cleanup(fail(PKV_ECUDA, "cudaStreamCreate copy"));
+  }
+  if (cudaEventCreateWithFlags(&p->up_done, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->ws_free, cudaEventDisableTiming) != cudaSuccess)
+    return cleanup(fail(PKV_ECUDA, "cudaEventCreate upload"));
+
   int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim);
   if (rc) return cleanup(rc);
   rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim);
@@ -284,6 +301,10 @@ int pkv_pool_destroy(pkv_pool* pool) {
   cudaStreamDestroy(pool->side);
   cudaEventDestroy(pool->fork);
   cudaEventDestroy(pool->join);
+  cudaStreamDestroy(pool->copy);
+  cudaEventDestroy(pool->up_done);
+  cudaEventDestroy(pool->ws_free);
+
   for (auto& r : pool->pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -365,11 +386,14 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
 
   // Upload the work lists: through a pinned staging slot (asynchronous; the
   // slot is reused only after its previous upload has completed), or for an
-  // unusually large list through pageable memory (free again on return).
+  // unusually large list through pageable memory (free again on return).  The
+  // copy runs on the pool's copy stream after the previous call's kernels, so
+  // it overlaps whatever the caller queued on `stream` before this call.
   const size_t meta_bytes = pl.off_part_o;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   if (meta_bytes) {
+    PKV_CUDA(cudaStreamWaitEvent(pool->copy, pool->ws_free, 0), "upload wait");
     uint8_t* host = nullptr;
     const bool use_pinned = meta_bytes <= pkv_pool::kStagingBytes;
     if (use_pinned) {
@@ -387,8 +411,10 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
       std::memcpy(host + pl.off_merge_dec, pl.merge_dec.data(), pl.merge_dec.size() * sizeof(MergeItem));
       std::memset(host + pl.off_merge_cnt, 0, pl.merge_dec.size() * sizeof(int32_t));
     }
-    PKV_CUDA(cudaMemcpyAsync(ws, host, meta_bytes, cudaMemcpyHostToDevice, s), "upload work list");
-    if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], s), "staging slot record");
+    PKV_CUDA(cudaMemcpyAsync(ws, host, meta_bytes, cudaMemcpyHostToDevice, pool->copy), "upload work list");
+    if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], pool->copy), "staging slot record");
+    PKV_CUDA(cudaEventRecord(pool->up_done, pool->copy), "upload record");
+    PKV_CUDA(cudaStreamWaitEvent(s, pool->up_done, 0), "upload join");
   }
 
   AttnArgs a;
@@ -418,14 +444,17 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   const WorkItem* d_tc = reinterpret_cast<const WorkItem*>(ws + pl.off_tc);
   const MergeItem* d_merge = reinterpret_cast<const MergeItem*>(ws + pl.off_merge);
   // The two attention kernels are independent (disjoint outputs and workspace
-  // regions): with both present, the split-KV kernel (HBM-bound) runs on the
-  // pool's side stream next to the tensor-core kernel on the caller's stream.
+  // regions): with both present, one runs on the caller's stream and the
+  // other on the pool's side stream.  The caller's stream is dispatched first
+  // (the side stream waits on the fork event), so it takes the kernel with the
+  // longer estimated time.
   const bool fork = !pl.tc.empty() && !pl.decode.empty();
   void* dec_stream = stream;
+  void* tc_stream = stream;
   if (fork) {
     PKV_CUDA(cudaEventRecord(pool->fork, s), "fork record");
     PKV_CUDA(cudaStreamWaitEvent(pool->side, pool->fork, 0), "fork wait");
-    dec_stream = pool->side;
+    (pl.decode_first ? tc_stream : dec_stream) = pool->side;
   }
   if (!pl.decode.empty()) {
     rc = timed_launch(pool, 1, dec_stream,
@@ -433,8 +462,8 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "split-KV attention launch");
   }
   if (!pl.tc.empty()) {
-    rc = timed_launch(pool, 2, stream, [&] {
-      return launch_tc(a, &pool->tmap_k, &pool->tmap_v, &tmap_q, d_tc, static_cast<int>(pl.tc.size()), stream);
+    rc = timed_launch(pool, 2, tc_stream, [&] {
+      return launch_tc(a, &pool->tmap_k, &pool->tmap_v, &tmap_q, d_tc, static_cast<int>(pl.tc.size()), tc_stream);
     });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "tensor-core attention launch");
   }
@@ -446,6 +475,8 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
     rc = timed_launch(pool, 3, stream, [&] { return launch_merge(a, d_merge, static_cast<int>(pl.merge.size()), stream); });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "merge launch");
   }
+  // The next call's upload may overwrite the work lists once these kernels are done.
+  PKV_CUDA(cudaEventRecord(pool->ws_free, s), "workspace release");
   return PKV_OK;
 }
 
