@@ -310,7 +310,6 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         }
         tc_commit(&bars[B::kS + t * kKSt + j % kKSt]);
       }
-      __syncwarp();
     };
     // O_t += P_t(j) V(j), P_t(j) from TMEM (over S_t(j)).
     auto issue_pv = [&](int t, int j) {
@@ -324,15 +323,15 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         // S commit of the tile (the tensor pipe completes one thread's MMAs in order).
         if (j == ntile[t] - 1) tc_commit(&bars[B::kPv + t]);
       }
-      __syncwarp();
     };
     // Each V stage is released once per tile, and only after its tile has
     // landed: an mbarrier does not keep phases apart, so a release for a later
     // use of a stage must never arrive before the current use is complete.
     // (A K stage is freed by the S commits, which follow its landing.)
+    // Only lane 0 issues MMAs and commits; the other lanes meet it again at
+    // the next warp-wide wait, which converges the warp.
     auto release = [&](int bar) {
       if (lane == 0) tc_commit(&bars[bar]);
-      __syncwarp();
     };
     if (ok && ntiles > 0) {
       if ((ok = mbar_wait_warp(&bars[B::kKFull], 0, s_abort))) {
@@ -368,7 +367,9 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
             if (!k_next && !(ok = mbar_wait_warp(&bars[B::kKFull + (j + 1) % kKSt], ((j + 1) / kKSt) & 1, s_abort)))
               break;
             k_next = true;
-            tc_fence_after();
+            // No tcgen05 fence: TMA data is ordered by the K barrier, and the P
+            // wait above already ordered the softmax's TMEM writes before this
+            // thread's MMAs, which the tensor pipe runs in issue order.
             issue_s(t, j + 1);
           }
         }
