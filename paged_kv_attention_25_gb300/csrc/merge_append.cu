@@ -24,18 +24,22 @@ __global__ void __launch_bounds__(128) merge_kernel(const AttnArgs a, const Merg
 // (fixed-size blocks in non-contiguous memory, "LLM上下文缓存与状态复用机制的分析和探索",
 // section 3.1).  Consecutive threads copy consecutive chunks of one row, so both
 // the read of the new rows and the write into the block are coalesced.
+// Idx: the chunk index type, 32-bit whenever the batch's chunks fit (integer
+// division is far cheaper there); chunks_per_row (D / 8) is a power of two.
+template <typename Idx>
 __global__ void __launch_bounds__(256) append_kernel(uint4* __restrict__ kp, uint4* __restrict__ vp, int num_blocks,
-                                                     int hkv, int chunks_per_row, const int32_t* __restrict__ bt,
+                                                     int hkv, int cpr_log2, const int32_t* __restrict__ bt,
                                                      int max_blocks, int num_reqs, const int32_t* __restrict__ cu,
                                                      const int32_t* __restrict__ pos, const uint4* __restrict__ k_new,
                                                      const uint4* __restrict__ v_new, int num_tokens, unsigned* err) {
-  const int64_t total = static_cast<int64_t>(num_tokens) * hkv * chunks_per_row;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(i % chunks_per_row);
-    const int64_t row = i / chunks_per_row;   // t * hkv + g
-    const int g = static_cast<int>(row % hkv);
-    const int t = static_cast<int>(row / hkv);
+  const int chunks_per_row = 1 << cpr_log2;
+  const Idx total = static_cast<Idx>(num_tokens) * static_cast<Idx>(hkv) * static_cast<Idx>(chunks_per_row);
+  for (Idx i = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<Idx>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i & static_cast<Idx>(chunks_per_row - 1));
+    const Idx row = i >> cpr_log2;   // t * hkv + g
+    const int g = static_cast<int>(row % static_cast<Idx>(hkv));
+    const int t = static_cast<int>(row / static_cast<Idx>(hkv));
     int lo = 0, hi = num_reqs - 1;             // last r with cu[r] <= t
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -72,16 +76,24 @@ int launch_append(const PoolView& pool, void* kp, void* vp, const int32_t* bt, i
                   int num_tokens, void* stream) {
   if (num_tokens <= 0) return cudaSuccess;
   const int cpr = pool.head_dim / 8;
+  const int cpr_log2 = cpr == 16 ? 4 : 3;   // head_dim 128 or 64
   const int64_t total = static_cast<int64_t>(num_tokens) * pool.num_kv_heads * cpr;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t want = (total + 255) / 256;
   const int grid = static_cast<int>(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
-  append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<uint4*>(kp), static_cast<uint4*>(vp), pool.num_blocks, pool.num_kv_heads, cpr, bt, max_blocks,
-      num_reqs, cu_q_lens, positions, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), num_tokens,
-      pool.err);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const auto kn = static_cast<const uint4*>(k_new);
+  const auto vn = static_cast<const uint4*>(v_new);
+  if (total + int64_t(grid) * 256 < (int64_t(1) << 31))   // the loop index stays below 2^31 too
+    append_kernel<uint32_t><<<grid, 256, 0, s>>>(static_cast<uint4*>(kp), static_cast<uint4*>(vp), pool.num_blocks,
+                                                 pool.num_kv_heads, cpr_log2, bt, max_blocks, num_reqs, cu_q_lens,
+                                                 positions, kn, vn, num_tokens, pool.err);
+  else
+    append_kernel<uint64_t><<<grid, 256, 0, s>>>(static_cast<uint4*>(kp), static_cast<uint4*>(vp), pool.num_blocks,
+                                                 pool.num_kv_heads, cpr_log2, bt, max_blocks, num_reqs, cu_q_lens,
+                                                 positions, kn, vn, num_tokens, pool.err);
   return cudaGetLastError();
 }
 
