@@ -184,3 +184,46 @@ def test_planner_without_host_positions_covers_whole_context(lib):
             assert its["kv_end"].max() == b.ctx_lens[r]
             # unknown positions: bounds cover the whole context
             assert (its["pos_max0"] == b.ctx_lens[r] - 1).all() and (its["pos_min0"] == 0).all()
+
+
+def _expected_decode_items(batch, num_sms):
+    """Split-KV item count under the planner's rule: the smallest of 1..4 splits per
+    CTA slot (3 per SM) whose items fill two waves, else 4; chunks in 16-key blocks,
+    at least 16 blocks, an even split of each (request, KV head) key range."""
+    G = batch.num_q_heads // batch.num_kv_heads
+    groups = []
+    for r in range(batch.num_reqs):
+        a, b = int(batch.cu_q_lens[r]), int(batch.cu_q_lens[r + 1])
+        if a < b and (b - a) * G <= 4:
+            kv = min(int(batch.ctx_lens[r]), int(batch.q_positions[a:b].max()) + 1)
+            groups.append(-(-kv // 16))
+    if not groups:
+        return 0
+    slots = num_sms * 3
+    total = sum(groups) * batch.num_kv_heads
+
+    def items(chunk):
+        n = 0
+        for u in groups:
+            per = -(-u // max(1, -(-u // chunk)))
+            n += max(1, -(-u // per))
+        return n * batch.num_kv_heads
+
+    chunk_for = lambda s: max(16, -(-total // (slots * s)))
+    for s in (1, 2, 3):
+        if items(chunk_for(s)) >= 2 * slots:
+            return items(chunk_for(s))
+    return items(chunk_for(4))
+
+
+@pytest.mark.parametrize("name", ["llama13b_mixed", "long_skewed_evict", "decode_lognormal_small"])
+def test_split_kv_split_count_fills_two_waves(lib, name):
+    batch = wl.WORKLOADS[name]()
+    meta = pkv.HostMeta(batch.cu_q_lens, batch.ctx_lens, batch.q_positions)
+    _, st = pkv.pkv_plan_inspect(batch.num_q_heads, batch.num_kv_heads, batch.head_dim, 152, meta)
+    assert st["num_decode_items"] == _expected_decode_items(batch, 152)
+    # the headline mix needs no split at all; the 65,536-token request still splits
+    if name == "llama13b_mixed":
+        assert st["num_merge_items"] == 0
+    if name == "long_skewed_evict":
+        assert st["num_decode_items"] >= 2 * 152 * 3 and st["num_merge_items"] > 0

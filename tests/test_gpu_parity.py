@@ -165,6 +165,19 @@ def test_attention_edge_shapes(G, D):
     full_parity(_edge_batch(G, D, seed=40 + G + D))
 
 
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_split_kv_groups_merged_by_their_last_split(G):
+    """Long decodes with 1, 2 or 4 query rows per KV head, cut into many splits: every
+    group is combined inside the split-KV kernel by whichever split finishes last."""
+    reqs = [wl._decode(9000), wl._decode(4100), wl._decode(777), wl._new_turn(3000, 1)]
+    batch = wl.build_batch(f"splits_G{G}", reqs, num_q_heads=2 * G, num_kv_heads=2, head_dim=128, seed=70 + G)
+    meta = pkv.HostMeta(batch.cu_q_lens, batch.ctx_lens, batch.q_positions)
+    _, st = pkv.pkv_plan_inspect(batch.num_q_heads, batch.num_kv_heads, batch.head_dim,
+                                 torch.cuda.get_device_properties(0).multi_processor_count, meta)
+    assert st["num_tc_items"] == 0 and st["num_merge_items"] >= 4
+    full_parity(batch)
+
+
 def test_block_permutation_gives_bit_identical_gpu_output():
     batch = wl.random_small(11, num_q_heads=8, num_kv_heads=2, head_dim=128, max_ctx=1500, max_q=150)
     _, o1, l1 = full_parity(batch)
