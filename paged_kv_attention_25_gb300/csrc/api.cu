@@ -444,17 +444,19 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   const WorkItem* d_tc = reinterpret_cast<const WorkItem*>(ws + pl.off_tc);
   const MergeItem* d_merge = reinterpret_cast<const MergeItem*>(ws + pl.off_merge);
   // The two attention kernels are independent (disjoint outputs and workspace
-  // regions): with both present, one runs on the caller's stream and the
-  // other on the pool's side stream.  The caller's stream is dispatched first
-  // (the side stream waits on the fork event), so it takes the kernel with the
-  // longer estimated time.
+  // regions): with both present, the split-KV kernel runs on the caller's
+  // stream and the tensor-core kernel on the pool's side stream.  The caller's
+  // stream is dispatched first (the side stream waits on the fork event), so
+  // the split-KV CTAs (three per SM) take the SMs and tensor-core CTAs (one SM
+  // each) fill them as the split-KV work drains; that order measured as fast
+  // as or faster than the reverse on every mixed workload.
   const bool fork = !pl.tc.empty() && !pl.decode.empty();
   void* dec_stream = stream;
   void* tc_stream = stream;
   if (fork) {
     PKV_CUDA(cudaEventRecord(pool->fork, s), "fork record");
     PKV_CUDA(cudaStreamWaitEvent(pool->side, pool->fork, 0), "fork wait");
-    (pl.decode_first ? tc_stream : dec_stream) = pool->side;
+    tc_stream = pool->side;
   }
   if (!pl.decode.empty()) {
     rc = timed_launch(pool, 1, dec_stream,

@@ -75,9 +75,6 @@ struct Plan {
   pkv_plan_stats stats{};
   // Workspace layout (byte offsets, 256-aligned sections).
   size_t off_decode = 0, off_tc = 0, off_merge = 0, off_merge_dec = 0, off_merge_cnt = 0, off_part_o = 0, off_part_lse = 0, total = 0;
-  // With both kernels present: the split-KV kernel's estimated time exceeds the
-  // tensor-core kernel's, so it is the one launched first (on the caller's stream).
-  bool decode_first = false;
   uint64_t signature = 0;
   bool valid = false;
 };

@@ -15,7 +15,6 @@
 // item per KV head); every other request goes to the tensor-core kernel in
 // tiles of at most 128 query rows.
 #include <algorithm>
-#include <cmath>
 #include <cstring>
 
 #include "internal.h"
@@ -38,14 +37,6 @@ constexpr int kDecodeSplitsPerSlot = 4;
 constexpr int kDecodeMinWaves = 2;
 constexpr int kTcSplitsPerSlot = 1;
 constexpr int kMinDecodeChunk = 16;     // blocks (256 keys) per split at least
-// Time estimates that order the two attention kernels (GB300, measured): the
-// split-KV kernel streams at about the HBM copy rate; a tensor-core item takes
-// a fixed time plus a time per 128-key tile (pairs of query tiles, and single
-// tiles about 10% faster per tile; D = 64 about 0.6 of D = 128 per tile).
-constexpr double kDecodeGBs = 6500.0;
-constexpr double kTcPairFixedNs = 4600.0;
-constexpr double kTcSingleFixedNs = 400.0;
-constexpr double kTcTileNs = 2200.0;
 constexpr int kMinTcChunk = 4;          // 128-key tiles (512 keys) per split at least
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -306,20 +297,6 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   st.decode_io_bytes = io_bytes(dec_groups);
   st.tc_io_bytes = io_bytes(tc_groups);
 
-  // Launch order.  The kernel launched first takes the SMs and the other fills
-  // in as its CTAs retire, so the longer one goes first: its tail then
-  // overlaps the shorter one instead of extending the step.
-  if (!plan->decode.empty() && !plan->tc.empty()) {
-    const double per_tile = D == 128 ? kTcTileNs : kTcTileNs * 0.6;
-    double w_tc = 0;   // ns of one SM
-    for (const auto& w : plan->tc) {
-      const double tiles = std::ceil((w.kv_end - w.kv_start) / double(kTcKeys));
-      w_tc += w.q_count2 > 0 ? kTcPairFixedNs + per_tile * tiles : kTcSingleFixedNs + 0.9 * per_tile * tiles;
-    }
-    const double t_tc = w_tc / std::max(1, pp.num_sms);
-    const double t_dec = double(st.decode_kv_bytes + st.decode_io_bytes) / kDecodeGBs;   // bytes / (GB/s) = ns
-    plan->decode_first = t_dec > t_tc;
-  }
 
   // 5. Workspace layout.
   size_t off = 0;
