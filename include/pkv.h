@@ -248,6 +248,26 @@ int pkv_last_plan_stats(const pkv_pool* pool, pkv_plan_stats* out);
 int pkv_swap_out(pkv_pool* pool, const int32_t* block_ids, int n, void* host_buf, void* stream);
 int pkv_swap_in(pkv_pool* pool, const int32_t* block_ids, int n, const void* host_buf, void* stream);
 
+/*
+ * Copy `bytes` bytes between device memory and host memory, asynchronously on
+ * `stream`: for moving a step's inputs in and its outputs out next to the
+ * attention kernels.  With pinned host memory (cudaHostAlloc / registered) a
+ * kernel on a few SMs moves the bytes through the host memory's device
+ * mapping (24 CTAs to the device, 8 to the host: about the CPU-GPU link's rate
+ * either way).  Beside the HBM-bound attention kernels alone such a copy
+ * slows them far less than a copy-engine transfer of the same bytes (measured
+ * on GB300: a 68 MB input copy beside a 200 us attention step, 363 us per step
+ * against 438 us); in a pipelined loop that also moves outputs and swaps,
+ * copy-engine transfers measured faster, as the copy kernels then hold SMs the
+ * tensor-core kernel needs.  With pageable host memory the call falls back to
+ * cudaMemcpyAsync.
+ * Any sizes and alignments are accepted (16-byte chunks where both ends are
+ * 16-byte aligned, bytes otherwise).  Errors: PKV_EINVAL for NULL pointers
+ * with bytes > 0, PKV_ECUDA for a failed launch or copy.
+ */
+int pkv_copy_to_device(void* dst, const void* host_src, size_t bytes, void* stream);
+int pkv_copy_to_host(void* host_dst, const void* src, size_t bytes, void* stream);
+
 /* Synchronise `stream`, read the device error word into *flags (may be NULL)
  * and clear it.  Returns PKV_EDEVICE if any bit was set (PKV_ETIMEOUT if the
  * timeout bit was), else PKV_OK. */

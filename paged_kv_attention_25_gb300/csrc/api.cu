@@ -562,6 +562,40 @@ int pkv_swap_in(pkv_pool* pool, const int32_t* block_ids, int n, const void* hos
   return swap_impl(pool, block_ids, n, const_cast<void*>(host_buf), false, stream);
 }
 
+// Host memory's device address if it is pinned and mapped, else nullptr.
+static void* mapped_device_address(const void* host) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, host) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
+      attr.devicePointer != nullptr)
+    return attr.devicePointer;
+  cudaGetLastError();   // clear a failed query on pageable memory
+  return nullptr;
+}
+
+static int host_copy(void* dev, const void* host, size_t bytes, bool to_host, void* stream) {
+  if (bytes == 0) return PKV_OK;
+  if (!dev || !host) return fail(PKV_EINVAL, "NULL pointer");
+  void* host_dev = mapped_device_address(host);
+  cudaError_t e;
+  if (host_dev) {
+    e = static_cast<cudaError_t>(to_host ? launch_host_copy(host_dev, dev, bytes, true, stream)
+                                         : launch_host_copy(dev, host_dev, bytes, false, stream));
+  } else {
+    e = cudaMemcpyAsync(to_host ? const_cast<void*>(host) : dev, to_host ? dev : host, bytes,
+                        to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  }
+  if (e != cudaSuccess) return cuda_fail(e, to_host ? "copy to host" : "copy to device");
+  return PKV_OK;
+}
+
+int pkv_copy_to_device(void* dst, const void* host_src, size_t bytes, void* stream) {
+  return host_copy(dst, host_src, bytes, false, stream);
+}
+
+int pkv_copy_to_host(void* host_dst, const void* src, size_t bytes, void* stream) {
+  return host_copy(const_cast<void*>(src), host_dst, bytes, true, stream);
+}
+
 int pkv_check_device_errors(pkv_pool* pool, void* stream, unsigned* flags) {
   if (!pool) return fail(PKV_EINVAL, "pool is NULL");
   PKV_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "cudaStreamSynchronize");

@@ -100,6 +100,8 @@ struct SwapIds {
   int32_t id[kSwapIdsPerLaunch];
 };
 
+// dst / src device addresses (host memory through its device mapping); any sizes.
+int launch_host_copy(void* dst, const void* src, size_t bytes, bool to_host, void* stream);
 int launch_swap(const PoolView& pool, void* kp, void* vp, void* host_dev, const int32_t* ids, int n, bool to_host,
                 int num_sms, void* stream);
 

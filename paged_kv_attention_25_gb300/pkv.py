@@ -41,7 +41,7 @@ EXPORTED = (
     "pkv_paged_attn_workspace_size", "pkv_paged_attn", "pkv_paged_attn_static", "pkv_last_plan_stats",
     "pkv_plan_inspect", "pkv_swap_out", "pkv_swap_in", "pkv_check_device_errors",
     "pkv_profile_enable", "pkv_profile_read", "pkv_device_sm_count", "pkv_last_error",
-    "pkv_version",
+    "pkv_version", "pkv_copy_to_device", "pkv_copy_to_host",
 )
 
 
@@ -117,6 +117,8 @@ def load_library():
             "pkv_profile_enable": [P, I],
             "pkv_profile_read": [P, ctypes.POINTER(pkv_profile), I],
             "pkv_device_sm_count": [ctypes.POINTER(I)],
+            "pkv_copy_to_device": [P, P, ctypes.c_size_t, P],
+            "pkv_copy_to_host": [P, P, ctypes.c_size_t, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -344,6 +346,31 @@ def pkv_swap_out(pool: Pool, block_ids, host_buf: torch.Tensor, stream=None):
     _check_host_buf(pool, host_buf, ids.shape[0])
     _check(load_library().pkv_swap_out(pool.handle, ids.ctypes.data, ids.shape[0], host_buf.data_ptr(),
                                         _stream(stream)))
+
+
+def _same_bytes(a: torch.Tensor, b: torch.Tensor):
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise TypeError("tensors must be contiguous")
+    n = a.numel() * a.element_size()
+    if n != b.numel() * b.element_size():
+        raise ValueError("tensors differ in size")
+    return n
+
+
+def pkv_copy_to_device(dst: torch.Tensor, host_src: torch.Tensor, stream=None):
+    """dst (CUDA) <- host_src (CPU; pinned for the kernel path), asynchronously on `stream`."""
+    if not dst.is_cuda or host_src.is_cuda:
+        raise TypeError("dst must be a CUDA tensor and host_src a CPU tensor")
+    _check(load_library().pkv_copy_to_device(dst.data_ptr(), host_src.data_ptr(), _same_bytes(dst, host_src),
+                                             _stream(stream)))
+
+
+def pkv_copy_to_host(host_dst: torch.Tensor, src: torch.Tensor, stream=None):
+    """host_dst (CPU; pinned for the kernel path) <- src (CUDA), asynchronously on `stream`."""
+    if host_dst.is_cuda or not src.is_cuda:
+        raise TypeError("host_dst must be a CPU tensor and src a CUDA tensor")
+    _check(load_library().pkv_copy_to_host(host_dst.data_ptr(), src.data_ptr(), _same_bytes(host_dst, src),
+                                           _stream(stream)))
 
 
 def pkv_swap_in(pool: Pool, block_ids, host_buf: torch.Tensor, stream=None):

@@ -309,6 +309,28 @@ def sampled_rows(batch, n, seed):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("nbytes,offset", [(1 << 20, 0), (12345, 0), (4099, 3), (16, 0), (0, 0)])
+def test_host_copies_bit_exact(pinned, nbytes, offset):
+    """pkv_copy_to_device / pkv_copy_to_host: every byte, aligned or not, kernel (pinned) or DMA path."""
+    rng = np.random.default_rng(nbytes + offset)
+    src = torch.from_numpy(rng.integers(0, 256, nbytes + offset + 8, dtype=np.uint8))
+    if pinned:
+        src = src.pin_memory()
+    dev = torch.full((nbytes + offset + 8,), 7, dtype=torch.uint8, device="cuda")
+    pkv.pkv_copy_to_device(dev[offset:offset + nbytes], src[offset:offset + nbytes])
+    back = torch.zeros(nbytes + offset + 8, dtype=torch.uint8)
+    if pinned:
+        back = back.pin_memory()
+    pkv.pkv_copy_to_host(back[offset:offset + nbytes], dev[offset:offset + nbytes])
+    torch.cuda.synchronize()
+    d = dev.cpu().numpy()
+    assert np.array_equal(d[offset:offset + nbytes], src.numpy()[offset:offset + nbytes])
+    assert (d[:offset] == 7).all() and (d[offset + nbytes:] == 7).all()   # nothing outside the range
+    assert np.array_equal(back.numpy()[offset:offset + nbytes], src.numpy()[offset:offset + nbytes])
+    assert (back.numpy()[offset + nbytes:] == 0).all()
+
+
 @pytest.mark.parametrize("name", ["llama13b_mixed", "decode_lognormal", "llama70b_gqa", "long_skewed_evict"])
 def test_full_size_workloads_sampled(name):
     batch = wl.WORKLOADS[name]()
