@@ -268,6 +268,53 @@ int pkv_swap_in(pkv_pool* pool, const int32_t* block_ids, int n, const void* hos
 int pkv_copy_to_device(void* dst, const void* host_src, size_t bytes, void* stream);
 int pkv_copy_to_host(void* host_dst, const void* src, size_t bytes, void* stream);
 
+/*
+ * Two-tier block manager (host only, no GPU calls): which KV blocks of which
+ * conversation live in the GPU pool (`gpu_blocks` physical blocks), in CPU
+ * host slots (`cpu_blocks` slots of one [cpu_blocks][2][Hkv][16][D] pinned
+ * buffer), or nowhere, and what each step must swap and recompute.  Pensieve
+ * (abstract) evicts cached history by conversation activity and recompute
+ * cost, at block granularity, and recomputes what was lost; the reading taken
+ * here:
+ *   - recompute cost of a token at position p = token_cost + p + 1 (fixed
+ *     per-token work in units of one key's attention, plus attention over its
+ *     p + 1 keys), so leading blocks are the cheapest to recompute;
+ *   - a conversation's blocks are, by position, [dropped][CPU][GPU]: eviction
+ *     moves an idle conversation's leading GPU block to the CPU tier (or drops
+ *     it when there is no CPU tier), and a full CPU tier drops its leading
+ *     block, so what must be recomputed is always a prefix [0, e);
+ *   - the victim is the conversation not in the step whose leading block has
+ *     the highest (steps since its last request) / (recompute cost); ties go
+ *     to the lower id.
+ * pkv_cache_step plans one step for n distinct conversations (conv_ids >= 0;
+ * an unknown id starts a new, empty conversation) that each add new_tokens[r]
+ * tokens, and fills:
+ *   - block_tables [n][max_blocks]: the conversation's pool blocks in position
+ *     order, -1 past ceil(ctx_lens[r] / 16);
+ *   - ctx_lens [n]: tokens after the step;
+ *   - recompute [n]: leading tokens [0, recompute[r]) to recompute this step
+ *     (query positions [0, recompute) U [old length, ctx_lens)), whose blocks
+ *     are fresh;
+ *   - swap_out [num_swap_out][2] = (pool block, host slot) and
+ *     swap_in [num_swap_in][2] = (host slot, pool block), each at most
+ *     swap_cap pairs.
+ * The caller runs every swap-out, then every swap-in, then appends the step's
+ * tokens (recomputed and new): a block freed by a swap-out may be reused in
+ * the same step.  Errors: PKV_EINVAL for bad arguments (a repeated id, a
+ * conversation longer than max_blocks blocks, more swaps than swap_cap),
+ * PKV_ENOMEM if the step's conversations cannot fit in the pool even after
+ * evicting every other conversation; on an error the manager is unchanged.
+ * pkv_cache_release forgets a conversation and frees its blocks and slots.
+ */
+typedef struct pkv_cache pkv_cache;
+int pkv_cache_create(int gpu_blocks, int cpu_blocks, float token_cost, pkv_cache** out);
+int pkv_cache_destroy(pkv_cache* cache);
+int pkv_cache_step(pkv_cache* cache, const int32_t* conv_ids, const int32_t* new_tokens, int n,
+                   int32_t* block_tables, int max_blocks, int32_t* ctx_lens, int32_t* recompute,
+                   int32_t* swap_out, int* num_swap_out, int32_t* swap_in, int* num_swap_in, int swap_cap);
+int pkv_cache_release(pkv_cache* cache, int conv);
+int pkv_cache_free_blocks(const pkv_cache* cache, int* gpu_free, int* cpu_free);
+
 /* Synchronise `stream`, read the device error word into *flags (may be NULL)
  * and clear it.  Returns PKV_EDEVICE if any bit was set (PKV_ETIMEOUT if the
  * timeout bit was), else PKV_OK. */

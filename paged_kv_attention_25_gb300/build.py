@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
-SOURCES = ["api.cu", "plan.cpp", "decode.cu", "attn_tc.cu", "merge_append.cu", "attn_static.cu", "swap.cu"]
+SOURCES = ["api.cu", "plan.cpp", "cache.cpp", "decode.cu", "attn_tc.cu", "merge_append.cu", "attn_static.cu", "swap.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -42,6 +42,7 @@ EXPORTED = (
     "pkv_plan_inspect", "pkv_swap_out", "pkv_swap_in", "pkv_check_device_errors",
     "pkv_profile_enable", "pkv_profile_read", "pkv_device_sm_count", "pkv_last_error",
     "pkv_version", "pkv_copy_to_device", "pkv_copy_to_host",
+    "pkv_cache_create", "pkv_cache_destroy", "pkv_cache_step", "pkv_cache_release", "pkv_cache_free_blocks",
 )
 
 
@@ -119,6 +120,11 @@ def load_library():
             "pkv_device_sm_count": [ctypes.POINTER(I)],
             "pkv_copy_to_device": [P, P, ctypes.c_size_t, P],
             "pkv_copy_to_host": [P, P, ctypes.c_size_t, P],
+            "pkv_cache_create": [I, I, F, ctypes.POINTER(P)],
+            "pkv_cache_destroy": [P],
+            "pkv_cache_step": [P, P, P, I, P, I, P, P, P, ctypes.POINTER(I), P, ctypes.POINTER(I), I],
+            "pkv_cache_release": [P, I],
+            "pkv_cache_free_blocks": [P, ctypes.POINTER(I), ctypes.POINTER(I)],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -346,6 +352,52 @@ def pkv_swap_out(pool: Pool, block_ids, host_buf: torch.Tensor, stream=None):
     _check_host_buf(pool, host_buf, ids.shape[0])
     _check(load_library().pkv_swap_out(pool.handle, ids.ctypes.data, ids.shape[0], host_buf.data_ptr(),
                                         _stream(stream)))
+
+
+class Cache:
+    """Two-tier (GPU pool / CPU host slots) block manager for conversations; host only."""
+
+    def __init__(self, gpu_blocks: int, cpu_blocks: int, token_cost: float = 0.0):
+        lib = load_library()
+        h = ctypes.c_void_p()
+        _check(lib.pkv_cache_create(gpu_blocks, cpu_blocks, float(token_cost), ctypes.byref(h)))
+        self.handle = h
+        self.gpu_blocks, self.cpu_blocks = gpu_blocks, cpu_blocks
+
+    def step(self, conv_ids, new_tokens, max_blocks: int):
+        """Plan one step; returns dict(block_tables [n, max_blocks], ctx_lens, recompute,
+        swap_out [k, 2] (pool block, host slot), swap_in [m, 2] (host slot, pool block))."""
+        ids, nt = _host_i32(conv_ids), _host_i32(new_tokens)
+        n = ids.shape[0]
+        cap = self.gpu_blocks + self.cpu_blocks + 1
+        bt = np.full((max(n, 1), max_blocks), -1, np.int32)
+        ctx, rec = np.zeros(max(n, 1), np.int32), np.zeros(max(n, 1), np.int32)
+        so, si = np.zeros((cap, 2), np.int32), np.zeros((cap, 2), np.int32)
+        nso, nsi = ctypes.c_int(), ctypes.c_int()
+        _check(load_library().pkv_cache_step(self.handle, ids.ctypes.data, nt.ctypes.data, n, bt.ctypes.data,
+                                             max_blocks, ctx.ctypes.data, rec.ctypes.data, so.ctypes.data,
+                                             ctypes.byref(nso), si.ctypes.data, ctypes.byref(nsi), cap))
+        return {"block_tables": bt[:n], "ctx_lens": ctx[:n], "recompute": rec[:n],
+                "swap_out": so[:nso.value].copy(), "swap_in": si[:nsi.value].copy()}
+
+    def release(self, conv: int):
+        _check(load_library().pkv_cache_release(self.handle, int(conv)))
+
+    def free_blocks(self):
+        g, c = ctypes.c_int(), ctypes.c_int()
+        _check(load_library().pkv_cache_free_blocks(self.handle, ctypes.byref(g), ctypes.byref(c)))
+        return g.value, c.value
+
+    def close(self):
+        if self.handle:
+            load_library().pkv_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def _same_bytes(a: torch.Tensor, b: torch.Tensor):
