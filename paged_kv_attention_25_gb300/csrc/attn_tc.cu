@@ -150,23 +150,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     mbar_init(&bars[B::kDrain], 1);
     *s_abort = 0;
     fence_mbar_init();
-    // Both query tiles by TMA, first of all copies: rows (token, head) of the
-    // tile land as [half][row][64 columns] (rows past the tile are other
-    // tokens' rows or zeros, computed and never stored).
-    prefetch_tmap(&tmap_q);
-    const uint32_t qbytes = static_cast<uint32_t>(D * 2 * G * a.q_box_tokens);
-    for (int t = 0; t < 2; ++t) {
-      if (rows[t] > 0) {
-        mbar_arrive_expect_tx(&bars[B::kQ + t], qbytes);
-        uint8_t* qt = smem + S::kOffQ + t * S::kQ;
-#pragma unroll
-        for (int hf = 0; hf < S::kHalves; ++hf)
-          tma_load_3d(qt + hf * (kTcRows * 128), &tmap_q, hf * 64, g * G, tok0[t], &bars[B::kQ + t]);
-      } else {
-        mbar_arrive(&bars[B::kQ + t]);
-      }
-    }
   }
+  if (warp == 9 && lane == 0) prefetch_tmap(&tmap_q);
   if (warp == 8 && lane == 0) {
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
@@ -295,6 +280,26 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     // apart (leading offset) and 8-key groups kGS apart (stride offset).
     const uint64_t dk = make_sdesc_sw128(sK, 16, S::kGS);
     const uint64_t dv = make_sdesc_sw128(sV, S::kHS, S::kGS);
+    // Both query tiles by TMA, issued here rather than before the CTA barrier:
+    // the copy's first use of the per-call tensor map takes a few thousand
+    // cycles, which the producers' first K/V copies need not wait for.  Rows
+    // (token, head) of a tile land as [half][row][64 columns] (rows past the
+    // tile are other tokens' rows or zeros, computed and never stored).
+    if (lane == 0) {
+      const uint32_t qbytes = static_cast<uint32_t>(D * 2 * G * a.q_box_tokens);
+      for (int t = 0; t < 2; ++t) {
+        if (rows[t] > 0) {
+          mbar_arrive_expect_tx(&bars[B::kQ + t], qbytes);
+          uint8_t* qt = smem + S::kOffQ + t * S::kQ;
+#pragma unroll
+          for (int hf = 0; hf < S::kHalves; ++hf)
+            tma_load_3d(qt + hf * (kTcRows * 128), &tmap_q, hf * 64, g * G, tok0[t], &bars[B::kQ + t]);
+        } else {
+          mbar_arrive(&bars[B::kQ + t]);
+        }
+      }
+    }
+    __syncwarp();
     bool ok = mbar_wait_warp(&bars[B::kQ], 0, s_abort) && mbar_wait_warp(&bars[B::kQ + 1], 0, s_abort);
     const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
     // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage).
