@@ -51,6 +51,9 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--swap-layers", type=int, default=4,
+                   help="layers (one pool each) of the layer-pipelined swap-in measurement; 0 skips it")
+    p.add_argument("--swap-steps", type=int, default=20)
     return p.parse_args(argv)
 
 
@@ -430,6 +433,72 @@ def run_ours(args):
     torch.cuda.synchronize()
     swap_out_gbs = sh.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
     swap_in_gbs = sh.numel() * 2 / (e1.elapsed_time(e2) / 1e3) / 1e9
+    del sh
+
+    # ---- layer-pipelined swap-in.  L layers, each its own pool holding the
+    # same KV, each getting back the step's swapped-out conversation history
+    # (swap_ids, swapped in from a pinned host copy of the same blocks, so the
+    # attention inputs do not change).  Three ways of running a step:
+    #   compute: every layer's append + attention, no swap-in;
+    #   serial:  per layer, the swap kernel brings the blocks in, then append +
+    #            attention (the swap-in sits on the critical path);
+    #   ahead:   every layer's pkv_swap_in_ahead on one copy stream at the
+    #            start of the step, then the layers in order, each waiting only
+    #            for its own blocks.
+    pipe = None
+    if args.swap_layers > 0:
+        layers = [(pool, ws)]
+        for _ in range(args.swap_layers - 1):
+            p = pkv.Pool(batch.num_blocks, batch.num_kv_heads, D, device=dev)
+            p.k.copy_(pool.k)
+            p.v.copy_(pool.v)
+            layers.append((p, p.workspace(pkv.pkv_paged_attn_workspace_size(p, Hq, meta))))
+        hosts = [torch.empty_like(swap_host).pin_memory() for _ in layers]
+        for (p, _), h in zip(layers, hosts):
+            pkv.pkv_swap_out(p, swap_ids, h)
+        cstream = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize()
+
+        def layer_step(p, w):
+            pkv.pkv_append(p, d["block_tables"], d["cu_q_lens"], d["q_positions"], d["k_new"], d["v_new"])
+            pkv.pkv_paged_attn(p, d["q"], d["q_positions"], d["block_tables"], d["ctx_lens"], d["cu_q_lens"],
+                               meta, batch.scale, out=out, lse=lse, workspace=w)
+
+        def run_mode(mode):
+            if mode == "ahead":
+                for (p, _), h in zip(layers, hosts):
+                    pkv.pkv_swap_in_ahead(p, swap_ids, h, cstream, stream=main)
+            for (p, w), h in zip(layers, hosts):
+                if mode == "serial":
+                    pkv.pkv_swap_in(p, swap_ids, h)
+                layer_step(p, w)
+
+        modes = ("compute", "serial", "ahead")
+        for m in modes:
+            for _ in range(3):
+                run_mode(m)
+        torch.cuda.synchronize()
+        times = {m: [] for m in modes}
+        for i in range(args.swap_steps):
+            for m in modes:   # interleaved, so that clock drift hits every mode alike
+                l2_flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(main)
+                run_mode(m)
+                b.record(main)
+                times[m].append((a, b))
+        torch.cuda.synchronize()
+        ms = {m: float(np.median([a.elapsed_time(b) for a, b in times[m]])) for m in modes}
+        for p, _ in layers:
+            if pkv.pkv_check_device_errors(p) != 0:
+                raise RuntimeError("device error word set in the swap-in pipeline")
+        exposed = ms["serial"] - ms["compute"]
+        pipe = {"layers": len(layers), "swap_in_bytes_per_layer": swap_bytes, "steps": args.swap_steps,
+                "ms_per_step_median": ms,
+                "swap_in_hidden_frac": (ms["serial"] - ms["ahead"]) / exposed if exposed > 0 else None}
+        for p, _ in layers[1:]:
+            p.close()
+        del layers, hosts
 
     if rank != 0:
         if world > 1:
@@ -487,7 +556,8 @@ def run_ours(args):
         "gpu_launches": int(sum(v["launches"] for v in prof.values())),
         "roofline": roof,
         "e2e": {"value": e_tok / e_sec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "swap": {"out_gbs": swap_out_gbs, "in_gbs": swap_in_gbs, "bytes": sh.numel() * 2},
+        "swap": {"out_gbs": swap_out_gbs, "in_gbs": swap_in_gbs, "bytes": len(ids) * 2 * batch.num_kv_heads * 16 * D * 2},
+        "swap_in_pipeline": pipe,
         "clocks": clk.summary(),
         "wall_s_timed": wall1 - wall0,
     }

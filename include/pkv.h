@@ -249,6 +249,39 @@ int pkv_swap_out(pkv_pool* pool, const int32_t* block_ids, int n, void* host_buf
 int pkv_swap_in(pkv_pool* pool, const int32_t* block_ids, int n, const void* host_buf, void* stream);
 
 /*
+ * Ahead-of-time swap-in (Pensieve method summary: ahead-of-time swapping and
+ * pipelined data transfer that overlap data movement with computation).
+ * pkv_swap_in_ahead starts a copy-engine transfer of host_buf
+ * ([n][2][Hkv][B][D], the pkv_swap_in layout; pinned for the transfer to be
+ * asynchronous) into a device staging buffer that the pool owns, on
+ * `copy_stream`, and returns.  The transfer starts after the work queued on
+ * `stream` before this call (for instance the swap-out that filled
+ * host_buf), so it takes no SMs and overlaps whatever the caller queues next.
+ * The blocks land in the pool at the start of the pool's next call that reads
+ * or writes it (pkv_append, pkv_paged_attn, pkv_swap_out, pkv_swap_in,
+ * another pkv_swap_in_ahead) or at pkv_swap_in_finish: that call's stream
+ * waits for the transfer, and a kernel scatters the staged blocks into
+ * block_ids.  Until then the pool's blocks keep their old contents, so calls
+ * take effect in call order; read the storage from pkv_pool_kv_ptrs only
+ * after pkv_swap_in_finish.
+ * Layer pipelining: with one pool per model layer, issue every layer's
+ * pkv_swap_in_ahead on one copy stream at the start of a step, then the
+ * layers' attention in order on the compute stream; layer l then waits only
+ * for its own blocks, and the transfers of later layers overlap the
+ * attention of earlier ones.
+ * The staging buffer grows (cudaMalloc, synchronising the device) when a call
+ * moves more blocks than any earlier one on the pool; n * 2 * Hkv * B * D * 2
+ * bytes.  host_buf must stay valid until the transfer has completed (a
+ * stream or event synchronisation on copy_stream, or the landing call's
+ * completion).  block_ids is a HOST array, copied by the call.
+ * Errors: PKV_EINVAL (NULL pool, ids or buffer with n > 0; an id outside the
+ * pool; nothing is started), PKV_ENOMEM (staging allocation), PKV_ECUDA.
+ */
+int pkv_swap_in_ahead(pkv_pool* pool, const int32_t* block_ids, int n, const void* host_buf, void* copy_stream,
+                      void* stream);
+int pkv_swap_in_finish(pkv_pool* pool, void* stream);
+
+/*
  * Copy `bytes` bytes between device memory and host memory, asynchronously on
  * `stream`: for moving a step's inputs in and its outputs out next to the
  * attention kernels.  With pinned host memory (cudaHostAlloc / registered) a

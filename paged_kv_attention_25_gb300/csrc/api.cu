@@ -90,6 +90,15 @@ struct pkv_pool {
   // the attention call (the append, typically); the kernels wait on up_done.
   cudaStream_t copy = nullptr;
   cudaEvent_t up_done = nullptr, ws_free = nullptr;
+  // Ahead-of-time swap-in: the copy engines bring the blocks into a device
+  // staging buffer on the caller's copy stream (swap_ready), and the pool's
+  // next call scatters them into place on its own stream (staged_free).
+  std::mutex swap_mu;
+  void* swap_staging = nullptr;
+  size_t swap_staging_bytes = 0;
+  cudaEvent_t swap_ready = nullptr, swap_staged_free = nullptr, swap_after = nullptr;
+  bool swap_pending = false;
+  std::vector<int32_t> swap_ids;
 
   // profiling
   bool prof_on = false;
@@ -304,6 +313,9 @@ int pkv_pool_destroy(pkv_pool* pool) {
   cudaStreamDestroy(pool->copy);
   cudaEventDestroy(pool->up_done);
   cudaEventDestroy(pool->ws_free);
+  if (pool->swap_staging) cudaFree(pool->swap_staging);
+  for (cudaEvent_t e : {pool->swap_ready, pool->swap_staged_free, pool->swap_after})
+    if (e) cudaEventDestroy(e);
 
   for (auto& r : pool->pending) {
     cudaEventDestroy(r.a);
@@ -321,6 +333,25 @@ int pkv_pool_kv_ptrs(const pkv_pool* pool, void** k, void** v) {
   return PKV_OK;
 }
 
+// Lands a pending ahead-of-time swap-in on `stream`: waits for its transfer,
+// then scatters the staged blocks into the pool (every block at full HBM
+// rate, on up to one CTA per SM).  Every call that reads or writes the pool
+// starts with this, so the blocks are in place before the call's kernels.
+static int finish_swap_in(pkv_pool* pool, void* stream) {
+  std::lock_guard<std::mutex> lk(pool->swap_mu);
+  if (!pool->swap_pending) return PKV_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PKV_CUDA(cudaStreamWaitEvent(s, pool->swap_ready, 0), "swap-in wait");
+  const int rc = timed_launch(pool, 4, stream, [&] {
+    return launch_swap(pool->view(), pool->k, pool->v, pool->swap_staging, pool->swap_ids.data(),
+                       static_cast<int>(pool->swap_ids.size()), false, pool->num_sms, stream);
+  });
+  if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "swap-in scatter launch");
+  PKV_CUDA(cudaEventRecord(pool->swap_staged_free, s), "swap-in release");
+  pool->swap_pending = false;
+  return PKV_OK;
+}
+
 int pkv_append(pkv_pool* pool, const int32_t* block_tables, int max_blocks, int num_reqs, const int32_t* cu_q_lens,
                const int32_t* positions, const void* k_new, const void* v_new, int num_tokens, void* stream) {
   if (!pool) return fail(PKV_EINVAL, "pool is NULL");
@@ -330,8 +361,10 @@ int pkv_append(pkv_pool* pool, const int32_t* block_tables, int max_blocks, int 
   if (!block_tables || !cu_q_lens || !positions || !k_new || !v_new) return fail(PKV_EINVAL, "NULL device pointer");
   if (!aligned16(k_new) || !aligned16(v_new)) return fail(PKV_EINVAL, "k_new / v_new must be 16-byte aligned");
   if (static_cast<int64_t>(max_blocks) * kBlockSize > (1ll << 31)) return fail(PKV_EINVAL, "max_blocks too large");
+  int rc = finish_swap_in(pool, stream);
+  if (rc) return rc;
   PoolView pv = pool->view();
-  int rc = timed_launch(pool, 0, stream, [&] {
+  rc = timed_launch(pool, 0, stream, [&] {
     return launch_append(pv, pool->k, pool->v, block_tables, max_blocks, num_reqs, cu_q_lens, positions, k_new,
                          v_new, num_tokens, stream);
   });
@@ -377,8 +410,10 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   if (!q || !q_positions || !block_tables || !ctx_lens || !cu_q_lens || !o) return fail(PKV_EINVAL, "NULL device pointer");
   if (!aligned16(q) || !aligned16(o)) return fail(PKV_EINVAL, "q and o must be 16-byte aligned");
   if (!(scale > 0.f)) return fail(PKV_EINVAL, "scale must be positive");
+  int rc = finish_swap_in(pool, stream);
+  if (rc) return rc;
   std::lock_guard<std::mutex> lk(pool->mu);
-  int rc = plan_for(pool, num_q_heads, num_reqs, num_tokens, max_blocks, host_meta);
+  rc = plan_for(pool, num_q_heads, num_reqs, num_tokens, max_blocks, host_meta);
   if (rc) return rc;
   const Plan& pl = pool->plan;
   if (!workspace || workspace_bytes < pl.total) return fail(PKV_EINVAL, "workspace missing or smaller than pkv_paged_attn_workspace_size()");
@@ -522,6 +557,8 @@ static int swap_impl(pkv_pool* pool, const int32_t* ids, int n, void* host, bool
   if (!ids || !host) return fail(PKV_EINVAL, "NULL block_ids or host buffer");
   for (int i = 0; i < n; ++i)
     if (ids[i] < 0 || ids[i] >= pool->num_blocks) return fail(PKV_EINVAL, "block id outside the pool");
+  const int frc = finish_swap_in(pool, stream);
+  if (frc) return frc;
   const size_t blk = static_cast<size_t>(pool->num_kv_heads) * kBlockSize * pool->head_dim * 2;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Pinned (page-locked, device-mapped) host memory: one kernel moves every block.
@@ -529,7 +566,7 @@ static int swap_impl(pkv_pool* pool, const int32_t* ids, int n, void* host, bool
   if (cudaPointerGetAttributes(&attr, host) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
       attr.devicePointer != nullptr && (reinterpret_cast<uintptr_t>(attr.devicePointer) & 15u) == 0) {
     const int rc = timed_launch(pool, 4, stream, [&] {
-      return launch_swap(pool->view(), pool->k, pool->v, attr.devicePointer, ids, n, out, pool->num_sms, stream);
+      return launch_swap(pool->view(), pool->k, pool->v, attr.devicePointer, ids, n, out, 0, stream);
     });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "swap kernel launch");
     return PKV_OK;
@@ -560,6 +597,59 @@ int pkv_swap_out(pkv_pool* pool, const int32_t* block_ids, int n, void* host_buf
 
 int pkv_swap_in(pkv_pool* pool, const int32_t* block_ids, int n, const void* host_buf, void* stream) {
   return swap_impl(pool, block_ids, n, const_cast<void*>(host_buf), false, stream);
+}
+
+int pkv_swap_in_ahead(pkv_pool* pool, const int32_t* block_ids, int n, const void* host_buf, void* copy_stream,
+                      void* stream) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  if (n < 0) return fail(PKV_EINVAL, "negative count");
+  if (n == 0) return PKV_OK;
+  if (!block_ids || !host_buf) return fail(PKV_EINVAL, "NULL block_ids or host buffer");
+  for (int i = 0; i < n; ++i)
+    if (block_ids[i] < 0 || block_ids[i] >= pool->num_blocks) return fail(PKV_EINVAL, "block id outside the pool");
+  // An earlier swap-in that has not landed yet lands first, on `stream`.
+  int rc = finish_swap_in(pool, stream);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(pool->swap_mu);
+  if (!pool->swap_ready) {
+    for (cudaEvent_t* e : {&pool->swap_ready, &pool->swap_staged_free, &pool->swap_after})
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+        *e = nullptr;
+        return fail(PKV_ECUDA, "cudaEventCreate swap-in");
+      }
+  }
+  const size_t bytes = static_cast<size_t>(n) * 2 * pool->num_kv_heads * kBlockSize * pool->head_dim * 2;
+  if (bytes > pool->swap_staging_bytes) {
+    if (pool->swap_staging) {
+      // the last scatter may still be reading the old buffer
+      PKV_CUDA(cudaEventSynchronize(pool->swap_staged_free), "swap-in staging release");
+      PKV_CUDA(cudaFree(pool->swap_staging), "cudaFree swap-in staging");
+      pool->swap_staging = nullptr;
+      pool->swap_staging_bytes = 0;
+    }
+    if (cudaMalloc(&pool->swap_staging, bytes) != cudaSuccess) {
+      pool->swap_staging = nullptr;
+      cudaGetLastError();
+      return fail(PKV_ENOMEM, "cudaMalloc swap-in staging");
+    }
+    pool->swap_staging_bytes = bytes;
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+  // The transfer follows the work queued on `stream` (a swap-out that fills
+  // host_buf, the last reads of the blocks) and the previous scatter.
+  PKV_CUDA(cudaEventRecord(pool->swap_after, static_cast<cudaStream_t>(stream)), "swap-in order");
+  PKV_CUDA(cudaStreamWaitEvent(cs, pool->swap_after, 0), "swap-in order");
+  PKV_CUDA(cudaStreamWaitEvent(cs, pool->swap_staged_free, 0), "swap-in staging wait");
+  PKV_CUDA(cudaMemcpyAsync(pool->swap_staging, host_buf, bytes, cudaMemcpyHostToDevice, cs), "swap-in transfer");
+  PKV_CUDA(cudaEventRecord(pool->swap_ready, cs), "swap-in record");
+  pool->swap_ids.assign(block_ids, block_ids + n);
+  pool->swap_pending = true;
+  return PKV_OK;
+}
+
+int pkv_swap_in_finish(pkv_pool* pool, void* stream) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  return finish_swap_in(pool, stream);
 }
 
 // Host memory's device address if it is pinned and mapped, else nullptr.

@@ -102,8 +102,11 @@ struct SwapIds {
 
 // dst / src device addresses (host memory through its device mapping); any sizes.
 int launch_host_copy(void* dst, const void* src, size_t bytes, bool to_host, void* stream);
-int launch_swap(const PoolView& pool, void* kp, void* vp, void* host_dev, const int32_t* ids, int n, bool to_host,
-                int num_sms, void* stream);
+// Moves n pool blocks to / from `buf`, laid out [n][2][Hkv][B][D]: host memory
+// through its device mapping, or a device buffer.  max_ctas = 0 takes the
+// CTA count that saturates the CPU-GPU link in that direction.
+int launch_swap(const PoolView& pool, void* kp, void* vp, void* buf, const int32_t* ids, int n, bool to_host,
+                int max_ctas, void* stream);
 
 int launch_append(const PoolView& pool, void* kp, void* vp, const int32_t* bt, int max_blocks, int num_reqs,
                   const int32_t* cu_q_lens, const int32_t* positions, const void* k_new, const void* v_new,

@@ -108,14 +108,13 @@ int launch_host_copy(void* dst, const void* src, size_t bytes, bool to_host, voi
 }
 
 int launch_swap(const PoolView& pool, void* kp, void* vp, void* host_dev, const int32_t* ids, int n, bool to_host,
-                int num_sms, void* stream) {
-  (void)num_sms;
+                int max_ctas, void* stream) {
   const int blk_chunks = pool.num_kv_heads * kBlockSize * pool.head_dim / 8;
   for (int i = 0; i < n; i += kSwapIdsPerLaunch) {
     const int m = n - i < kSwapIdsPerLaunch ? n - i : kSwapIdsPerLaunch;
     SwapIds s;
     for (int j = 0; j < m; ++j) s.id[j] = ids[i + j];
-    const int cap = to_host ? kSwapCtasOut : kSwapCtasIn;
+    const int cap = max_ctas > 0 ? max_ctas : (to_host ? kSwapCtasOut : kSwapCtasIn);
     const int grid = m < cap ? m : cap;
     uint4* h = static_cast<uint4*>(host_dev) + static_cast<int64_t>(i) * 2 * blk_chunks;
     swap_kernel<<<grid, kSwapThreads, 0, static_cast<cudaStream_t>(stream)>>>(

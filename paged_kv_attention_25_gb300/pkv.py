@@ -39,7 +39,8 @@ KERNELS = ("append", "split_kv", "tensor_core", "merge", "swap")
 EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_kv_ptrs", "pkv_append",
     "pkv_paged_attn_workspace_size", "pkv_paged_attn", "pkv_paged_attn_static", "pkv_last_plan_stats",
-    "pkv_plan_inspect", "pkv_swap_out", "pkv_swap_in", "pkv_check_device_errors",
+    "pkv_plan_inspect", "pkv_swap_out", "pkv_swap_in", "pkv_swap_in_ahead", "pkv_swap_in_finish",
+    "pkv_check_device_errors",
     "pkv_profile_enable", "pkv_profile_read", "pkv_device_sm_count", "pkv_last_error",
     "pkv_version", "pkv_copy_to_device", "pkv_copy_to_host",
     "pkv_cache_create", "pkv_cache_destroy", "pkv_cache_step", "pkv_cache_release", "pkv_cache_free_blocks",
@@ -114,6 +115,8 @@ def load_library():
                                  I, ctypes.POINTER(I), ctypes.POINTER(pkv_plan_stats)],
             "pkv_swap_out": [P, P, I, P, P],
             "pkv_swap_in": [P, P, I, P, P],
+            "pkv_swap_in_ahead": [P, P, I, P, P, P],
+            "pkv_swap_in_finish": [P, P],
             "pkv_check_device_errors": [P, P, ctypes.POINTER(ctypes.c_uint)],
             "pkv_profile_enable": [P, I],
             "pkv_profile_read": [P, ctypes.POINTER(pkv_profile), I],
@@ -431,6 +434,20 @@ def pkv_swap_in(pool: Pool, block_ids, host_buf: torch.Tensor, stream=None):
     _check_host_buf(pool, host_buf, ids.shape[0])
     _check(load_library().pkv_swap_in(pool.handle, ids.ctypes.data, ids.shape[0], host_buf.data_ptr(),
                                        _stream(stream)))
+
+
+def pkv_swap_in_ahead(pool: Pool, block_ids, host_buf: torch.Tensor, copy_stream, stream=None):
+    """Start the copy-engine transfer of host_buf [n, 2, Hkv, 16, D] on copy_stream (after the work queued
+    on `stream`); the blocks land in block_ids at the pool's next call or at pkv_swap_in_finish."""
+    ids = _host_i32(block_ids)
+    _check_host_buf(pool, host_buf, ids.shape[0])
+    _check(load_library().pkv_swap_in_ahead(pool.handle, ids.ctypes.data, ids.shape[0], host_buf.data_ptr(),
+                                             _stream(copy_stream), _stream(stream)))
+
+
+def pkv_swap_in_finish(pool: Pool, stream=None):
+    """Land a pending ahead-of-time swap-in on `stream` (no-op if none is pending)."""
+    _check(load_library().pkv_swap_in_finish(pool.handle, _stream(stream)))
 
 
 def _check_host_buf(pool, host_buf, n):

@@ -52,6 +52,14 @@ def test_calls_without_device_fail_cleanly(lib):
     assert not h.value
 
 
+def test_swap_in_ahead_rejects_null_pool(lib):
+    ids = (ctypes.c_int32 * 1)(0)
+    buf = ctypes.create_string_buffer(64)
+    assert lib.pkv_swap_in_ahead(None, ids, 1, buf, None, None) == pkv.PKV_EINVAL
+    assert lib.pkv_swap_in_finish(None, None) == pkv.PKV_EINVAL
+    assert "pool" in pkv.pkv_last_error()
+
+
 def test_pool_create_rejects_bad_shapes(lib):
     for desc, code in [(pkv.pkv_pool_desc(64, 32, 4, 64, 0, None, None), pkv.PKV_EUNSUPPORTED),
                        (pkv.pkv_pool_desc(64, 16, 4, 96, 0, None, None), pkv.PKV_EUNSUPPORTED),
