@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--swap-layers", type=int, default=4,
                    help="layers (one pool each) of the layer-pipelined swap-in measurement; 0 skips it")
     p.add_argument("--swap-steps", type=int, default=20)
+    p.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3"], default="bf16",
+                   help="KV cache element type (fp8_e4m3: decode-regime workloads only)")
     return p.parse_args(argv)
 
 
@@ -172,23 +174,43 @@ def recorded_traffic(kernel: str, workload: str):
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample(batch, budget_s: float, kp=None, vp=None):
+FP8_SCALE = 2.0 ** -6   # k_scale = v_scale of the synthetic FP8 pools (codes span magnitudes 2 .. 240)
+
+
+def oracle_pools(batch, kv_dtype: str):
+    """The oracle's pools after the step's append (bf16 bits, or FP8 codes)."""
+    import oracle
+    from paged_kv_attention_25_gb300 import workloads as wl
+    if kv_dtype == "fp8_e4m3":
+        kp, vp = wl.fp8_pool_arrays(batch)
+        oracle.append_fp8(kp, vp, FP8_SCALE, FP8_SCALE, batch.block_tables, batch.cu_q_lens, batch.q_positions,
+                          batch.k_new, batch.v_new)
+    else:
+        kp, vp = batch.pool_arrays()
+        oracle.append(kp, vp, batch.block_tables, batch.cu_q_lens, batch.q_positions, batch.k_new, batch.v_new)
+    return kp, vp
+
+
+def oracle_sample(batch, budget_s: float, kp=None, vp=None, kv_dtype: str = "bf16"):
     """Time the CPU oracle on a stratified sample of the batch's query tokens (all heads each).
 
     Returns (tokens_per_s, seconds, n_tokens, threads, description)."""
     import oracle
     oracle.build()
     if kp is None:
-        kp, vp = batch.pool_arrays()
-        oracle.append(kp, vp, batch.block_tables, batch.cu_q_lens, batch.q_positions, batch.k_new, batch.v_new)
+        kp, vp = oracle_pools(batch, kv_dtype)
     T, Hq = batch.num_tokens, batch.num_q_heads
 
     def run(tokens):
         t = np.repeat(tokens, Hq).astype(np.int32)
         h = np.tile(np.arange(Hq, dtype=np.int32), len(tokens))
         t0 = time.perf_counter()
-        oracle.paged_attn_rows(batch.q, kp, vp, batch.block_tables, batch.ctx_lens, batch.cu_q_lens,
-                               batch.q_positions, batch.scale, t, h)
+        if kv_dtype == "fp8_e4m3":
+            oracle.paged_attn_rows_fp8(batch.q, kp, vp, FP8_SCALE, FP8_SCALE, batch.block_tables, batch.ctx_lens,
+                                       batch.cu_q_lens, batch.q_positions, batch.scale, t, h)
+        else:
+            oracle.paged_attn_rows(batch.q, kp, vp, batch.block_tables, batch.ctx_lens, batch.cu_q_lens,
+                                   batch.q_positions, batch.scale, t, h)
         return time.perf_counter() - t0
 
     pilot_stride = max(1, T // 16)
@@ -211,15 +233,14 @@ def run_reference(args):
     from paged_kv_attention_25_gb300 import workloads as wl
     import oracle
     batch = wl.WORKLOADS[args.workload]()
-    kp, vp = batch.pool_arrays()
-    oracle.append(kp, vp, batch.block_tables, batch.cu_q_lens, batch.q_positions, batch.k_new, batch.v_new)
+    kp, vp = oracle_pools(batch, args.kv_dtype)
     per_step = max(0.05, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_sample(batch, per_step, kp, vp)
+        oracle_sample(batch, per_step, kp, vp, args.kv_dtype)
     toks = secs = 0.0
     info = None
     for _ in range(args.steps):
-        rate, dt, n, thr, desc = oracle_sample(batch, per_step, kp, vp)
+        rate, dt, n, thr, desc = oracle_sample(batch, per_step, kp, vp, args.kv_dtype)
         toks += n
         secs += dt
         info = (thr, desc)
@@ -228,7 +249,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {**batch.describe(), "sample_per_step": info[1]},
+        "config": {**batch.describe(), "kv_dtype": args.kv_dtype, "sample_per_step": info[1]},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": info[0], "kind": "oracle", "sample": info[1]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -258,8 +279,11 @@ def run_ours(args):
 
     maker = wl.WORKLOADS[args.workload]
     batch = maker() if world == 1 else maker(seed=maker.__defaults__[0] + 1000 * rank)
-    pool = pkv.Pool(batch.num_blocks, batch.num_kv_heads, batch.head_dim, device=dev)
-    wl.fill_pool(batch, pool.k, pool.v)
+    fp8 = args.kv_dtype == "fp8_e4m3"
+    kv_t = torch.uint8 if fp8 else torch.bfloat16
+    pool_kw = {"dtype": args.kv_dtype, "k_scale": FP8_SCALE, "v_scale": FP8_SCALE} if fp8 else {}
+    pool = pkv.Pool(batch.num_blocks, batch.num_kv_heads, batch.head_dim, device=dev, **pool_kw)
+    (wl.fill_pool_fp8 if fp8 else wl.fill_pool)(batch, pool.k, pool.v)
     d = wl.upload(batch, dev)
     meta = pkv.HostMeta(batch.cu_q_lens, batch.ctx_lens, batch.q_positions)
     T, Hq, D = batch.num_tokens, batch.num_q_heads, batch.head_dim
@@ -277,8 +301,8 @@ def run_ours(args):
     r_swap = int(cand[np.argsort(batch.ctx_lens[cand])[len(cand) // 2]])
     first_q = int(batch.q_positions[batch.cu_q_lens[r_swap]:batch.cu_q_lens[r_swap + 1]].min())
     swap_ids = batch.block_tables[r_swap, :max(1, first_q // 16)].astype(np.int32)
-    swap_host = torch.empty((len(swap_ids), 2, batch.num_kv_heads, 16, D), dtype=torch.bfloat16).pin_memory()
-    swap_bytes = swap_host.numel() * 2
+    swap_host = torch.empty((len(swap_ids), 2, batch.num_kv_heads, 16, D), dtype=kv_t).pin_memory()
+    swap_bytes = swap_host.numel() * swap_host.element_size()
     begun = torch.cuda.Event()
     swapped = torch.cuda.Event()
 
@@ -421,7 +445,7 @@ def run_ours(args):
 
     # ---- swap bandwidth alone (both directions, pinned host)
     ids = batch.used_blocks[:min(len(batch.used_blocks), 4096)].astype(np.int32)
-    sh = torch.empty((len(ids), 2, batch.num_kv_heads, 16, D), dtype=torch.bfloat16).pin_memory()
+    sh = torch.empty((len(ids), 2, batch.num_kv_heads, 16, D), dtype=kv_t).pin_memory()
     pkv.pkv_swap_out(pool, ids, sh)
     torch.cuda.synchronize()
     e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -431,8 +455,9 @@ def run_ours(args):
     pkv.pkv_swap_in(pool, ids, sh)
     e2.record(main)
     torch.cuda.synchronize()
-    swap_out_gbs = sh.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
-    swap_in_gbs = sh.numel() * 2 / (e1.elapsed_time(e2) / 1e3) / 1e9
+    swap_bw_bytes = sh.numel() * sh.element_size()
+    swap_out_gbs = swap_bw_bytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+    swap_in_gbs = swap_bw_bytes / (e1.elapsed_time(e2) / 1e3) / 1e9
     del sh
 
     # ---- layer-pipelined swap-in.  L layers, each its own pool holding the
@@ -449,7 +474,7 @@ def run_ours(args):
     if args.swap_layers > 0:
         layers = [(pool, ws)]
         for _ in range(args.swap_layers - 1):
-            p = pkv.Pool(batch.num_blocks, batch.num_kv_heads, D, device=dev)
+            p = pkv.Pool(batch.num_blocks, batch.num_kv_heads, D, device=dev, **pool_kw)
             p.k.copy_(pool.k)
             p.v.copy_(pool.v)
             layers.append((p, p.workspace(pkv.pkv_paged_attn_workspace_size(p, Hq, meta))))
@@ -536,7 +561,7 @@ def run_ours(args):
             achieved, peak, unit, bound = nbytes / avg_s / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
         roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                 "frac": achieved / peak, "peak_source": f"{peak_src} (burst)",
-                "traffic": recorded_traffic(dom, batch.name), "algorithmic_bytes": nbytes,
+                "traffic": recorded_traffic(dom, batch.name + ("_fp8" if fp8 else "")), "algorithmic_bytes": nbytes,
                 "algorithmic_flops": flops, "avg_launch_us": avg_s * 1e6}
 
     step_ms_avg = 1e3 * secs_all / args.steps
@@ -544,8 +569,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms_avg, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**batch.describe(), "l2": "flushed between steps (258 MB write, then 258 MB read)",
+        "vs_baseline": None, "dtype": "fp8_e4m3 KV, bf16 Q/O, fp32 softmax" if fp8 else "bf16", "data": "synthetic",
+        "config": {**batch.describe(), "kv_dtype": args.kv_dtype,
+                   "l2": "flushed between steps (258 MB write, then 258 MB read)",
                    "e2e_l2": "no flush: each step reads all visible KV and moves its inputs/outputs (working set >> 129 MB L2)",
                    "parallelism": f"replicas x{world}", "swap_out_bytes_per_step": swap_bytes},
         "kv_gbs": kv_bytes / (step_ms_avg / 1e3) / 1e9,
@@ -556,13 +582,13 @@ def run_ours(args):
         "gpu_launches": int(sum(v["launches"] for v in prof.values())),
         "roofline": roof,
         "e2e": {"value": e_tok / e_sec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "swap": {"out_gbs": swap_out_gbs, "in_gbs": swap_in_gbs, "bytes": len(ids) * 2 * batch.num_kv_heads * 16 * D * 2},
+        "swap": {"out_gbs": swap_out_gbs, "in_gbs": swap_in_gbs, "bytes": swap_bw_bytes},
         "swap_in_pipeline": pipe,
         "clocks": clk.summary(),
         "wall_s_timed": wall1 - wall0,
     }
     if world == 1 and not args.no_cpu_baseline:
-        rate, dt, n, thr, desc = oracle_sample(batch, args.cpu_seconds)
+        rate, dt, n, thr, desc = oracle_sample(batch, args.cpu_seconds, kv_dtype=args.kv_dtype)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc,
                                 "seconds": dt}
     print(json.dumps(line), flush=True)

@@ -43,7 +43,9 @@
  *   K, V (new)   : [num_tokens][num_kv_heads][head_dim] bf16
  *   O            : [num_tokens][num_q_heads][head_dim] bf16
  *   LSE          : [num_tokens][num_q_heads] fp32, natural log
- *   swap buffer  : [n][2][num_kv_heads][block_size][head_dim] bf16 (K then V)
+ *   swap buffer  : [n][2][num_kv_heads][block_size][head_dim] of the pool's
+ *                  element type (K then V)
+ *   FP8 pools hold e4m3 codes (one byte) in the pool layout above.
  *
  * Supported shapes: block_size 16; head_dim 64 or 128; num_q_heads a
  * multiple of num_kv_heads with group size G = num_q_heads/num_kv_heads <= 128.
@@ -67,6 +69,17 @@ extern "C" {
 #define PKV_EUNSUPPORTED 6 /* valid but not supported (e.g. head_dim 96) */
 
 #define PKV_DTYPE_BF16 0
+/* FP8 KV cache: K and V stored as OCP FP8 E4M3 codes (1 sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN; largest
+ * finite 448), one scale per pool for K and one for V: the value of a code c
+ * is e4m3(c) * k_scale (or v_scale).  pkv_append quantises each new bf16
+ * element x to the code nearest (ties to even) to the fp32 quotient x / scale,
+ * finite values beyond 448 saturating to +-448.  Such pools are served by the
+ * CUDA-core split-KV kernel only: pkv_paged_attn takes batches whose every
+ * request has at most 4 query rows per KV head (q_len * G <= 4, the decode
+ * regime) and returns PKV_EUNSUPPORTED otherwise.  Q, O and the new K/V given
+ * to pkv_append stay bf16. */
+#define PKV_DTYPE_FP8_E4M3 1
 
 /* Bits of the device error word (pkv_check_device_errors). */
 #define PKV_DEVERR_BLOCK_ID 1u   /* a block-table entry outside [0, num_blocks) */
@@ -81,12 +94,16 @@ typedef struct {
   int block_size;   /* tokens per block; must be 16 */
   int num_kv_heads; /* >= 1 */
   int head_dim;     /* 64 or 128 */
-  int dtype;        /* PKV_DTYPE_BF16 */
+  int dtype;        /* PKV_DTYPE_BF16 or PKV_DTYPE_FP8_E4M3 */
   /* Optional caller-owned device storage for the two pools (each
-   * num_blocks*num_kv_heads*block_size*head_dim*2 bytes, 16-byte aligned).
-   * NULL: the library allocates (and zero-fills) the storage itself. */
+   * num_blocks*num_kv_heads*block_size*head_dim*E bytes, E = 2 for bf16 and 1
+   * for fp8, 16-byte aligned).  NULL: the library allocates (and zero-fills)
+   * the storage itself. */
   void* k_storage;
   void* v_storage;
+  /* PKV_DTYPE_FP8_E4M3 only: dequantisation scales (finite, > 0). */
+  float k_scale;
+  float v_scale;
 } pkv_pool_desc;
 
 /* Host copies of the batch metadata, used to plan the work split.

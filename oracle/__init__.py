@@ -56,8 +56,17 @@ def _load():
             lib.oracle_append.argtypes = [P, P, I, I, I, I, P, I, P, P, I, I, P, P]
             lib.oracle_swap_out.argtypes = [P, P, I, I, I, I, P, I, P]
             lib.oracle_swap_in.argtypes = [P, P, I, I, I, I, P, I, P]
+            lib.oracle_paged_attn_rows_fp8.argtypes = [P, P, P, D, D, I, I, I, I, I, P, I, P, P, P, I, D, P, P, I,
+                                                       P, P]
+            lib.oracle_append_fp8.argtypes = [P, P, ctypes.c_float, ctypes.c_float, I, I, I, I, P, I, P, P, I, I,
+                                              P, P]
+            lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_decode.restype = D
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
             for f in (lib.oracle_paged_attn_rows, lib.oracle_paged_attn, lib.oracle_append,
-                      lib.oracle_swap_out, lib.oracle_swap_in):
+                      lib.oracle_swap_out, lib.oracle_swap_in, lib.oracle_paged_attn_rows_fp8,
+                      lib.oracle_append_fp8):
                 f.restype = I
             lib.oracle_num_threads.restype = I
             _lib = lib
@@ -133,6 +142,77 @@ def paged_attn_rows(q, k_pool, v_pool, block_tables, ctx_lens, cu_q_lens, q_posi
     if rc:
         raise ValueError("oracle_paged_attn_rows: precondition violated")
     return out, lse
+
+
+# ----------------------------------------------------------------------------- FP8 (E4M3) KV cache
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (fp64) of E4M3 codes (uint8 array), from the format's definition."""
+    lib = _load()
+    table = np.array([lib.oracle_e4m3_decode(c) for c in range(256)], np.float64)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 codes (ties to even, finite values saturating) of float32 values."""
+    lib = _load()
+    flat = np.asarray(x, dtype=np.float32).ravel()
+    out = np.fromiter((lib.oracle_e4m3_encode(float(v)) for v in flat), dtype=np.uint8, count=flat.size)
+    return out.reshape(np.shape(x))
+
+
+def paged_attn_rows_fp8(q, k_pool, v_pool, k_scale, v_scale, block_tables, ctx_lens, cu_q_lens, q_positions,
+                        scale, rows_t, rows_h):
+    """Oracle attention over FP8 pools (uint8 E4M3 codes [NB,Hkv,B,D]) for selected rows."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    k_pool = _c(k_pool, np.uint8)
+    v_pool = _c(v_pool, np.uint8)
+    bt = _c(block_tables, np.int32)
+    ctx = _c(ctx_lens, np.int32)
+    cu = _c(cu_q_lens, np.int32)
+    pos = _c(q_positions, np.int32)
+    rt = _c(rows_t, np.int32)
+    rh = _c(rows_h, np.int32)
+    T, Hq, D = q.shape
+    NB, Hkv, B, _ = k_pool.shape
+    n = rt.shape[0]
+    out = np.zeros((n, D), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = lib.oracle_paged_attn_rows_fp8(_p(q), _p(k_pool), _p(v_pool), float(np.float32(k_scale)),
+                                        float(np.float32(v_scale)), NB, Hkv, B, D, Hq, _p(bt), bt.shape[1],
+                                        _p(ctx), _p(cu), _p(pos), ctx.shape[0], float(scale), _p(rt), _p(rh), n,
+                                        _p(out), _p(lse))
+    if rc:
+        raise ValueError("oracle_paged_attn_rows_fp8: precondition violated")
+    return out, lse
+
+
+def paged_attn_fp8(q, k_pool, v_pool, k_scale, v_scale, block_tables, ctx_lens, cu_q_lens, q_positions, scale):
+    """Full oracle attention over FP8 pools; returns (O [T,Hq,D], LSE [T,Hq]) in fp64."""
+    T, Hq, D = np.shape(q)
+    rt = np.repeat(np.arange(T, dtype=np.int32), Hq)
+    rh = np.tile(np.arange(Hq, dtype=np.int32), T)
+    o, l = paged_attn_rows_fp8(q, k_pool, v_pool, k_scale, v_scale, block_tables, ctx_lens, cu_q_lens,
+                               q_positions, scale, rt, rh)
+    return o.reshape(T, Hq, D), l.reshape(T, Hq)
+
+
+def append_fp8(k_pool, v_pool, k_scale, v_scale, block_tables, cu_q_lens, positions, k_new, v_new):
+    """In-place FP8 append: new bf16 rows (uint16 bits) quantised into uint8 code pools."""
+    lib = _load()
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    assert k_pool.dtype == np.uint8 and v_pool.dtype == np.uint8
+    bt = _c(block_tables, np.int32)
+    cu = _c(cu_q_lens, np.int32)
+    pos = _c(positions, np.int32)
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    NB, Hkv, B, D = k_pool.shape
+    rc = lib.oracle_append_fp8(_p(k_pool), _p(v_pool), float(k_scale), float(v_scale), NB, Hkv, B, D, _p(bt),
+                               bt.shape[1], _p(cu), _p(pos), cu.shape[0] - 1, pos.shape[0], _p(kn), _p(vn))
+    if rc:
+        raise ValueError("oracle_append_fp8: slot out of range")
 
 
 def append(k_pool, v_pool, block_tables, cu_q_lens, positions, k_new, v_new):

@@ -65,6 +65,8 @@ int pkv::set_last_error(int code, const std::string& msg) { return fail(code, ms
 
 struct pkv_pool {
   int num_blocks = 0, block_size = 0, num_kv_heads = 0, head_dim = 0;
+  int elem_bytes = 2;                 // 2: bf16; 1: fp8 e4m3 codes
+  float k_scale = 1.f, v_scale = 1.f;
   void* k = nullptr;
   void* v = nullptr;
   bool owns = false;
@@ -106,7 +108,11 @@ struct pkv_pool {
   std::vector<ProfRec> pending;
   pkv_profile totals{};
 
-  PoolView view() const { return PoolView{k, v, num_blocks, num_kv_heads, head_dim, d_err}; }
+  PoolView view() const {
+    return PoolView{k, v, num_blocks, num_kv_heads, head_dim, d_err, elem_bytes, k_scale, v_scale};
+  }
+  // Bytes of one physical block of K (or V): all KV heads.
+  size_t block_bytes() const { return static_cast<size_t>(num_kv_heads) * kBlockSize * head_dim * elem_bytes; }
 
   cudaEvent_t take_event() {
     if (ev_free.empty()) {
@@ -213,7 +219,11 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
   if (desc->num_blocks < 1 || desc->num_kv_heads < 1) return fail(PKV_EINVAL, "num_blocks and num_kv_heads must be >= 1");
   if (desc->block_size != kBlockSize) return fail(PKV_EUNSUPPORTED, "block_size must be 16");
   if (desc->head_dim != 64 && desc->head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
-  if (desc->dtype != PKV_DTYPE_BF16) return fail(PKV_EUNSUPPORTED, "only bf16 pools are supported");
+  if (desc->dtype != PKV_DTYPE_BF16 && desc->dtype != PKV_DTYPE_FP8_E4M3)
+    return fail(PKV_EUNSUPPORTED, "dtype must be PKV_DTYPE_BF16 or PKV_DTYPE_FP8_E4M3");
+  const bool fp8 = desc->dtype == PKV_DTYPE_FP8_E4M3;
+  if (fp8 && !(desc->k_scale > 0.f && desc->k_scale <= 3.4e38f && desc->v_scale > 0.f && desc->v_scale <= 3.4e38f))
+    return fail(PKV_EINVAL, "fp8 pools need finite k_scale and v_scale > 0");
   if ((desc->k_storage == nullptr) != (desc->v_storage == nullptr))
     return fail(PKV_EINVAL, "give both k_storage and v_storage or neither");
   if (desc->k_storage && (!aligned16(desc->k_storage) || !aligned16(desc->v_storage)))
@@ -223,6 +233,11 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
   p->block_size = desc->block_size;
   p->num_kv_heads = desc->num_kv_heads;
   p->head_dim = desc->head_dim;
+  if (fp8) {
+    p->elem_bytes = 1;
+    p->k_scale = desc->k_scale;
+    p->v_scale = desc->v_scale;
+  }
   auto cleanup = [p](int rc) {
     if (p->owns) {
       cudaFree(p->k);
@@ -246,7 +261,7 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaGetDevice"));
   e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaDeviceGetAttribute"));
-  const size_t bytes = static_cast<size_t>(desc->num_blocks) * desc->num_kv_heads * kBlockSize * desc->head_dim * 2;
+  const size_t bytes = static_cast<size_t>(desc->num_blocks) * p->block_bytes();
   if (desc->k_storage) {
     p->k = desc->k_storage;
     p->v = desc->v_storage;
@@ -285,10 +300,14 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
       cudaEventCreateWithFlags(&p->ws_free, cudaEventDisableTiming) != cudaSuccess)
     return cleanup(fail(PKV_ECUDA, "cudaEventCreate upload"));
 
-  int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim);
-  if (rc) return cleanup(rc);
-  rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim);
-  if (rc) return cleanup(rc);
+  // The tensor-core kernel's block maps (bf16 pools only: fp8 pools are read
+  // by the split-KV kernel alone).
+  if (!fp8) {
+    int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim);
+    if (rc) return cleanup(rc);
+    rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim);
+    if (rc) return cleanup(rc);
+  }
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaDeviceSynchronize"));
   *out = p;
@@ -375,7 +394,8 @@ int pkv_append(pkv_pool* pool, const int32_t* block_tables, int max_blocks, int 
 static int plan_for(pkv_pool* pool, int num_q_heads, int num_reqs, int num_tokens, int max_blocks,
                     const pkv_host_meta* meta) {
   if (!meta) return fail(PKV_EINVAL, "host_meta is NULL");
-  PlanParams pp{num_q_heads, pool->num_kv_heads, pool->head_dim, pool->num_sms, num_reqs, num_tokens, max_blocks};
+  PlanParams pp{num_q_heads, pool->num_kv_heads, pool->head_dim, pool->num_sms, num_reqs, num_tokens, max_blocks,
+                pool->elem_bytes};
   const uint64_t sig = plan_signature(pp, *meta);
   if (pool->plan.valid && pool->plan.signature == sig) return PKV_OK;
   const char* err = "plan failed";
@@ -416,6 +436,8 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   rc = plan_for(pool, num_q_heads, num_reqs, num_tokens, max_blocks, host_meta);
   if (rc) return rc;
   const Plan& pl = pool->plan;
+  if (pool->elem_bytes == 1 && !pl.tc.empty())
+    return fail(PKV_EUNSUPPORTED, "fp8 pools take decode-regime batches only: every request needs q_len * G <= 4");
   if (!workspace || workspace_bytes < pl.total) return fail(PKV_EINVAL, "workspace missing or smaller than pkv_paged_attn_workspace_size()");
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(PKV_EINVAL, "workspace must be 256-byte aligned");
 
@@ -559,7 +581,7 @@ static int swap_impl(pkv_pool* pool, const int32_t* ids, int n, void* host, bool
     if (ids[i] < 0 || ids[i] >= pool->num_blocks) return fail(PKV_EINVAL, "block id outside the pool");
   const int frc = finish_swap_in(pool, stream);
   if (frc) return frc;
-  const size_t blk = static_cast<size_t>(pool->num_kv_heads) * kBlockSize * pool->head_dim * 2;
+  const size_t blk = pool->block_bytes();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Pinned (page-locked, device-mapped) host memory: one kernel moves every block.
   cudaPointerAttributes attr{};
@@ -618,7 +640,7 @@ int pkv_swap_in_ahead(pkv_pool* pool, const int32_t* block_ids, int n, const voi
         return fail(PKV_ECUDA, "cudaEventCreate swap-in");
       }
   }
-  const size_t bytes = static_cast<size_t>(n) * 2 * pool->num_kv_heads * kBlockSize * pool->head_dim * 2;
+  const size_t bytes = static_cast<size_t>(n) * 2 * pool->block_bytes();
   if (bytes > pool->swap_staging_bytes) {
     if (pool->swap_staging) {
       // the last scatter may still be reading the old buffer

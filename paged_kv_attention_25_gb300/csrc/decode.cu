@@ -16,6 +16,10 @@
 //
 // Arithmetic: scores in fp32 with scale*log2(e) folded into q, exp2 on the
 // SFU, fp32 accumulation; O rounded to bf16 once at the end.
+//
+// FP8 pools (F8): the chunks are e4m3 codes, half the bytes, so each warp
+// keeps twice the stages in flight; k_scale is folded into q and v_scale into
+// the final 1/l, so the inner loops see the codes' values (see load_row).
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -27,11 +31,11 @@ namespace pkv {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 2;
 
-template <int D>
+template <int D, bool F8>
 struct DecodeSmem {
-  static constexpr int kChunk = kBlockSize * D * 2;            // bytes of one (block, head) of K or V
+  static constexpr int kStages = F8 ? 4 : 2;                   // per-warp ring depth
+  static constexpr int kChunk = kBlockSize * D * (F8 ? 1 : 2);  // bytes of one (block, head) of K or V
   static constexpr int kStage = 2 * kChunk;                    // K then V
   static constexpr int kRing = kWarps * kStages * kStage;
   static constexpr int kMergeFloats = kWarps * kDecodeMaxRows * (D + 2);
@@ -40,42 +44,63 @@ struct DecodeSmem {
   static constexpr int kTotal = kRing + kMergeFloats * 4 + kPBuf + kBars + 16;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kWarps * 32, 3)
-decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
-  using S = DecodeSmem<D>;
-  constexpr int kDPL = D / 32;   // head dims per lane
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  float* merge = reinterpret_cast<float*>(smem + S::kRing);
-  float* pbuf = merge + S::kMergeFloats;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(pbuf) + S::kPBuf);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + kWarps * kStages);
+// Head dims [lane*kDPL, lane*kDPL + kDPL) of one key row as floats.  bf16:
+// exact widening.  F8: byte moves turn each e4m3 code into a bf16 bit pattern
+// (sign to bit 15, the 4 exponent and 3 mantissa bits to the low end of bf16's
+// exponent field and the top of its mantissa; subnormal codes land on bf16
+// subnormals), which reads the code as exactly its value times 2^-120 (bf16's
+// exponent bias is 127, e4m3's 7).  The 2^120 is restored outside the inner
+// loops by exact power-of-two factors (kF8Pre on q and on p, kF8Post on the
+// score and on 1/l), so every product stays a normal float.
+template <int kDPL, bool F8>
+__device__ __forceinline__ void load_row(const uint8_t* p, float* f) {
+  if constexpr (F8) {
+    const uint32_t v = kDPL == 4 ? *reinterpret_cast<const uint32_t*>(p) : *reinterpret_cast<const uint16_t*>(p);
+    const uint32_t y01 = __byte_perm(v, 0u, 0x1404);   // code 1 in bits 24..31, code 0 in bits 8..15
+    const uint32_t w01 = (y01 & 0x80008000u) | ((y01 >> 4) & 0x07F007F0u);
+    f[0] = bf16lo_to_f32(w01);
+    f[1] = bf16hi_to_f32(w01);
+    if constexpr (kDPL == 4) {
+      const uint32_t y23 = __byte_perm(v, 0u, 0x3424);
+      const uint32_t w23 = (y23 & 0x80008000u) | ((y23 >> 4) & 0x07F007F0u);
+      f[2] = bf16lo_to_f32(w23);
+      f[3] = bf16hi_to_f32(w23);
+    }
+  } else if constexpr (kDPL == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    f[0] = bf16lo_to_f32(v.x); f[1] = bf16hi_to_f32(v.x);
+    f[2] = bf16lo_to_f32(v.y); f[3] = bf16hi_to_f32(v.y);
+  } else {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    f[0] = bf16lo_to_f32(v); f[1] = bf16hi_to_f32(v);
+  }
+}
+constexpr float kF8Pre = 18446744073709551616.0f;   // 2^64
+constexpr float kF8Post = 72057594037927936.0f;     // 2^56; kF8Pre * kF8Post = 2^120
 
-  // The work item and the launch's error word are read together: every global
-  // round trip before the first copy is paid by every CTA.  Once any wait in
-  // this launch has given up, the remaining CTAs do nothing (__syncthreads_or
-  // makes the decision the same for every thread).
-  const WorkItem it = items[blockIdx.x];
-  const unsigned err0 = *reinterpret_cast<volatile unsigned*>(a.pool.err);
-  if (__syncthreads_or((err0 & PKV_DEVERR_TIMEOUT) != 0)) return;
+// The streaming part of one item for items of at most R query rows (R = 1, 2
+// or 4: the row loops are unrolled for R, so a one-row decode item issues no
+// instructions for absent rows).  Each warp streams its share of the blocks
+// and leaves its online-softmax state (m, l, acc) for rows [0, rows) in
+// `merge`.
+template <int D, bool F8, int R>
+__device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& it, int rows, uint8_t* ring,
+                                            float* merge, float* pbuf, uint64_t* bars, volatile int* s_abort) {
+  using S = DecodeSmem<D, F8>;
+  constexpr int kStages = S::kStages;
+  constexpr int kDPL = D / 32;   // head dims per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
-  const int rows = it.q_count * G;
   const int Hkv = a.pool.num_kv_heads;
   const int g = it.kv_head;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kWarps * kStages; ++i) mbar_init(&bars[i], 1);
-    *s_abort = 0;
-    fence_mbar_init();
-  }
-
-  // Per-row query (pre-scaled by scale*log2 e) and position; rows >= `rows` are inert.
-  float q[kDecodeMaxRows][kDPL];
-  int qpos[kDecodeMaxRows];
+  // Per-row query (pre-scaled by scale*log2 e, and k_scale * kF8Pre for fp8)
+  // and position; rows >= `rows` are inert.
+  const float qs = F8 ? a.scale_log2 * a.pool.k_scale * kF8Pre : a.scale_log2;
+  float q[R][kDPL];
+  int qpos[R];
 #pragma unroll
-  for (int r = 0; r < kDecodeMaxRows; ++r) {
+  for (int r = 0; r < R; ++r) {
     qpos[r] = -1;
 #pragma unroll
     for (int d = 0; d < kDPL; ++d) q[r][d] = 0.f;
@@ -84,17 +109,10 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
       const int h = g * G + r % G;
       qpos[r] = __ldg(a.q_positions + t);
       const uint16_t* src = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D + lane * kDPL;
-      if constexpr (kDPL == 4) {
-        const uint2 v = *reinterpret_cast<const uint2*>(src);
-        q[r][0] = bf16lo_to_f32(v.x) * a.scale_log2;
-        q[r][1] = bf16hi_to_f32(v.x) * a.scale_log2;
-        q[r][2] = bf16lo_to_f32(v.y) * a.scale_log2;
-        q[r][3] = bf16hi_to_f32(v.y) * a.scale_log2;
-      } else {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
-        q[r][0] = bf16lo_to_f32(v) * a.scale_log2;
-        q[r][1] = bf16hi_to_f32(v) * a.scale_log2;
-      }
+      float qf[kDPL];
+      load_row<kDPL, false>(reinterpret_cast<const uint8_t*>(src), qf);
+#pragma unroll
+      for (int d = 0; d < kDPL; ++d) q[r][d] = qf[d] * qs;
     }
   }
   // Key range from the planner's position bound (the device positions only
@@ -150,9 +168,9 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
   for (int s = 0; s < kStages; ++s)
     if (s < nb_w) issue(s);
 
-  float m[kDecodeMaxRows], l[kDecodeMaxRows], acc[kDecodeMaxRows][kDPL];
+  float m[R], l[R], acc[R][kDPL];
 #pragma unroll
-  for (int r = 0; r < kDecodeMaxRows; ++r) {
+  for (int r = 0; r < R; ++r) {
     m[r] = -CUDART_INF_F;
     l[r] = 0.f;
 #pragma unroll
@@ -175,33 +193,26 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
     const uint8_t* kb = my_ring + st * S::kStage;
     const uint8_t* vb = kb + S::kChunk;
     const int key0 = (blk0 + warp + kWarps * i) * kBlockSize;
+    constexpr int kRowBytes = D * (F8 ? 1 : 2);
+    constexpr int kLaneBytes = kDPL * (F8 ? 1 : 2);
 
     // q . k for 16 keys, this lane's dims.
-    float part[kDecodeMaxRows][kBlockSize];
+    float part[R][kBlockSize];
 #pragma unroll
     for (int k = 0; k < kBlockSize; ++k) {
       float kf[kDPL];
-      if constexpr (kDPL == 4) {
-        const uint2 v = *reinterpret_cast<const uint2*>(kb + (k * D + lane * kDPL) * 2);
-        kf[0] = bf16lo_to_f32(v.x); kf[1] = bf16hi_to_f32(v.x);
-        kf[2] = bf16lo_to_f32(v.y); kf[3] = bf16hi_to_f32(v.y);
-      } else {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(kb + (k * D + lane * kDPL) * 2);
-        kf[0] = bf16lo_to_f32(v); kf[1] = bf16hi_to_f32(v);
-      }
+      load_row<kDPL, F8>(kb + k * kRowBytes + lane * kLaneBytes, kf);
 #pragma unroll
-      for (int r = 0; r < kDecodeMaxRows; ++r) {
-        if (r < rows) {
-          float s = 0.f;
+      for (int r = 0; r < R; ++r) {
+        float s = 0.f;
 #pragma unroll
-          for (int d = 0; d < kDPL; ++d) s = fmaf(q[r][d], kf[d], s);
-          part[r][k] = s;
-        }
+        for (int d = 0; d < kDPL; ++d) s = fmaf(q[r][d], kf[d], s);
+        part[r][k] = s;
       }
     }
 
 #pragma unroll
-    for (int r = 0; r < kDecodeMaxRows; ++r) {
+    for (int r = 0; r < R; ++r) {
       if (r >= rows) break;
       // Transpose-reduce the 16 partial dot products over the 32 lanes:
       // afterwards lane holds the full score of key (lane >> 1).
@@ -231,6 +242,7 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
         v1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
       }
       float s = v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
+      if constexpr (F8) s *= kF8Post;
       const int key = key0 + (lane >> 1);
       if (key > qpos[r] || key >= kv_end) s = -CUDART_INF_F;
       float mx = s;
@@ -247,7 +259,7 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
       m[r] = m_new;
 #pragma unroll
       for (int d = 0; d < kDPL; ++d) acc[r][d] *= alpha;
-      if ((lane & 1) == 0) my_p[r * kBlockSize + (lane >> 1)] = p;
+      if ((lane & 1) == 0) my_p[r * kBlockSize + (lane >> 1)] = F8 ? p * kF8Pre : p;
     }
     __syncwarp();
 
@@ -256,18 +268,11 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
     for (int k = 0; k < kBlockSize; ++k) {
       float vf[kDPL];
       const bool live = key0 + k < kv_end;
-      if constexpr (kDPL == 4) {
-        const uint2 v = *reinterpret_cast<const uint2*>(vb + (k * D + lane * kDPL) * 2);
-        vf[0] = bf16lo_to_f32(v.x); vf[1] = bf16hi_to_f32(v.x);
-        vf[2] = bf16lo_to_f32(v.y); vf[3] = bf16hi_to_f32(v.y);
-      } else {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(vb + (k * D + lane * kDPL) * 2);
-        vf[0] = bf16lo_to_f32(v); vf[1] = bf16hi_to_f32(v);
-      }
+      load_row<kDPL, F8>(vb + k * kRowBytes + lane * kLaneBytes, vf);
 #pragma unroll
       for (int d = 0; d < kDPL; ++d) vf[d] = live ? vf[d] : 0.f;
 #pragma unroll
-      for (int r = 0; r < kDecodeMaxRows; ++r) {
+      for (int r = 0; r < R; ++r) {
         if (r >= rows) break;
         const float p = my_p[r * kBlockSize + k];
 #pragma unroll
@@ -287,10 +292,10 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
       (void)mbar_wait_warp(&my_full[j % kStages], (j / kStages) & 1, nullptr);
   }
 
-  // Merge the four warps' (m, l, acc) states.
+  // This warp's (m, l, acc) states for the CTA-wide merge.
   float* wm = merge + (warp * kDecodeMaxRows) * (D + 2);
 #pragma unroll
-  for (int r = 0; r < kDecodeMaxRows; ++r) {
+  for (int r = 0; r < R; ++r) {
     if (r >= rows) break;
     float* dst = wm + r * (D + 2);
 #pragma unroll
@@ -300,6 +305,41 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
       dst[D + 1] = l[r];
     }
   }
+}
+
+template <int D, bool F8>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
+  using S = DecodeSmem<D, F8>;
+  constexpr int kStages = S::kStages;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  float* merge = reinterpret_cast<float*>(smem + S::kRing);
+  float* pbuf = merge + S::kMergeFloats;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(pbuf) + S::kPBuf);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + kWarps * kStages);
+
+  // The work item and the launch's error word are read together: every global
+  // round trip before the first copy is paid by every CTA.  Once any wait in
+  // this launch has given up, the remaining CTAs do nothing (__syncthreads_or
+  // makes the decision the same for every thread).
+  const WorkItem it = items[blockIdx.x];
+  const unsigned err0 = *reinterpret_cast<volatile unsigned*>(a.pool.err);
+  if (__syncthreads_or((err0 & PKV_DEVERR_TIMEOUT) != 0)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.group;
+  const int rows = it.q_count * G;
+  const int g = it.kv_head;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWarps * kStages; ++i) mbar_init(&bars[i], 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  // `rows` is the same for the whole CTA, so every thread takes the same branch.
+  if (rows <= 1) stream_item<D, F8, 1>(a, it, rows, ring, merge, pbuf, bars, s_abort);
+  else if (rows <= 2) stream_item<D, F8, 2>(a, it, rows, ring, merge, pbuf, bars, s_abort);
+  else stream_item<D, F8, 4>(a, it, rows, ring, merge, pbuf, bars, s_abort);
   __syncthreads();
 
   constexpr float kLn2 = 0.69314718055994530942f;
@@ -323,7 +363,7 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
         o1 += src[d + 1] * f;
       }
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const float inv = lsum > 0.f ? (F8 ? a.pool.v_scale * kF8Post : 1.f) / lsum : 0.f;
     o0 *= inv;
     o1 *= inv;
     const float lse = lsum > 0.f ? (mstar + fast_log2(lsum)) * kLn2 : -CUDART_INF_F;
@@ -364,19 +404,21 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
 
 }  // namespace
 
-template <int D>
+template <int D, bool F8>
 static int launch_decode_d(const AttnArgs& a, const WorkItem* items, int n_items, void* stream) {
-  const int smem = DecodeSmem<D>::kTotal;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = DecodeSmem<D, F8>::kTotal;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D><<<n_items, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(a, items);
+  decode_kernel<D, F8><<<n_items, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(a, items);
   return cudaGetLastError();
 }
 
 int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream) {
   if (n_items <= 0) return cudaSuccess;
-  if (a.pool.head_dim == 128) return launch_decode_d<128>(a, items, n_items, stream);
-  return launch_decode_d<64>(a, items, n_items, stream);
+  const bool f8 = a.pool.elem_bytes == 1;
+  if (a.pool.head_dim == 128)
+    return f8 ? launch_decode_d<128, true>(a, items, n_items, stream) : launch_decode_d<128, false>(a, items, n_items, stream);
+  return f8 ? launch_decode_d<64, true>(a, items, n_items, stream) : launch_decode_d<64, false>(a, items, n_items, stream);
 }
 
 }  // namespace pkv

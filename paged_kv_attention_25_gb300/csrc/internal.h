@@ -64,6 +64,7 @@ struct PlanParams {
   int num_reqs;
   int num_tokens;
   int max_blocks;   // block-table row length; 0 = not checked (host-only planning)
+  int kv_elem_bytes = 2;   // bytes per pool element (2 bf16, 1 fp8)
 };
 
 struct Plan {
@@ -91,7 +92,9 @@ struct PoolView {
   const void* k;
   const void* v;
   int num_blocks, num_kv_heads, head_dim;
-  unsigned* err;   // device error word
+  unsigned* err;     // device error word
+  int elem_bytes;    // 2: bf16 pool; 1: fp8 e4m3 codes
+  float k_scale, v_scale;   // fp8 dequantisation scales (1 for bf16)
 };
 
 // Block ids of one swap launch, passed by value as a kernel parameter.

@@ -273,7 +273,7 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   std::vector<int> req_kv_dec(R, 0), req_kv_tc(R, 0);
   for (const auto& g : dec_groups) req_kv_dec[g.req] = std::max(req_kv_dec[g.req], g.kv_len);
   for (const auto& g : tc_groups) req_kv_tc[g.req] = std::max(req_kv_tc[g.req], g.kv_len);
-  const int64_t per_key = int64_t(2) * Hkv * D * 2;   // K and V, all KV heads, bf16
+  const int64_t per_key = int64_t(2) * Hkv * D * pp.kv_elem_bytes;   // K and V, all KV heads
   for (int r = 0; r < R; ++r) {
     st.decode_kv_bytes += req_kv_dec[r] * per_key;
     st.tc_kv_bytes += req_kv_tc[r] * per_key;

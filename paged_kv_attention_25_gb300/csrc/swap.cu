@@ -109,7 +109,7 @@ int launch_host_copy(void* dst, const void* src, size_t bytes, bool to_host, voi
 
 int launch_swap(const PoolView& pool, void* kp, void* vp, void* host_dev, const int32_t* ids, int n, bool to_host,
                 int max_ctas, void* stream) {
-  const int blk_chunks = pool.num_kv_heads * kBlockSize * pool.head_dim / 8;
+  const int blk_chunks = pool.num_kv_heads * kBlockSize * pool.head_dim * pool.elem_bytes / 16;
   for (int i = 0; i < n; i += kSwapIdsPerLaunch) {
     const int m = n - i < kSwapIdsPerLaunch ? n - i : kSwapIdsPerLaunch;
     SwapIds s;

@@ -53,10 +53,14 @@ class PkvError(RuntimeError):
         self.code = code
 
 
+PKV_DTYPE_BF16 = 0
+PKV_DTYPE_FP8_E4M3 = 1
+
+
 class pkv_pool_desc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int), ("block_size", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int), ("k_storage", ctypes.c_void_p),
-                ("v_storage", ctypes.c_void_p)]
+                ("v_storage", ctypes.c_void_p), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class pkv_host_meta(ctypes.Structure):
@@ -196,24 +200,35 @@ class HostMeta:
 
 
 class Pool:
-    """A KV block pool: K and V storage [num_blocks, num_kv_heads, 16, head_dim] bf16 in torch memory."""
+    """A KV block pool: K and V storage [num_blocks, num_kv_heads, 16, head_dim] in torch memory, bf16
+    (dtype "bf16") or E4M3 codes as uint8 (dtype "fp8_e4m3", values code * k_scale / code * v_scale)."""
 
     def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, block_size: int = 16,
-                 device=None, k_storage: torch.Tensor | None = None, v_storage: torch.Tensor | None = None):
+                 device=None, k_storage: torch.Tensor | None = None, v_storage: torch.Tensor | None = None,
+                 dtype: str = "bf16", k_scale: float = 1.0, v_scale: float = 1.0):
         lib = load_library()
+        if dtype not in ("bf16", "fp8_e4m3"):
+            raise ValueError("dtype must be 'bf16' or 'fp8_e4m3'")
+        fp8 = dtype == "fp8_e4m3"
+        tdtype = torch.uint8 if fp8 else torch.bfloat16
         if device is None:
             device = torch.device("cuda", torch.cuda.current_device())
         shape = (num_blocks, num_kv_heads, block_size, head_dim)
         if k_storage is None:
-            k_storage = torch.zeros(shape, dtype=torch.bfloat16, device=device)
-            v_storage = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+            k_storage = torch.zeros(shape, dtype=tdtype, device=device)
+            v_storage = torch.zeros(shape, dtype=tdtype, device=device)
         for t, n in ((k_storage, "k_storage"), (v_storage, "v_storage")):
-            _dev_bf16(t, n)
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == tdtype and t.is_contiguous()):
+                raise TypeError(f"{n} must be a contiguous {tdtype} CUDA tensor")
             if tuple(t.shape) != shape:
                 raise ValueError(f"{n} must have shape {shape}")
         self.k, self.v = k_storage, v_storage
         self.num_blocks, self.num_kv_heads, self.head_dim, self.block_size = num_blocks, num_kv_heads, head_dim, block_size
-        desc = pkv_pool_desc(num_blocks, block_size, num_kv_heads, head_dim, 0, self.k.data_ptr(), self.v.data_ptr())
+        self.dtype, self.elem_bytes = dtype, (1 if fp8 else 2)
+        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
+        desc = pkv_pool_desc(num_blocks, block_size, num_kv_heads, head_dim,
+                             PKV_DTYPE_FP8_E4M3 if fp8 else PKV_DTYPE_BF16, self.k.data_ptr(), self.v.data_ptr(),
+                             self.k_scale, self.v_scale)
         h = ctypes.c_void_p()
         with torch.cuda.device(self.k.device):
             _check(lib.pkv_pool_create(ctypes.byref(desc), ctypes.byref(h)))
@@ -453,7 +468,7 @@ def pkv_swap_in_finish(pool: Pool, stream=None):
 def _check_host_buf(pool, host_buf, n):
     if not (isinstance(host_buf, torch.Tensor) and not host_buf.is_cuda and host_buf.is_contiguous()):
         raise TypeError("host_buf must be a contiguous CPU tensor (pinned for asynchronous copies)")
-    need = n * 2 * pool.num_kv_heads * pool.block_size * pool.head_dim * 2
+    need = n * 2 * pool.num_kv_heads * pool.block_size * pool.head_dim * pool.elem_bytes
     if host_buf.numel() * host_buf.element_size() < need:
         raise ValueError(f"host_buf holds fewer than {need} bytes")
 

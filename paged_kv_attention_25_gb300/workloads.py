@@ -338,6 +338,18 @@ def random_small(seed: int, *, num_q_heads: int = 4, num_kv_heads: int = 2, head
                        head_dim=head_dim, pool_factor=1.5, seed=seed)
 
 
+def decode_small(seed: int, *, num_q_heads: int = 4, num_kv_heads: int = 4, head_dim: int = 128,
+                 num_reqs: int = 6, max_ctx: int = 3000, tokens: int = 1) -> Batch:
+    """A decode-regime batch: every request has ``tokens`` new tokens (tokens * G <= 4 query
+    rows per KV head) after a history of ~U[0, max_ctx) cached tokens; one request has the
+    full max_ctx so that its keys are split over several items."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 555])))
+    hist = [int(max_ctx)] + [int(x) for x in g.integers(0, max_ctx, size=num_reqs - 1)]
+    reqs = [_decode(h) if tokens == 1 else _new_turn(h, tokens) for h in hist]
+    return build_batch(f"decode_small_{seed}", reqs, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                       head_dim=head_dim, pool_factor=1.5, seed=seed)
+
+
 # ---------------------------------------------------------------------------
 # Device copies (input marshalling only).
 # ---------------------------------------------------------------------------
@@ -361,6 +373,45 @@ def upload(batch: Batch, device="cuda") -> dict:
         "cu_q_lens": i32(batch.cu_q_lens),
         "q_positions": i32(batch.q_positions),
     }
+
+
+def fp8_codes(shape, seed: int) -> np.ndarray:
+    """Random E4M3 code bytes for synthetic FP8 pool contents: a random sign, exponent
+    field uniform in [8, 14] and mantissa field uniform in [0, 7], so magnitudes are
+    log-uniform over [2, 240] and no code is NaN (only the bit layout is used here)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 808])))
+    f = g.integers(0, 2 * 7 * 8, size=shape, dtype=np.uint8)   # (sign, exponent - 8, mantissa) in one draw
+    return ((f // 56) << 7) | ((8 + (f % 56) // 8) << 3) | (f % 8)
+
+
+FP8_DISTINCT_BLOCKS = 1024
+
+
+def fp8_pool_arrays(batch: Batch):
+    """FP8 pool contents [NB, Hkv, B, D] uint8 for a batch: zero codes outside the used
+    blocks; used block i holds row i % FP8_DISTINCT_BLOCKS of a table of random codes
+    (fp8_codes), so full-size pools are generated in seconds."""
+    shape = (batch.num_blocks, batch.num_kv_heads, 16, batch.head_dim)
+    kp, vp = np.zeros(shape, np.uint8), np.zeros(shape, np.uint8)
+    u = batch.used_blocks.size
+    if u:
+        n = (min(u, FP8_DISTINCT_BLOCKS),) + shape[1:]
+        pick = np.arange(u) % n[0]
+        kp[batch.used_blocks] = fp8_codes(n, batch.seed * 2 + 1)[pick]
+        vp[batch.used_blocks] = fp8_codes(n, batch.seed * 2 + 2)[pick]
+    return kp, vp
+
+
+def fill_pool_fp8(batch: Batch, k_storage, v_storage):
+    """Write fp8_pool_arrays(batch) into device uint8 storage (used blocks only; zeros elsewhere)."""
+    import torch
+    k_storage.zero_()
+    v_storage.zero_()
+    if batch.used_blocks.size:
+        kp, vp = fp8_pool_arrays(batch)
+        idx = torch.from_numpy(batch.used_blocks.astype(np.int64)).to(k_storage.device)
+        k_storage[idx] = torch.from_numpy(kp[batch.used_blocks]).to(k_storage.device)
+        v_storage[idx] = torch.from_numpy(vp[batch.used_blocks]).to(v_storage.device)
 
 
 def fill_pool(batch: Batch, k_storage, v_storage):

@@ -287,3 +287,121 @@ def test_swap_roundtrip_moves_whole_blocks():
     assert np.array_equal(k2[others], kp[others])
     with pytest.raises(ValueError):
         oracle.swap_out(kp, vp, np.array([batch.num_blocks], np.int32))
+
+
+# ----------------------------------------------------------------------------- FP8 (E4M3) KV cache
+# The codec is pinned to torch's float8_e4m3fn conversions (a library routine
+# for the same format) and to a brute-force nearest-code search; the FP8
+# attention and append are pinned to the (already pinned) bf16 oracle on values
+# that both formats hold exactly.
+
+def _e4m3_table():
+    vals = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    return np.arange(256), vals
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref)) and np.isnan(ours).sum() == 2   # 0x7F, 0xFF
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert ours[0x7E] == 448.0 and ours[0x38] == 1.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encode_matches_torch_within_range():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(40000) * 60, rng.standard_normal(20000) * 2.0 ** -7,
+                        rng.uniform(-447.9, 447.9, 20000)]).astype(np.float32)
+    _, vals = _e4m3_table()
+    pos = np.unique(vals[(vals > 0) & ~np.isnan(vals)])
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)          # exact ties, both signs
+    x = np.concatenate([x, mids, -mids, np.float32([0.0, -0.0])])
+    ours = oracle.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_encode_is_nearest_code_with_ties_to_even():
+    codes, vals = _e4m3_table()
+    fin = ~np.isnan(vals)
+    codes, vals = codes[fin], vals[fin]
+    rng = np.random.default_rng(6)
+    pos = np.unique(vals[vals > 0])
+    mids = (pos[:-1] + pos[1:]) / 2
+    x = np.concatenate([rng.uniform(-600, 600, 3000), rng.uniform(-2.0 ** -5, 2.0 ** -5, 2000), mids, -mids,
+                        [448.0, 455.0, 464.0, 1000.0, -1000.0]]).astype(np.float32)
+    got = oracle.e4m3_encode(x)
+    for xi, gi in zip(x.astype(np.float64), got):
+        d = np.abs(vals - xi)
+        cand = codes[d == d.min()]
+        cand = cand[(cand >> 7) == (1 if np.signbit(xi) else 0)] if len(cand) > 1 else cand
+        if len(cand) > 1:   # a tie between neighbours: the even mantissa wins
+            cand = cand[(cand & 1) == 0]
+        assert len(cand) == 1 and gi == cand[0], (xi, gi, cand)
+
+
+def test_e4m3_encode_saturates_and_keeps_nan():
+    got = oracle.e4m3_encode(np.float32([1e6, -1e6, np.inf, -np.inf, 449.0, -463.9]))
+    assert list(got) == [0x7E, 0xFE, 0x7E, 0xFE, 0x7E, 0xFE]
+    nan_code = int(oracle.e4m3_encode(np.float32([np.nan]))[0])
+    assert nan_code & 0x7F == 0x7F
+
+
+def _exact_e4m3_bf16(shape, rng):
+    """bf16 bit patterns of values that E4M3 holds exactly (|v| in [2^-6, 240])."""
+    codes = rng.integers(0, 112, size=shape)
+    codes = ((codes // 56) << 7) | ((1 + (codes % 56) // 8 * 2) << 3) | (codes % 8)
+    vals = oracle.e4m3_decode(codes.astype(np.uint8)).astype(np.float32)
+    return (vals.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_fp8_append_equals_bf16_append_on_exact_values():
+    # scale 1 and values that E4M3 holds exactly: every code decodes to the
+    # appended value, in the slot the bf16 append writes.
+    b = wl.random_small(31, num_q_heads=4, num_kv_heads=2, head_dim=64)
+    rng = np.random.default_rng(31)
+    kn, vn = _exact_e4m3_bf16(b.k_new.shape, rng), _exact_e4m3_bf16(b.v_new.shape, rng)
+    shape = (b.num_blocks, 2, 16, 64)
+    k8, v8 = np.zeros(shape, np.uint8), np.zeros(shape, np.uint8)
+    oracle.append_fp8(k8, v8, 1.0, 1.0, b.block_tables, b.cu_q_lens, b.q_positions, kn, vn)
+    kb, vb = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    oracle.append(kb, vb, b.block_tables, b.cu_q_lens, b.q_positions, kn, vn)
+    assert np.array_equal(oracle.e4m3_decode(k8), f64(kb)) and np.array_equal(oracle.e4m3_decode(v8), f64(vb))
+
+
+def test_fp8_append_rounds_each_quotient_to_its_nearest_code():
+    b = wl.random_small(32, num_q_heads=4, num_kv_heads=2, head_dim=64)
+    ks, vs = np.float32(0.0123), np.float32(0.5)
+    shape = (b.num_blocks, 2, 16, 64)
+    k8, v8 = np.zeros(shape, np.uint8), np.zeros(shape, np.uint8)
+    oracle.append_fp8(k8, v8, ks, vs, b.block_tables, b.cu_q_lens, b.q_positions, b.k_new, b.v_new)
+    kb = np.zeros(shape, np.uint16)
+    oracle.append(kb, np.zeros(shape, np.uint16), b.block_tables, b.cu_q_lens, b.q_positions, b.k_new, b.v_new)
+    mark = np.zeros(shape, np.uint16)
+    oracle.append(mark, np.zeros(shape, np.uint16), b.block_tables, b.cu_q_lens, b.q_positions,
+                  np.full_like(b.k_new, 0x3F80), np.full_like(b.v_new, 0x3F80))   # 1.0 in every written slot
+    written = mark != 0
+    x = (f64(kb[written]).astype(np.float32) / ks).astype(np.float64)
+    got = oracle.e4m3_decode(k8[written])
+    _, vals = _e4m3_table()
+    fin = np.sort(vals[~np.isnan(vals)])
+    # |code value - quotient| is the distance to the nearest representable value (saturating at 448)
+    nearest = np.abs(fin[None, :] - np.clip(x, -448, 448)[:, None]).min(axis=1)
+    assert np.allclose(np.abs(got - np.clip(x, -448, 448)), nearest, rtol=0, atol=0)
+    assert (k8[~written] == 0).all() and (v8[~written] == 0).all()
+
+
+def test_fp8_attention_equals_bf16_attention_on_exact_values():
+    # Power-of-two scales: every dequantised value is a bf16 value, so the FP8
+    # oracle must reproduce the bf16 oracle on the equivalent bf16 pools.
+    b = wl.decode_small(33, num_q_heads=8, num_kv_heads=4, head_dim=64, num_reqs=4, max_ctx=200)
+    k8, v8 = wl.fp8_pool_arrays(b)
+    ks, vs = 2.0 ** -6, 2.0 ** -4
+    to_bf16 = lambda codes, s: ((oracle.e4m3_decode(codes) * s).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kb, vb = to_bf16(k8, ks), to_bf16(v8, vs)
+    assert np.array_equal(f64(kb), oracle.e4m3_decode(k8) * ks)
+    O8, L8 = oracle.paged_attn_fp8(b.q, k8, v8, ks, vs, b.block_tables, b.ctx_lens, b.cu_q_lens, b.q_positions, b.scale)
+    O, L = oracle.paged_attn(b.q, kb, vb, b.block_tables, b.ctx_lens, b.cu_q_lens, b.q_positions, b.scale)
+    assert np.allclose(O8, O, rtol=0, atol=1e-12) and np.allclose(L8, L, rtol=0, atol=1e-12)
