@@ -23,6 +23,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "merge.cuh"
 #include "ptx.cuh"
@@ -263,22 +265,30 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     }
     __syncwarp();
 
-    // acc += p . V for this lane's dims; keys at or past kv_end read as zero.
+    // acc += p . V for this lane's dims.  In the item's last block, keys at
+    // or past kv_end read as zero, so that no stale value (NaN included) meets
+    // their zero p; every other block is whole and skips the test.
+    auto pv = [&](auto masked) {
 #pragma unroll
-    for (int k = 0; k < kBlockSize; ++k) {
-      float vf[kDPL];
-      const bool live = key0 + k < kv_end;
-      load_row<kDPL, F8>(vb + k * kRowBytes + lane * kLaneBytes, vf);
+      for (int k = 0; k < kBlockSize; ++k) {
+        float vf[kDPL];
+        load_row<kDPL, F8>(vb + k * kRowBytes + lane * kLaneBytes, vf);
+        if constexpr (decltype(masked)::value) {
+          const bool live = key0 + k < kv_end;
 #pragma unroll
-      for (int d = 0; d < kDPL; ++d) vf[d] = live ? vf[d] : 0.f;
+          for (int d = 0; d < kDPL; ++d) vf[d] = live ? vf[d] : 0.f;
+        }
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if (r >= rows) break;
-        const float p = my_p[r * kBlockSize + k];
+        for (int r = 0; r < R; ++r) {
+          if (r >= rows) break;
+          const float p = my_p[r * kBlockSize + k];
 #pragma unroll
-        for (int d = 0; d < kDPL; ++d) acc[r][d] = fmaf(p, vf[d], acc[r][d]);
+          for (int d = 0; d < kDPL; ++d) acc[r][d] = fmaf(p, vf[d], acc[r][d]);
+        }
       }
-    }
+    };
+    if (key0 + kBlockSize > kv_end) pv(std::true_type{});   // warp-uniform
+    else pv(std::false_type{});
     __syncwarp();
     consumed = i + 1;
     if (i + kStages < nb_w) issue(i + kStages);
