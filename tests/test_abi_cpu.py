@@ -64,7 +64,14 @@ def test_pool_create_rejects_bad_shapes(lib):
     for desc, code in [(pkv.pkv_pool_desc(64, 32, 4, 64, 0, None, None), pkv.PKV_EUNSUPPORTED),
                        (pkv.pkv_pool_desc(64, 16, 4, 96, 0, None, None), pkv.PKV_EUNSUPPORTED),
                        (pkv.pkv_pool_desc(0, 16, 4, 64, 0, None, None), pkv.PKV_EINVAL),
-                       (pkv.pkv_pool_desc(64, 16, 4, 64, 7, None, None), pkv.PKV_EUNSUPPORTED)]:
+                       (pkv.pkv_pool_desc(64, 16, 4, 64, 7, None, None), pkv.PKV_EUNSUPPORTED),
+                       # FP8 pools need finite positive scales (checked before any CUDA call)
+                       (pkv.pkv_pool_desc(64, 16, 4, 64, pkv.PKV_DTYPE_FP8_E4M3, None, None, 0.0, 1.0), pkv.PKV_EINVAL),
+                       (pkv.pkv_pool_desc(64, 16, 4, 64, pkv.PKV_DTYPE_FP8_E4M3, None, None, 1.0, -2.0), pkv.PKV_EINVAL),
+                       (pkv.pkv_pool_desc(64, 16, 4, 64, pkv.PKV_DTYPE_FP8_E4M3, None, None, float("nan"), 1.0),
+                        pkv.PKV_EINVAL),
+                       (pkv.pkv_pool_desc(64, 16, 4, 64, pkv.PKV_DTYPE_FP8_E4M3, None, None, float("inf"), 1.0),
+                        pkv.PKV_EINVAL)]:
         h = ctypes.c_void_p()
         assert lib.pkv_pool_create(ctypes.byref(desc), ctypes.byref(h)) == code
 
