@@ -77,6 +77,34 @@ __device__ __forceinline__ void load_row(const uint8_t* p, float* f) {
     f[0] = bf16lo_to_f32(v); f[1] = bf16hi_to_f32(v);
   }
 }
+// The F8 inner loops keep the widened codes as bf16 bit patterns (two per
+// 32-bit word, lowest element in the low half) and multiply them with
+// mixed-precision FMAs: bf16 operands, exact products, fp32 accumulation.
+template <int kDPL>
+__device__ __forceinline__ void load_row_bf16(const uint8_t* p, uint32_t* w) {
+  const uint32_t v = kDPL == 4 ? *reinterpret_cast<const uint32_t*>(p) : *reinterpret_cast<const uint16_t*>(p);
+  const uint32_t y01 = __byte_perm(v, 0u, 0x1404);
+  w[0] = (y01 & 0x80008000u) | ((y01 >> 4) & 0x07F007F0u);
+  if constexpr (kDPL == 4) {
+    const uint32_t y23 = __byte_perm(v, 0u, 0x3424);
+    w[1] = (y23 & 0x80008000u) | ((y23 >> 4) & 0x07F007F0u);
+  }
+}
+// c0 += lo(a) * lo(b), c1 += hi(a) * hi(b).
+__device__ __forceinline__ void fma_bf16x2(float& c0, float& c1, uint32_t a, uint32_t b) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(a), "r"(b));
+}
+// c0 += p * lo(b), c1 += p * hi(b), p a bf16.
+__device__ __forceinline__ void fma_bf16_bcast(float& c0, float& c1, uint16_t p, uint32_t b) {
+  asm("{\n\t.reg .b16 bl, bh;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, %2, bl, %0;\n\tfma.rn.f32.bf16 %1, %2, bh, %1;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "h"(p), "r"(b));
+}
+
 constexpr float kF8Pre = 18446744073709551616.0f;   // 2^64
 constexpr float kF8Post = 72057594037927936.0f;     // 2^56; kF8Pre * kF8Post = 2^120
 
@@ -98,23 +126,33 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
 
   // Per-row query (pre-scaled by scale*log2 e, and k_scale * kF8Pre for fp8)
   // and position; rows >= `rows` are inert.
-  const float qs = F8 ? a.scale_log2 * a.pool.k_scale * kF8Pre : a.scale_log2;
+  // F8: q stays bf16 (qw) and the whole scale goes onto each score instead.
+  const float qs = a.scale_log2;
+  const float s_scale = a.scale_log2 * a.pool.k_scale * kF8Post;
   float q[R][kDPL];
+  uint32_t qw[R][kDPL / 2];
   int qpos[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     qpos[r] = -1;
 #pragma unroll
     for (int d = 0; d < kDPL; ++d) q[r][d] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kDPL / 2; ++j) qw[r][j] = 0u;
     if (r < rows) {
       const int t = it.q_start + r / G;
       const int h = g * G + r % G;
       qpos[r] = __ldg(a.q_positions + t);
       const uint16_t* src = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D + lane * kDPL;
-      float qf[kDPL];
-      load_row<kDPL, false>(reinterpret_cast<const uint8_t*>(src), qf);
+      if constexpr (F8) {
 #pragma unroll
-      for (int d = 0; d < kDPL; ++d) q[r][d] = qf[d] * qs;
+        for (int j = 0; j < kDPL / 2; ++j) qw[r][j] = reinterpret_cast<const uint32_t*>(src)[j];
+      } else {
+        float qf[kDPL];
+        load_row<kDPL, false>(reinterpret_cast<const uint8_t*>(src), qf);
+#pragma unroll
+        for (int d = 0; d < kDPL; ++d) q[r][d] = qf[d] * qs;
+      }
     }
   }
   // Key range from the planner's position bound (the device positions only
@@ -202,14 +240,26 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     float part[R][kBlockSize];
 #pragma unroll
     for (int k = 0; k < kBlockSize; ++k) {
-      float kf[kDPL];
-      load_row<kDPL, F8>(kb + k * kRowBytes + lane * kLaneBytes, kf);
+      if constexpr (F8) {
+        uint32_t kw[kDPL / 2];
+        load_row_bf16<kDPL>(kb + k * kRowBytes + lane * kLaneBytes, kw);
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float s = 0.f;
+        for (int r = 0; r < R; ++r) {
+          float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int d = 0; d < kDPL; ++d) s = fmaf(q[r][d], kf[d], s);
-        part[r][k] = s;
+          for (int j = 0; j < kDPL / 2; ++j) fma_bf16x2(s0, s1, qw[r][j], kw[j]);
+          part[r][k] = s0 + s1;
+        }
+      } else {
+        float kf[kDPL];
+        load_row<kDPL, F8>(kb + k * kRowBytes + lane * kLaneBytes, kf);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          float s = 0.f;
+#pragma unroll
+          for (int d = 0; d < kDPL; ++d) s = fmaf(q[r][d], kf[d], s);
+          part[r][k] = s;
+        }
       }
     }
 
@@ -244,7 +294,7 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
         v1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
       }
       float s = v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
-      if constexpr (F8) s *= kF8Post;
+      if constexpr (F8) s = (s * kF8Pre) * s_scale;
       const int key = key0 + (lane >> 1);
       if (key > qpos[r] || key >= kv_end) s = -CUDART_INF_F;
       float mx = s;
@@ -261,7 +311,13 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
       m[r] = m_new;
 #pragma unroll
       for (int d = 0; d < kDPL; ++d) acc[r][d] *= alpha;
-      if ((lane & 1) == 0) my_p[r * kBlockSize + (lane >> 1)] = F8 ? p * kF8Pre : p;
+      if ((lane & 1) == 0) {
+        if constexpr (F8)   // bf16 p (times kF8Pre) for the mixed-precision PV FMAs
+          reinterpret_cast<uint16_t*>(my_p)[r * kBlockSize + (lane >> 1)] =
+              static_cast<uint16_t>(pack_bf16x2(p * kF8Pre, 0.f) & 0xffffu);
+        else
+          my_p[r * kBlockSize + (lane >> 1)] = p;
+      }
     }
     __syncwarp();
 
@@ -271,6 +327,23 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     auto pv = [&](auto masked) {
 #pragma unroll
       for (int k = 0; k < kBlockSize; ++k) {
+        if constexpr (F8) {
+          uint32_t vw[kDPL / 2];
+          load_row_bf16<kDPL>(vb + k * kRowBytes + lane * kLaneBytes, vw);
+          if constexpr (decltype(masked)::value) {
+            const bool live = key0 + k < kv_end;
+#pragma unroll
+            for (int j = 0; j < kDPL / 2; ++j) vw[j] = live ? vw[j] : 0u;
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            if (r >= rows) break;
+            const uint16_t p = reinterpret_cast<const uint16_t*>(my_p)[r * kBlockSize + k];
+#pragma unroll
+            for (int j = 0; j < kDPL / 2; ++j) fma_bf16_bcast(acc[r][2 * j], acc[r][2 * j + 1], p, vw[j]);
+          }
+          continue;
+        }
         float vf[kDPL];
         load_row<kDPL, F8>(vb + k * kRowBytes + lane * kLaneBytes, vf);
         if constexpr (decltype(masked)::value) {
