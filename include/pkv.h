@@ -399,8 +399,10 @@ typedef struct {
 
 /* Plan a batch on the host only (no device needed) and copy out its work
  * items: the split-KV items first, then the tensor-core items.  At most
- * max_items are written; *num_items receives the total.  stats may be NULL.
- * Used to test the planner; pkv_paged_attn plans internally. */
+ * max_items are written; *num_items receives the total.  stats may be NULL;
+ * its byte figures are those of a bf16 pool (pkv_last_plan_stats reports a
+ * pool's own, FP8 included).  Used to test the planner; pkv_paged_attn plans
+ * internally. */
 int pkv_plan_inspect(int num_q_heads, int num_kv_heads, int head_dim, int num_sms, int num_reqs,
                      int num_tokens, const pkv_host_meta* host_meta, pkv_work_desc* items,
                      int max_items, int* num_items, pkv_plan_stats* stats);
