@@ -18,8 +18,10 @@
 // SFU, fp32 accumulation; O rounded to bf16 once at the end.
 //
 // FP8 pools (F8): the chunks are e4m3 codes, half the bytes, so each warp
-// keeps twice the stages in flight; k_scale is folded into q and v_scale into
-// the final 1/l, so the inner loops see the codes' values (see load_row).
+// keeps twice the stages in flight.  The codes are widened to bf16 bit
+// patterns by byte moves and multiplied with mixed-precision FMAs (see
+// load_row_bf16); k_scale goes into each score's scale and v_scale into the
+// final 1/l.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -46,29 +48,10 @@ struct DecodeSmem {
   static constexpr int kTotal = kRing + kMergeFloats * 4 + kPBuf + kBars + 16;
 };
 
-// Head dims [lane*kDPL, lane*kDPL + kDPL) of one key row as floats.  bf16:
-// exact widening.  F8: byte moves turn each e4m3 code into a bf16 bit pattern
-// (sign to bit 15, the 4 exponent and 3 mantissa bits to the low end of bf16's
-// exponent field and the top of its mantissa; subnormal codes land on bf16
-// subnormals), which reads the code as exactly its value times 2^-120 (bf16's
-// exponent bias is 127, e4m3's 7).  The 2^120 is restored outside the inner
-// loops by exact power-of-two factors (kF8Pre on q and on p, kF8Post on the
-// score and on 1/l), so every product stays a normal float.
-template <int kDPL, bool F8>
+// Head dims [lane*kDPL, lane*kDPL + kDPL) of one bf16 row as floats (exact).
+template <int kDPL>
 __device__ __forceinline__ void load_row(const uint8_t* p, float* f) {
-  if constexpr (F8) {
-    const uint32_t v = kDPL == 4 ? *reinterpret_cast<const uint32_t*>(p) : *reinterpret_cast<const uint16_t*>(p);
-    const uint32_t y01 = __byte_perm(v, 0u, 0x1404);   // code 1 in bits 24..31, code 0 in bits 8..15
-    const uint32_t w01 = (y01 & 0x80008000u) | ((y01 >> 4) & 0x07F007F0u);
-    f[0] = bf16lo_to_f32(w01);
-    f[1] = bf16hi_to_f32(w01);
-    if constexpr (kDPL == 4) {
-      const uint32_t y23 = __byte_perm(v, 0u, 0x3424);
-      const uint32_t w23 = (y23 & 0x80008000u) | ((y23 >> 4) & 0x07F007F0u);
-      f[2] = bf16lo_to_f32(w23);
-      f[3] = bf16hi_to_f32(w23);
-    }
-  } else if constexpr (kDPL == 4) {
+  if constexpr (kDPL == 4) {
     const uint2 v = *reinterpret_cast<const uint2*>(p);
     f[0] = bf16lo_to_f32(v.x); f[1] = bf16hi_to_f32(v.x);
     f[2] = bf16lo_to_f32(v.y); f[3] = bf16hi_to_f32(v.y);
@@ -77,13 +60,20 @@ __device__ __forceinline__ void load_row(const uint8_t* p, float* f) {
     f[0] = bf16lo_to_f32(v); f[1] = bf16hi_to_f32(v);
   }
 }
-// The F8 inner loops keep the widened codes as bf16 bit patterns (two per
-// 32-bit word, lowest element in the low half) and multiply them with
-// mixed-precision FMAs: bf16 operands, exact products, fp32 accumulation.
+// The same dims of one row of e4m3 codes as bf16 bit patterns, two per 32-bit
+// word (lowest element in the low half).  Byte moves put each code's sign in
+// bit 15 and its 4 exponent and 3 mantissa bits at the low end of bf16's
+// exponent field and the top of its mantissa (subnormal codes land on bf16
+// subnormals), which reads the code as exactly its value times 2^-120 (bf16's
+// exponent bias is 127, e4m3's 7).  The 2^120 is restored outside the inner
+// loops by exact power-of-two factors (kF8Pre on each score and on p, kF8Post
+// in the score scale and in 1/l), so that the sums stay in the normal range.
+// The inner loops multiply these patterns with mixed-precision FMAs: bf16
+// operands, exact products, fp32 accumulation.
 template <int kDPL>
 __device__ __forceinline__ void load_row_bf16(const uint8_t* p, uint32_t* w) {
   const uint32_t v = kDPL == 4 ? *reinterpret_cast<const uint32_t*>(p) : *reinterpret_cast<const uint16_t*>(p);
-  const uint32_t y01 = __byte_perm(v, 0u, 0x1404);
+  const uint32_t y01 = __byte_perm(v, 0u, 0x1404);   // code 1 in bits 24..31, code 0 in bits 8..15
   w[0] = (y01 & 0x80008000u) | ((y01 >> 4) & 0x07F007F0u);
   if constexpr (kDPL == 4) {
     const uint32_t y23 = __byte_perm(v, 0u, 0x3424);
@@ -149,7 +139,7 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
         for (int j = 0; j < kDPL / 2; ++j) qw[r][j] = reinterpret_cast<const uint32_t*>(src)[j];
       } else {
         float qf[kDPL];
-        load_row<kDPL, false>(reinterpret_cast<const uint8_t*>(src), qf);
+        load_row<kDPL>(reinterpret_cast<const uint8_t*>(src), qf);
 #pragma unroll
         for (int d = 0; d < kDPL; ++d) q[r][d] = qf[d] * qs;
       }
@@ -252,7 +242,7 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
         }
       } else {
         float kf[kDPL];
-        load_row<kDPL, F8>(kb + k * kRowBytes + lane * kLaneBytes, kf);
+        load_row<kDPL>(kb + k * kRowBytes + lane * kLaneBytes, kf);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           float s = 0.f;
@@ -342,21 +332,21 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
 #pragma unroll
             for (int j = 0; j < kDPL / 2; ++j) fma_bf16_bcast(acc[r][2 * j], acc[r][2 * j + 1], p, vw[j]);
           }
-          continue;
-        }
-        float vf[kDPL];
-        load_row<kDPL, F8>(vb + k * kRowBytes + lane * kLaneBytes, vf);
-        if constexpr (decltype(masked)::value) {
-          const bool live = key0 + k < kv_end;
+        } else {
+          float vf[kDPL];
+          load_row<kDPL>(vb + k * kRowBytes + lane * kLaneBytes, vf);
+          if constexpr (decltype(masked)::value) {
+            const bool live = key0 + k < kv_end;
 #pragma unroll
-          for (int d = 0; d < kDPL; ++d) vf[d] = live ? vf[d] : 0.f;
-        }
+            for (int d = 0; d < kDPL; ++d) vf[d] = live ? vf[d] : 0.f;
+          }
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if (r >= rows) break;
-          const float p = my_p[r * kBlockSize + k];
+          for (int r = 0; r < R; ++r) {
+            if (r >= rows) break;
+            const float p = my_p[r * kBlockSize + k];
 #pragma unroll
-          for (int d = 0; d < kDPL; ++d) acc[r][d] = fmaf(p, vf[d], acc[r][d]);
+            for (int d = 0; d < kDPL; ++d) acc[r][d] = fmaf(p, vf[d], acc[r][d]);
+          }
         }
       }
     };
