@@ -22,6 +22,7 @@ With --gpus N under torchrun every rank runs its own replica of the workload
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -362,6 +363,19 @@ def run_ours(args):
     tokens_all, secs_all = aggregate_ranks(float(T * args.steps), dev_s)
     value = tokens_all / secs_all
     st = pkv.pkv_last_plan_stats(pool)
+    # Host planning time for this batch, uncached (the step reuses its cached
+    # plan while the batch metadata is unchanged): median of 5 plans.
+    lib = pkv.load_library()
+    n_items, plan_st, sms = ctypes.c_int(), pkv.pkv_plan_stats(), pkv.pkv_device_sm_count()
+    plan_s = []
+    for _ in range(5):   # one planner run each (the work items are counted, not copied out)
+        p0 = time.perf_counter()
+        rc = lib.pkv_plan_inspect(Hq, batch.num_kv_heads, D, sms, batch.num_reqs, T, ctypes.byref(meta.c), None, 0,
+                                  ctypes.byref(n_items), ctypes.byref(plan_st))
+        plan_s.append(time.perf_counter() - p0)
+        if rc:
+            raise RuntimeError(pkv.pkv_last_error())
+    plan_host_us = 1e6 * float(np.median(plan_s))
 
     # ---- end to end: host inputs in, O/LSE out, through the public API.
     # A serving loop: step i+1's inputs cross the link (copy stream `cin`)
@@ -578,7 +592,8 @@ def run_ours(args):
         "tflops": (st["decode_flops"] + st["tc_flops"]) / (step_ms_avg / 1e3) / 1e12,
         "kernels": {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(1, v["launches"])}
                     for k, v in prof.items()},
-        "plan": {k: st[k] for k in ("num_decode_items", "num_tc_items", "num_merge_items")},
+        "plan": {**{k: st[k] for k in ("num_decode_items", "num_tc_items", "num_merge_items")},
+                 "host_plan_us_uncached": plan_host_us},
         "gpu_launches": int(sum(v["launches"] for v in prof.values())),
         "roofline": roof,
         "e2e": {"value": e_tok / e_sec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

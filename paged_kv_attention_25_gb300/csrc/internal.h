@@ -78,6 +78,11 @@ struct Plan {
   size_t off_decode = 0, off_tc = 0, off_merge = 0, off_merge_dec = 0, off_merge_cnt = 0, off_part_o = 0, off_part_lse = 0, total = 0;
   uint64_t signature = 0;
   bool valid = false;
+  // Scratch of the longest-first ordering.  A pool re-plans into the same Plan
+  // whenever the batch changes, so every vector keeps its capacity from one
+  // plan to the next: no reallocation, and no fresh pages to fault in.
+  std::vector<uint32_t> order_key, order_idx, order_idx2;
+  std::vector<WorkItem> order_tmp;
 };
 
 // Record `msg` as this thread's pkv_last_error() and return `code`.

@@ -73,7 +73,17 @@ uint64_t plan_signature(const PlanParams& pp, const pkv_host_meta& meta) {
 }
 
 int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, const char** err) {
-  *plan = Plan();
+  // Reset, keeping every vector's capacity.
+  plan->decode.clear();
+  plan->tc.clear();
+  plan->merge.clear();
+  plan->merge_dec.clear();
+  plan->num_partial_rows = 0;
+  plan->stats = pkv_plan_stats{};
+  plan->off_decode = plan->off_tc = plan->off_merge = plan->off_merge_dec = plan->off_merge_cnt = 0;
+  plan->off_part_o = plan->off_part_lse = plan->total = 0;
+  plan->signature = 0;
+  plan->valid = false;
   const int R = pp.num_reqs, T = pp.num_tokens, Hq = pp.num_q_heads, Hkv = pp.num_kv_heads, D = pp.head_dim;
   if (R < 0 || T < 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) {
     *err = "plan: bad head counts or sizes";
@@ -256,12 +266,42 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   for (const auto& g : dec_groups) emit(g, kBlockSize, dec_chunk, plan->decode, true);
   for (const auto& g : tc_groups) emit(g, kTcKeys, tc_chunk, plan->tc, false);
 
-  // 3. Longest items first, so that the tail of each launch is short.
-  auto longer = [](const WorkItem& a, const WorkItem& b) {
-    return (a.kv_end - a.kv_start) > (b.kv_end - b.kv_start);
+  // 3. Longest items first, so that the tail of each launch is short; equal
+  // lengths keep their emission order.  A stable LSD radix sort of the item
+  // indices on (longest length - length), 8 bits a pass and only as many
+  // passes as the longest length has bytes; the items are then moved once.
+  auto longest_first = [plan](std::vector<WorkItem>& v) {
+    const size_t n = v.size();
+    if (n < 2) return;
+    std::vector<uint32_t>& key = plan->order_key;
+    std::vector<uint32_t>& idx = plan->order_idx;
+    std::vector<uint32_t>& idx2 = plan->order_idx2;
+    key.resize(n);
+    idx.resize(n);
+    idx2.resize(n);
+    uint32_t longest = 0;
+    for (size_t i = 0; i < n; ++i) {
+      key[i] = static_cast<uint32_t>(v[i].kv_end - v[i].kv_start);
+      longest = std::max(longest, key[i]);
+    }
+    for (size_t i = 0; i < n; ++i) {
+      key[i] = longest - key[i];
+      idx[i] = static_cast<uint32_t>(i);
+    }
+    for (int shift = 0; shift < 32 && (longest >> shift) != 0; shift += 8) {
+      uint32_t start[257] = {};
+      for (size_t i = 0; i < n; ++i) ++start[((key[idx[i]] >> shift) & 255u) + 1];
+      for (int b = 0; b < 256; ++b) start[b + 1] += start[b];
+      for (size_t i = 0; i < n; ++i) idx2[start[(key[idx[i]] >> shift) & 255u]++] = idx[i];
+      idx.swap(idx2);
+    }
+    std::vector<WorkItem>& tmp = plan->order_tmp;
+    tmp.resize(n);
+    for (size_t i = 0; i < n; ++i) tmp[i] = v[idx[i]];
+    v.swap(tmp);
   };
-  std::stable_sort(plan->decode.begin(), plan->decode.end(), longer);
-  std::stable_sort(plan->tc.begin(), plan->tc.end(), longer);
+  longest_first(plan->decode);
+  longest_first(plan->tc);
   plan->num_partial_rows = part_rows;
 
   // 4. Statistics (algorithmic work; each (request, KV head) KV read once).

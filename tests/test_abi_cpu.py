@@ -81,6 +81,10 @@ def check_plan(batch, num_sms=148):
     Hq, Hkv, D = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
     G = Hq // Hkv
     items, st = pkv.pkv_plan_inspect(Hq, Hkv, D, num_sms, meta)
+    # Each kernel's list runs longest item first (split-KV items, then tensor-core items).
+    for k in (1, 2):
+        lens = [int(it["kv_end"]) - int(it["kv_start"]) for it in items if int(it["kernel"]) == k]
+        assert all(a >= b for a, b in zip(lens, lens[1:])), f"kernel {k} items not longest first"
     # Group items by (kernel, request, kv head, q_start, q_count).
     groups = {}
     for it in items:
