@@ -156,6 +156,19 @@ def test_planner_covers_every_row_once(lib, maker):
     check_plan(maker())
 
 
+def test_planner_random_batches(lib):
+    # Random shapes, lengths and request mixes (decode, prefill, new turn, recompute),
+    # and SM counts from one SM up, through the same coverage and ordering checks.
+    rng = np.random.default_rng(2024)
+    for seed in range(40):
+        g = int(rng.choice([1, 2, 4, 5, 8]))
+        hkv = int(rng.integers(1, 5))
+        b = wl.random_small(100 + seed, num_q_heads=g * hkv, num_kv_heads=hkv, head_dim=int(rng.choice([64, 128])),
+                            num_reqs=int(rng.integers(1, 9)), max_ctx=int(rng.integers(2, 2500)),
+                            max_q=int(rng.integers(1, 200)))
+        check_plan(b, num_sms=int(rng.choice([1, 7, 148, 152])))
+
+
 def test_planner_splits_long_context_and_routes(lib):
     """One 65,537-token decode next to short requests: the long one is cut into many splits."""
     reqs = [wl._decode(65536), wl._decode(100), wl._new_turn(50, 30),
