@@ -200,9 +200,11 @@ int pkv_paged_attn_workspace_size(pkv_pool* pool, int num_q_heads, int num_reqs,
  * work other than this pool's earlier attention calls.
  * Streams: the kernels run after the upload and after the work already on
  * `stream`.  When the batch has both split-KV and tensor-core work, the
- * split-KV kernel runs on a second stream owned by the pool, forked from
- * `stream` (event) and joined back into it before the merge; every effect of
- * the call is complete once `stream` passes the point after it.
+ * split-KV kernel runs on `stream` and the tensor-core kernel on a second
+ * stream owned by the pool, forked from `stream` (event) and joined back into
+ * it before the merge; every effect of the call is complete once `stream`
+ * passes the point after it.  A pending ahead-of-time swap-in on the pool
+ * (pkv_swap_in_ahead) lands on `stream` before the kernels.
  * num_tokens == 0 is a no-op.  Errors: PKV_EINVAL for bad shapes, a workspace
  * that is too small, or host metadata that is inconsistent.
  */

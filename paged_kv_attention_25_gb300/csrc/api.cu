@@ -83,7 +83,7 @@ struct pkv_pool {
   cudaEvent_t pinned_done[2] = {nullptr, nullptr};
   int pinned_slot = 0;
   std::vector<uint8_t> staging;
-  // The split-KV kernel runs on `side`, concurrently with the tensor-core
+  // The tensor-core kernel runs on `side`, concurrently with the split-KV
   // kernel on the caller's stream (fork / join through the two events).
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
