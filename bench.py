@@ -6,18 +6,30 @@ batch's new tokens, host planning, the split-KV and tensor-core attention
 kernels, the log-sum-exp merge, and a swap-out of one conversation's blocks to
 pinned host memory on a side stream (the CPU cache tier), joined at the end.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--workloads all|none|a,b,...] [--impl ours|reference] [--kv-dtype bf16|fp8_e4m3]
 
-Prints one JSON line on rank 0.  `value` is query tokens per second of the
-whole job with inputs resident in HBM (device-timed with CUDA events, L2
-flushed between steps); `e2e` is the same metric through the public API with
-every step's inputs copied in from pinned host memory and its O/LSE copied out
-inside the timed region (a serving loop: the next step's inputs cross the link
-while the current step computes);
-`roofline` reports the dominant kernel against MEASURED_PEAKS.json;
-`cpu_baseline` times the CPU oracle on a bounded sample of the same workload.
-With --gpus N under torchrun every rank runs its own replica of the workload
-(weak scaling; no collective on the data path).
+Prints one JSON line on rank 0.  The headline (`value`, `e2e`, `roofline`) is
+the Llama-2-70B grouped-query workload (`llama70b_gqa`, the largest amount of
+attention work of the five workloads); `per_workload` repeats the measurement
+for every workload.  For each workload:
+  value     query tokens per second with inputs resident in HBM (device-timed
+            with CUDA events, L2 flushed between steps);
+  e2e       the same metric through the library's C ABI in a serving loop: every
+            step's inputs are copied in from pinned host memory and its O/LSE
+            copied out (pkv_copy_to_device / pkv_copy_to_host) inside the timed
+            region, while the next step's inputs cross the link;
+  e2e_replan  the same loop with the batch metadata changing every step (each
+            decode's position moves), so the host plans every step inside the
+            timed region;
+  roofline  per attention kernel, from a pass that runs the two kernels one
+            after the other so that each kernel's CUDA events bracket its own
+            execution: algorithmic bytes and FLOPs per launch (planner
+            statistics) over the launch's average duration, against
+            MEASURED_PEAKS.json.
+`cpu_baseline` times the CPU oracle on a bounded sample of the headline
+workload.  With --gpus N under torchrun every rank runs its own replica of
+the workload (weak scaling; no collective on the data path).
 """
 from __future__ import annotations
 
@@ -25,7 +37,6 @@ import argparse
 import ctypes
 import hashlib
 import json
-import math
 import os
 import subprocess
 import sys
@@ -40,23 +51,27 @@ METRIC = "paged multi-token attn: query tok/s, KV GB/s & TC util vs GB300 roofli
 UNIT = "query tok/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HEADLINE = "llama70b_gqa"
+ALL_WORKLOADS = ("tiny_mixed", "llama13b_mixed", "decode_lognormal", "llama70b_gqa", "long_skewed_evict")
+REPLAN_VARIANTS = 8
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="llama13b_mixed")
+    p.add_argument("--workload", default=HEADLINE, help="the headline workload")
+    p.add_argument("--workloads", default="all",
+                   help="workloads measured in per_workload: all, none, or a comma-separated list")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--swap-layers", type=int, default=4,
                    help="layers (one pool each) of the layer-pipelined swap-in measurement; 0 skips it")
     p.add_argument("--swap-steps", type=int, default=20)
-    p.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3"], default="bf16",
-                   help="KV cache element type (fp8_e4m3: decode-regime workloads only)")
+    p.add_argument("--kv-dtype", choices=["bf16", "fp8_e4m3"], default="bf16", help="KV cache element type")
     return p.parse_args(argv)
 
 
@@ -151,10 +166,13 @@ class ClockSampler:
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+KERNEL_SOURCES = {"split_kv": "decode.cu", "tensor_core": "attn_tc.cu"}
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM traffic per launch from the committed ncu summary, if it was taken on this kernel source."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
-    src = {"split_kv": "decode.cu", "tensor_core": "attn_tc.cu"}.get(kernel)
+    src = KERNEL_SOURCES.get(kernel)
     if not src or not os.path.exists(path):
         return None
     with open(os.path.join(ROOT, "paged_kv_attention_25_gb300", "csrc", src), "rb") as f:
@@ -171,6 +189,61 @@ def recorded_traffic(kernel: str, workload: str):
         return float(vals["dram_bytes_per_launch_full_size"])
     except (KeyError, ValueError):
         return None
+
+
+def kernel_work(stats: dict, kernel: str):
+    """Algorithmic bytes and FLOPs of one launch of an attention kernel (planner statistics)."""
+    if kernel == "split_kv":
+        return stats["decode_kv_bytes"] + stats["decode_io_bytes"], stats["decode_flops"]
+    return stats["tc_kv_bytes"] + stats["tc_io_bytes"], stats["tc_flops"]
+
+
+def kernel_roofline(stats: dict, kernel: str, avg_s: float, peaks: dict, peak_src: str, workload: str):
+    """Roofline of one attention kernel: the binding roof is the larger of its HBM and tensor times."""
+    nbytes, flops = kernel_work(stats, kernel)
+    hbm = nbytes / avg_s / 1e9
+    tfl = flops / avg_s / 1e12
+    hbm_frac = hbm / peaks["hbm_gbs"]
+    tc_frac = tfl / peaks["bf16_tflops"]
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    tensor = kernel == "tensor_core" and t_tc > t_hbm
+    return {"kernel": kernel, "bound": "tensor" if tensor else "hbm",
+            "achieved": tfl if tensor else hbm, "peak": peaks["bf16_tflops"] if tensor else peaks["hbm_gbs"],
+            "unit": "TFLOP/s" if tensor else "GB/s", "frac": tc_frac if tensor else hbm_frac,
+            "hbm_gbs": hbm, "hbm_frac": hbm_frac, "tflops": tfl, "tensor_frac": tc_frac,
+            "roofline_frac": max(t_hbm, t_tc) / avg_s,
+            "peak_source": f"{peak_src} (burst)", "avg_launch_us": avg_s * 1e6,
+            "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "traffic": recorded_traffic(kernel, workload)}
+
+
+# ----------------------------------------------------------------------------- workload variants
+
+def replan_variants(batch, n: int):
+    """n variants of a batch's (ctx_lens, q_positions) that differ in every decode request.
+
+    Variant v moves each one-token request's query position (and context end)
+    back by v tokens, so the variants have distinct plans; multi-token requests
+    are unchanged.  Every variant only reads keys the pool already holds."""
+    q_lens = np.diff(batch.cu_q_lens)
+    out = []
+    for v in range(n):
+        ctx = batch.ctx_lens.copy()
+        pos = batch.q_positions.copy()
+        for r in np.flatnonzero(q_lens == 1):
+            s = min(v, int(ctx[r]) - 1)
+            ctx[r] -= s
+            pos[batch.cu_q_lens[r]] -= s
+        out.append((ctx.astype(np.int32), pos.astype(np.int32)))
+    return out
+
+
+def config_of(batch, args):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {**batch.describe(), "kv_dtype": args.kv_dtype,
+            "l2": "flushed between device-timed steps (258 MB write, then 258 MB read)",
+            "parallelism": f"replicas x{args.gpus}"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
@@ -232,7 +305,6 @@ def run_reference(args):
     if rank != 0:
         return
     from paged_kv_attention_25_gb300 import workloads as wl
-    import oracle
     batch = wl.WORKLOADS[args.workload]()
     kp, vp = oracle_pools(batch, args.kv_dtype)
     per_step = max(0.05, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -250,7 +322,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {**batch.describe(), "kv_dtype": args.kv_dtype, "sample_per_step": info[1]},
+        "config": config_of(batch, args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": info[0], "kind": "oracle", "sample": info[1]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -259,26 +331,34 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_ours(args):
+class Bench:
+    """Device state shared by the workloads: streams, L2 flush buffers."""
+
+    def __init__(self, args, dev):
+        import torch
+        self.args, self.dev = args, dev
+        self.main = torch.cuda.current_stream()
+        self.side = torch.cuda.Stream(device=dev)
+        self.flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.flush_r = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.flush_sum = torch.empty((), dtype=torch.float32, device=dev)
+
+    def l2_flush(self):
+        # Write a buffer twice the size of L2, then read another one, so that
+        # each step starts with a cold L2 that holds no dirty lines of the flush
+        # (whose write-back would otherwise land in the step).
+        self.flush.zero_()
+        self.flush_sum.copy_(self.flush_r.sum())
+
+
+def measure_workload(B: Bench, name: str, headline: bool, rank: int, world: int):
+    """Every measurement of one workload; returns (line fields, objects kept for the headline extras)."""
     import torch
-    import torch.distributed as dist
-    from paged_kv_attention_25_gb300 import build as pkv_build
     from paged_kv_attention_25_gb300 import pkv
     from paged_kv_attention_25_gb300 import workloads as wl
 
-    world, rank, local = dist_info()
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    if rank == 0:
-        pkv_build.build()
-    barrier()
-    pkv_build.build()   # no-op when fresh; other ranks wait for rank 0 above
-
-    maker = wl.WORKLOADS[args.workload]
+    args, dev, main, side = B.args, B.dev, B.main, B.side
+    maker = wl.WORKLOADS[name]
     batch = maker() if world == 1 else maker(seed=maker.__defaults__[0] + 1000 * rank)
     fp8 = args.kv_dtype == "fp8_e4m3"
     kv_t = torch.uint8 if fp8 else torch.bfloat16
@@ -291,8 +371,6 @@ def run_ours(args):
     out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
     ws = pool.workspace(pkv.pkv_paged_attn_workspace_size(pool, Hq, meta))
-    main = torch.cuda.current_stream()
-    side = torch.cuda.Stream(device=dev)
 
     # Swap-out target: the cached-history blocks (read-only in this step) of the
     # conversation with the median context, i.e. one conversation moved to the
@@ -309,60 +387,56 @@ def run_ours(args):
 
     # The swap-out moves cached history that this step's append does not
     # write, so it starts with the step, beside the append.
-    def step():
+    def step(di=d, meta_=meta, o=out, l_=lse):
         begun.record(main)
         side.wait_event(begun)
         pkv.pkv_swap_out(pool, swap_ids, swap_host, stream=side)
         swapped.record(side)
-        pkv.pkv_append(pool, d["block_tables"], d["cu_q_lens"], d["q_positions"], d["k_new"], d["v_new"])
-        pkv.pkv_paged_attn(pool, d["q"], d["q_positions"], d["block_tables"], d["ctx_lens"], d["cu_q_lens"],
-                           meta, batch.scale, out=out, lse=lse, workspace=ws)
+        pkv.pkv_append(pool, di["block_tables"], di["cu_q_lens"], di["q_positions"], di["k_new"], di["v_new"])
+        pkv.pkv_paged_attn(pool, di["q"], di["q_positions"], di["block_tables"], di["ctx_lens"], di["cu_q_lens"],
+                           meta_, batch.scale, out=o, lse=l_, workspace=ws)
         main.wait_event(swapped)
 
-    # L2 flush between steps: write a buffer twice the size of L2, then read
-    # another one, so that each step starts with a cold L2 that holds no dirty
-    # lines of the flush (whose write-back would otherwise land in the step).
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_r = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_sum = torch.empty((), dtype=torch.float32, device=dev)
-
-    def l2_flush():
-        flush.zero_()
-        flush_sum.copy_(flush_r.sum())
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     if pkv.pkv_check_device_errors(pool) != 0:
-        raise RuntimeError("device error word set during warm-up")
+        raise RuntimeError(f"{name}: device error word set during warm-up")
 
-    # ---- timed region: K steps, L2 flushed between steps, per-step CUDA events
-    pkv.pkv_profile_read(pool, reset=True)
-    pkv.pkv_profile_enable(pool, True)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
-    gpu_index = int(visible[dev.index]) if dev.index < len(visible) and visible[dev.index].isdigit() else dev.index
-    with ClockSampler(gpu_index) as clk:
+    def timed_steps(n, mode):
+        """n device-timed steps, L2 flushed between them; returns (per-step ms, kernel profile)."""
+        pkv.pkv_profile_read(pool, reset=True)
+        pkv.pkv_profile_enable(pool, mode)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         barrier()
         torch.cuda.synchronize()
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            l2_flush()
+        for i in range(n):
+            B.l2_flush()
             starts[i].record(main)
             step()
             ends[i].record(main)
         torch.cuda.synchronize()
-        wall1 = time.perf_counter()
         barrier()
-    pkv.pkv_profile_enable(pool, False)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    prof = pkv.pkv_profile_read(pool, reset=True)
-    if pkv.pkv_check_device_errors(pool) != 0:
-        raise RuntimeError("device error word set during the timed region")
+        pkv.pkv_profile_enable(pool, 0)
+        prof = pkv.pkv_profile_read(pool, reset=True)
+        if pkv.pkv_check_device_errors(pool) != 0:
+            raise RuntimeError(f"{name}: device error word set during a timed region")
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)], prof
+
+    # ---- value: K steps as a serving step runs them (the two attention kernels side by side)
+    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    gpu_index = int(visible[dev.index]) if dev.index < len(visible) and visible[dev.index].isdigit() else dev.index
+    with ClockSampler(gpu_index) as clk:
+        wall0 = time.perf_counter()
+        step_ms, prof = timed_steps(args.steps, 1)
+        wall1 = time.perf_counter()
     dev_s = sum(step_ms) / 1e3
     tokens_all, secs_all = aggregate_ranks(float(T * args.steps), dev_s)
-    value = tokens_all / secs_all
     st = pkv.pkv_last_plan_stats(pool)
+    # ---- per-kernel durations: the same steps with the two attention kernels one after the other
+    ser_ms, ser_prof = timed_steps(max(10, args.steps // 2), 2)
+
     # Host planning time for this batch, uncached (the step reuses its cached
     # plan while the batch metadata is unchanged): median of 5 plans.
     lib = pkv.load_library()
@@ -377,18 +451,22 @@ def run_ours(args):
             raise RuntimeError(pkv.pkv_last_error())
     plan_host_us = 1e6 * float(np.median(plan_s))
 
-    # ---- end to end: host inputs in, O/LSE out, through the public API.
+    # ---- end to end through the C ABI: host inputs in, O/LSE out.
     # A serving loop: step i+1's inputs cross the link (copy stream `cin`)
     # while step i computes, and step i's O/LSE go back on `cout` (the link is
     # full duplex); inputs and outputs are double-buffered and events order the
-    # reuse of each buffer.  Every step still copies all of its inputs in and
-    # its result out and runs the same swap-out as the device-timed step; the
-    # timed region is the whole loop.  No L2 flush here: each step reads every
-    # visible KV block (hundreds of MB for the bench workloads) and moves its
-    # inputs and outputs, several times the 129 MB of L2, so no step finds the
-    # previous one's data in L2.
+    # reuse of each buffer.  Every step copies all of its inputs in and its
+    # result out with pkv_copy_to_device / pkv_copy_to_host and runs the same
+    # swap-out as the device-timed step; the timed region is the whole loop.
+    # No L2 flush here: each step reads every visible KV block (hundreds of MB
+    # for the bench workloads) and moves its inputs and outputs, several times
+    # the 129 MB of L2, so no step finds the previous one's data in L2.
     e2e_steps = args.e2e_steps or max(10, args.steps // 4)
     host_in = {k: (v.cpu().pin_memory()) for k, v in d.items()}
+    variants = replan_variants(batch, REPLAN_VARIANTS)
+    host_var = [{"ctx_lens": torch.from_numpy(c).pin_memory(), "q_positions": torch.from_numpy(p).pin_memory()}
+                for c, p in variants]
+    meta_var = [pkv.HostMeta(batch.cu_q_lens, c, p) for c, p in variants]
     host_out = torch.empty_like(out, device="cpu").pin_memory()
     host_lse = torch.empty_like(lse, device="cpu").pin_memory()
     dev_in = [{k: torch.empty_like(v) for k, v in d.items()} for _ in range(2)]
@@ -401,65 +479,110 @@ def run_ours(args):
     out_read = [torch.cuda.Event() for _ in range(2)]  # O/LSE of slot s copied to the host
     meta_e = pkv.HostMeta(host_in["cu_q_lens"].numpy(), host_in["ctx_lens"].numpy(), host_in["q_positions"].numpy())
 
-    def copy_in(i):
+    def copy_in(i, replan):
         s = i % 2
         cin.wait_event(done[s])
-        with torch.cuda.stream(cin):
-            for k in dev_in[s]:
-                dev_in[s][k].copy_(host_in[k], non_blocking=True)
+        for k in dev_in[s]:
+            src = host_var[i % len(host_var)][k] if replan and k in ("ctx_lens", "q_positions") else host_in[k]
+            pkv.pkv_copy_to_device(dev_in[s][k], src, stream=cin)
         in_ready[s].record(cin)
 
-    def e2e_step(i):
+    def e2e_step(i, replan):
         s = i % 2
         di, (o_s, l_s) = dev_in[s], outs[s]
         main.wait_event(in_ready[s])
         main.wait_event(out_read[s])
-        begun.record(main)
-        side.wait_event(begun)
-        pkv.pkv_swap_out(pool, swap_ids, swap_host, stream=side)
-        swapped.record(side)
-        pkv.pkv_append(pool, di["block_tables"], di["cu_q_lens"], di["q_positions"], di["k_new"], di["v_new"])
-        pkv.pkv_paged_attn(pool, di["q"], di["q_positions"], di["block_tables"], di["ctx_lens"], di["cu_q_lens"],
-                           meta_e, batch.scale, out=o_s, lse=l_s, workspace=ws)
-        main.wait_event(swapped)
+        step(di, meta_var[i % len(meta_var)] if replan else meta_e, o_s, l_s)
         done[s].record(main)
         cout.wait_event(done[s])
-        with torch.cuda.stream(cout):
-            host_out.copy_(o_s, non_blocking=True)
-            host_lse.copy_(l_s, non_blocking=True)
+        pkv.pkv_copy_to_host(host_out, o_s, stream=cout)
+        pkv.pkv_copy_to_host(host_lse, l_s, stream=cout)
         out_read[s].record(cout)
 
-    def e2e_loop(n):
+    def e2e_loop(n, replan):
         # Step i is queued before step i+1's input copy: the copy engines take
         # transfers in order, so step i's small work-list upload must not sit
         # behind the next step's inputs (the big copy still runs during step i).
-        copy_in(0)
+        copy_in(0, replan)
         for i in range(n):
-            e2e_step(i)
+            e2e_step(i, replan)
             if i + 1 < n:
-                copy_in(i + 1)
+                copy_in(i + 1, replan)
         main.wait_stream(cout)
 
-    for ev in done + out_read:
-        ev.record(main)
-    e2e_loop(3)
-    torch.cuda.synchronize()
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    e_start.record(main)
-    e2e_loop(e2e_steps)
-    e_end.record(main)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_s = e_start.elapsed_time(e_end) / 1e3
-    e_tok, e_sec = aggregate_ranks(float(T * e2e_steps), e2e_s)
-    if pkv.pkv_check_device_errors(pool) != 0:
-        raise RuntimeError("device error word set in the end-to-end loop")
+    def e2e_timed(replan):
+        for ev in done + out_read:
+            ev.record(main)
+        e2e_loop(3, replan)
+        torch.cuda.synchronize()
+        built0 = pkv.pkv_last_plan_stats(pool)["plans_built"]
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e_start.record(main)
+        e2e_loop(e2e_steps, replan)
+        e_end.record(main)
+        torch.cuda.synchronize()
+        barrier()
+        plans = pkv.pkv_last_plan_stats(pool)["plans_built"] - built0
+        e_tok, e_sec = aggregate_ranks(float(T * e2e_steps), e_start.elapsed_time(e_end) / 1e3)
+        if pkv.pkv_check_device_errors(pool) != 0:
+            raise RuntimeError(f"{name}: device error word set in the end-to-end loop")
+        return e_tok / e_sec, plans
+
+    e2e_value, _ = e2e_timed(False)
+    replan_value, replans = e2e_timed(True)
+
+    peaks, peak_src = load_peaks()
+    ser = {k: v for k, v in ser_prof.items() if k in KERNEL_SOURCES and v["launches"]}
+    kname = name + ("_fp8" if fp8 else "")
+    roofs = {k: kernel_roofline(st, k, v["total_ms"] / v["launches"] / 1e3, peaks, peak_src, kname)
+             for k, v in ser.items()}
+    # The kernel that dominates the step: the most device time in the pass
+    # where each kernel runs alone.
+    dom = max(ser, key=lambda k: ser[k]["total_ms"]) if ser else None
+    step_ms_avg = 1e3 * secs_all / args.steps
+    kv_bytes = st["decode_kv_bytes"] + st["tc_kv_bytes"]
+    res = {
+        "value": tokens_all / secs_all, "unit": UNIT, "ms_per_step": step_ms_avg,
+        "config": config_of(batch, args),
+        "kv_gbs": kv_bytes / (step_ms_avg / 1e3) / 1e9,
+        "tflops": (st["decode_flops"] + st["tc_flops"]) / (step_ms_avg / 1e3) / 1e12,
+        "kernels": {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(1, v["launches"])}
+                    for k, v in prof.items()},
+        "kernels_one_at_a_time": {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(1, v["launches"])}
+                                  for k, v in ser_prof.items()},
+        "ms_per_step_one_at_a_time": float(np.mean(ser_ms)),
+        "roofline": roofs.get(dom),
+        "roofline_per_kernel": roofs,
+        "plan": {**{k: st[k] for k in ("num_decode_items", "num_tc_items", "num_merge_items")},
+                 "host_plan_us_uncached": plan_host_us},
+        "gpu_launches": int(sum(v["launches"] for v in prof.values())),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "pkv_copy_to_device / pkv_copy_to_host from pinned host memory, copy engines"},
+        "e2e_replan": {"value": replan_value, "unit": UNIT, "plans_built": int(replans), "steps": e2e_steps,
+                       "variants": REPLAN_VARIANTS},
+        "clocks": clk.summary(),
+        "wall_s_timed": wall1 - wall0,
+        "swap_out_bytes_per_step": swap_bytes,
+    }
+    keep = {"batch": batch, "pool": pool, "ws": ws, "d": d, "meta": meta, "out": out, "lse": lse,
+            "swap_ids": swap_ids, "swap_host": swap_host, "kv_t": kv_t, "pool_kw": pool_kw} if headline else None
+    return res, keep
+
+
+def headline_extras(B: Bench, k: dict):
+    """Swap bandwidth and the layer-pipelined swap-in, on the headline workload."""
+    import torch
+    from paged_kv_attention_25_gb300 import pkv
+    args, dev, main = B.args, B.dev, B.main
+    batch, pool, d, meta = k["batch"], k["pool"], k["d"], k["meta"]
+    D, Hq = batch.head_dim, batch.num_q_heads
+    swap_ids, swap_host = k["swap_ids"], k["swap_host"]
 
     # ---- swap bandwidth alone (both directions, pinned host)
     ids = batch.used_blocks[:min(len(batch.used_blocks), 4096)].astype(np.int32)
-    sh = torch.empty((len(ids), 2, batch.num_kv_heads, 16, D), dtype=kv_t).pin_memory()
+    sh = torch.empty((len(ids), 2, batch.num_kv_heads, 16, D), dtype=k["kv_t"]).pin_memory()
     pkv.pkv_swap_out(pool, ids, sh)
     torch.cuda.synchronize()
     e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -470,8 +593,8 @@ def run_ours(args):
     e2.record(main)
     torch.cuda.synchronize()
     swap_bw_bytes = sh.numel() * sh.element_size()
-    swap_out_gbs = swap_bw_bytes / (e0.elapsed_time(e1) / 1e3) / 1e9
-    swap_in_gbs = swap_bw_bytes / (e1.elapsed_time(e2) / 1e3) / 1e9
+    swap = {"out_gbs": swap_bw_bytes / (e0.elapsed_time(e1) / 1e3) / 1e9,
+            "in_gbs": swap_bw_bytes / (e1.elapsed_time(e2) / 1e3) / 1e9, "bytes": swap_bw_bytes}
     del sh
 
     # ---- layer-pipelined swap-in.  L layers, each its own pool holding the
@@ -486,9 +609,9 @@ def run_ours(args):
     #            for its own blocks.
     pipe = None
     if args.swap_layers > 0:
-        layers = [(pool, ws)]
+        layers = [(pool, k["ws"])]
         for _ in range(args.swap_layers - 1):
-            p = pkv.Pool(batch.num_blocks, batch.num_kv_heads, D, device=dev, **pool_kw)
+            p = pkv.Pool(batch.num_blocks, batch.num_kv_heads, D, device=dev, **k["pool_kw"])
             p.k.copy_(pool.k)
             p.v.copy_(pool.v)
             layers.append((p, p.workspace(pkv.pkv_paged_attn_workspace_size(p, Hq, meta))))
@@ -501,7 +624,7 @@ def run_ours(args):
         def layer_step(p, w):
             pkv.pkv_append(p, d["block_tables"], d["cu_q_lens"], d["q_positions"], d["k_new"], d["v_new"])
             pkv.pkv_paged_attn(p, d["q"], d["q_positions"], d["block_tables"], d["ctx_lens"], d["cu_q_lens"],
-                               meta, batch.scale, out=out, lse=lse, workspace=w)
+                               meta, batch.scale, out=k["out"], lse=k["lse"], workspace=w)
 
         def run_mode(mode):
             if mode == "ahead":
@@ -520,7 +643,7 @@ def run_ours(args):
         times = {m: [] for m in modes}
         for i in range(args.swap_steps):
             for m in modes:   # interleaved, so that clock drift hits every mode alike
-                l2_flush()
+                B.l2_flush()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(main)
                 run_mode(m)
@@ -532,75 +655,85 @@ def run_ours(args):
             if pkv.pkv_check_device_errors(p) != 0:
                 raise RuntimeError("device error word set in the swap-in pipeline")
         exposed = ms["serial"] - ms["compute"]
-        pipe = {"layers": len(layers), "swap_in_bytes_per_layer": swap_bytes, "steps": args.swap_steps,
-                "ms_per_step_median": ms,
+        pipe = {"layers": len(layers), "swap_in_bytes_per_layer": swap_host.numel() * swap_host.element_size(),
+                "steps": args.swap_steps, "ms_per_step_median": ms,
                 "swap_in_hidden_frac": (ms["serial"] - ms["ahead"]) / exposed if exposed > 0 else None}
         for p, _ in layers[1:]:
             p.close()
         del layers, hosts
+    return swap, pipe
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_attention_25_gb300 import build as pkv_build
+
+    world, rank, local = dist_info()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        pkv_build.build()
+    barrier()
+    pkv_build.build()   # no-op when fresh; other ranks wait for rank 0 above
+    args.gpus = world
+    B = Bench(args, dev)
+
+    head, keep = measure_workload(B, args.workload, True, rank, world)
+    swap, pipe = headline_extras(B, keep)
+    batch = keep["batch"]
+    keep["pool"].close()
+    del keep
+    torch.cuda.empty_cache()
+
+    if args.workloads == "all":
+        names = list(ALL_WORKLOADS)
+    elif args.workloads == "none":
+        names = []
+    else:
+        names = [n for n in args.workloads.split(",") if n]
+    per = {args.workload: {k: head[k] for k in ("value", "ms_per_step", "e2e", "e2e_replan", "roofline_per_kernel",
+                                                "kernels_one_at_a_time", "plan", "kv_gbs", "tflops")}}
+    from paged_kv_attention_25_gb300 import pkv
+    for n in names:
+        if n == args.workload:
+            continue
+        try:
+            r, _ = measure_workload(B, n, False, rank, world)
+        except pkv.PkvError as e:
+            if e.code != pkv.PKV_EUNSUPPORTED:
+                raise
+            per[n] = {"unsupported": str(e)}
+            torch.cuda.empty_cache()
+            continue
+        per[n] = {k: r[k] for k in ("value", "ms_per_step", "e2e", "e2e_replan", "roofline_per_kernel",
+                                    "kernels_one_at_a_time", "plan", "kv_gbs", "tflops")}
+        per[n]["config"] = r["config"]
+        torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
-
-    # ---- roofline of the dominant kernel
-    peaks, peak_src = load_peaks()
-    fam = {k: v for k, v in prof.items() if k in ("split_kv", "tensor_core") and v["launches"]}
-
-    def work(k):   # algorithmic bytes and flops of one launch of kernel family k
-        if k == "split_kv":
-            return st["decode_kv_bytes"] + st["decode_io_bytes"], st["decode_flops"]
-        return st["tc_kv_bytes"] + st["tc_io_bytes"], st["tc_flops"]
-
-    def roof_time(k):   # the kernel's time at its roofline (the larger of HBM and tensor time)
-        nb, fl = work(k)
-        return max(nb / (peaks["hbm_gbs"] * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
-
-    # The dominant kernel is the one with the most work at its roofline.  (The
-    # split-KV kernel is launched first on a second stream and the tensor-core
-    # kernel's CTAs wait for SMs, so the tensor-core kernel's event window also
-    # covers part of the split-KV kernel when both run: measured time would pick
-    # the wrong one.)
-    dom = max(fam, key=roof_time) if fam else None
-    roof = None
-    if dom:
-        avg_s = fam[dom]["total_ms"] / fam[dom]["launches"] / 1e3
-        nbytes, flops = work(dom)
-        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-        t_tc = flops / (peaks["bf16_tflops"] * 1e12)
-        if t_tc > t_hbm:
-            achieved, peak, unit, bound = flops / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor"
-        else:
-            achieved, peak, unit, bound = nbytes / avg_s / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
-        roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "peak_source": f"{peak_src} (burst)",
-                "traffic": recorded_traffic(dom, batch.name + ("_fp8" if fp8 else "")), "algorithmic_bytes": nbytes,
-                "algorithmic_flops": flops, "avg_launch_us": avg_s * 1e6}
-
-    step_ms_avg = 1e3 * secs_all / args.steps
-    kv_bytes = st["decode_kv_bytes"] + st["tc_kv_bytes"]
+    fp8 = args.kv_dtype == "fp8_e4m3"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_ms_avg, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8_e4m3 KV, bf16 Q/O, fp32 softmax" if fp8 else "bf16", "data": "synthetic",
-        "config": {**batch.describe(), "kv_dtype": args.kv_dtype,
-                   "l2": "flushed between steps (258 MB write, then 258 MB read)",
-                   "e2e_l2": "no flush: each step reads all visible KV and moves its inputs/outputs (working set >> 129 MB L2)",
-                   "parallelism": f"replicas x{world}", "swap_out_bytes_per_step": swap_bytes},
-        "kv_gbs": kv_bytes / (step_ms_avg / 1e3) / 1e9,
-        "tflops": (st["decode_flops"] + st["tc_flops"]) / (step_ms_avg / 1e3) / 1e12,
-        "kernels": {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(1, v["launches"])}
-                    for k, v in prof.items()},
-        "plan": {**{k: st[k] for k in ("num_decode_items", "num_tc_items", "num_merge_items")},
-                 "host_plan_us_uncached": plan_host_us},
-        "gpu_launches": int(sum(v["launches"] for v in prof.values())),
-        "roofline": roof,
-        "e2e": {"value": e_tok / e_sec, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "swap": {"out_gbs": swap_out_gbs, "in_gbs": swap_in_gbs, "bytes": swap_bw_bytes},
-        "swap_in_pipeline": pipe,
-        "clocks": clk.summary(),
-        "wall_s_timed": wall1 - wall0,
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3 KV, bf16 Q/O, fp32 softmax" if fp8 else "bf16",
+        "data": "synthetic", "config": head["config"],
+        "kv_gbs": head["kv_gbs"], "tflops": head["tflops"], "kernels": head["kernels"],
+        "kernels_one_at_a_time": head["kernels_one_at_a_time"],
+        "ms_per_step_one_at_a_time": head["ms_per_step_one_at_a_time"],
+        "plan": head["plan"], "gpu_launches": head["gpu_launches"],
+        "roofline": head["roofline"], "roofline_per_kernel": head["roofline_per_kernel"],
+        "e2e": head["e2e"], "e2e_replan": head["e2e_replan"],
+        "swap": swap, "swap_in_pipeline": pipe, "swap_out_bytes_per_step": head["swap_out_bytes_per_step"],
+        "clocks": head["clocks"], "wall_s_timed": head["wall_s_timed"],
+        "per_workload": per,
     }
     if world == 1 and not args.no_cpu_baseline:
         rate, dt, n, thr, desc = oracle_sample(batch, args.cpu_seconds, kv_dtype=args.kv_dtype)

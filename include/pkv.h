@@ -129,6 +129,8 @@ typedef struct {
   int64_t decode_io_bytes;  /* Q read + O/LSE written for the split-KV kernel's rows */
   int64_t tc_io_bytes;      /* Q read + O/LSE written for the tensor-core kernel's rows */
   size_t workspace_bytes;   /* what pkv_paged_attn needs for this batch */
+  int64_t plans_built;      /* pkv_last_plan_stats: plans this pool has built so far
+                               (a call whose metadata equals the cached plan's builds none) */
 } pkv_plan_stats;
 
 /* Accumulated device time per kernel family while profiling is on. */
@@ -169,6 +171,10 @@ int pkv_append(pkv_pool* pool, const int32_t* block_tables, int max_blocks, int 
  * Workspace bytes pkv_paged_attn needs for this batch (plans the batch on the
  * host; the plan is cached and reused by a following pkv_paged_attn with the
  * same metadata).  Synchronous, host only.
+ * Plan cache: a pool keeps its last plan together with exact copies of the
+ * parameters and host metadata (cu_q_lens, ctx_lens, q_positions) it was
+ * built from, and reuses it only when a call's are equal element by element;
+ * any other batch is planned afresh.
  */
 int pkv_paged_attn_workspace_size(pkv_pool* pool, int num_q_heads, int num_reqs, int num_tokens,
                                   const pkv_host_meta* host_meta, size_t* bytes);
@@ -228,16 +234,21 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
  * library holds until the process exits.  The call makes no cudaMalloc,
  * cudaFree or other allocating call.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current).  Make that first
- *     call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and creates the one
+ *     CUDA event that orders calls (below).  Make that first call before any
+ *     stream capture.
  *   - A batch whose plan needs more scratch than PKV_STATIC_SCRATCH_BYTES is
  *     rejected with PKV_EINVAL before anything is launched; use
  *     pkv_paged_attn with a caller workspace for it.
  *   - Every call uses the same array, which keeps the last call's contents.
- *     Nothing in it is read before the same call writes it, so no clearing is
- *     needed, but calls whose work overlaps on the GPU (on different streams,
- *     or enqueued while an earlier one still runs elsewhere) race on it:
- *     serialise them, e.g. on one stream.
+ *     Nothing in it is read before the same call writes it (the merge
+ *     counters are cleared by the call's own upload), so no clearing is
+ *     needed.  Calls on one device are ordered on the GPU in the order they
+ *     were made, whatever their pools and streams: each call's upload into the
+ *     array waits for the previous call's kernels (an event the library
+ *     records after them), and the host side holds a lock for the call's
+ *     duration.  Work that other code runs on the array is not ordered: the
+ *     array is this entry point's alone.
  */
 #define PKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int pkv_paged_attn_static(pkv_pool* pool, const void* q, int num_q_heads, const int32_t* q_positions,
@@ -302,20 +313,12 @@ int pkv_swap_in_finish(pkv_pool* pool, void* stream);
 
 /*
  * Copy `bytes` bytes between device memory and host memory, asynchronously on
- * `stream`: for moving a step's inputs in and its outputs out next to the
- * attention kernels.  With pinned host memory (cudaHostAlloc / registered) a
- * kernel on a few SMs moves the bytes through the host memory's device
- * mapping (24 CTAs to the device, 8 to the host: about the CPU-GPU link's rate
- * either way).  Beside the HBM-bound attention kernels alone such a copy
- * slows them far less than a copy-engine transfer of the same bytes (measured
- * on GB300: a 68 MB input copy beside a 200 us attention step, 363 us per step
- * against 438 us); in a pipelined loop that also moves outputs and swaps,
- * copy-engine transfers measured faster, as the copy kernels then hold SMs the
- * tensor-core kernel needs.  With pageable host memory the call falls back to
- * cudaMemcpyAsync.
- * Any sizes and alignments are accepted (16-byte chunks where both ends are
- * 16-byte aligned, bytes otherwise).  Errors: PKV_EINVAL for NULL pointers
- * with bytes > 0, PKV_ECUDA for a failed launch or copy.
+ * `stream`, by the copy engines (cudaMemcpyAsync): how a serving loop moves a
+ * step's inputs in and its outputs out next to the library's calls.  Pinned
+ * host memory (cudaHostAlloc / registered) makes the copy asynchronous; with
+ * pageable memory the driver may serialise it with the host.  Any sizes and
+ * alignments.  Errors: PKV_EINVAL for NULL pointers with bytes > 0, PKV_ECUDA
+ * for a failed copy.
  */
 int pkv_copy_to_device(void* dst, const void* host_src, size_t bytes, void* stream);
 int pkv_copy_to_host(void* host_dst, const void* src, size_t bytes, void* stream);
@@ -372,10 +375,27 @@ int pkv_cache_free_blocks(const pkv_cache* cache, int* gpu_free, int* cpu_free);
  * timeout bit was), else PKV_OK. */
 int pkv_check_device_errors(pkv_pool* pool, void* stream, unsigned* flags);
 
+/* Test and diagnostic settings of a pool, for checking the failure path
+ * without a GPU fault:
+ *   PKV_DEBUG_WAIT_LIMIT_NS: wall-clock limit of every bounded wait in this
+ *     pool's attention kernels (default 1 s; 1 us .. 60 s);
+ *   PKV_DEBUG_WITHHOLD_COPY: 1 (2) = the first CTA of the split-KV
+ *     (tensor-core) kernel never issues its first K copy, so that the wait for
+ *     it runs out: the kernel records PKV_DEVERR_TIMEOUT, drains its copies,
+ *     frees what it holds and returns, and that call's outputs are undefined;
+ *     0 = off (default).
+ * Errors: PKV_EINVAL for an unknown setting or a value out of range. */
+#define PKV_DEBUG_WAIT_LIMIT_NS 1
+#define PKV_DEBUG_WITHHOLD_COPY 2
+int pkv_debug_set(pkv_pool* pool, int what, int64_t value);
+
 /* Kernel timing with CUDA events recorded around every launch on the launch
- * stream.  Enabling adds one event pair per launch.  pkv_profile_read
- * synchronises the recorded events, adds their durations into *out and, if
- * reset != 0, clears the totals. */
+ * stream.  on: 0 off, 1 on, 2 on with the two attention kernels of a call run
+ * one after the other on the caller's stream (instead of side by side), so
+ * that each kernel's events bracket its own execution alone.  Enabling adds
+ * one event pair per launch.  pkv_profile_read synchronises the recorded
+ * events, adds their durations into *out and, if reset != 0, clears the
+ * totals. */
 int pkv_profile_enable(pkv_pool* pool, int on);
 int pkv_profile_read(pkv_pool* pool, pkv_profile* out, int reset);
 

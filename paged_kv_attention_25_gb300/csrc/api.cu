@@ -102,8 +102,13 @@ struct pkv_pool {
   bool swap_pending = false;
   std::vector<int32_t> swap_ids;
 
-  // profiling
+  // Test and diagnostic settings (pkv_debug_set).
+  uint64_t wait_ns = 1000000000ull;   // limit of every bounded wait in the kernels
+  int withhold = 0;                   // see AttnArgs::withhold
+
+  // profiling (prof_mode 2: the two attention kernels run one after the other)
   bool prof_on = false;
+  int prof_mode = 0;
   std::vector<cudaEvent_t> ev_free;
   std::vector<ProfRec> pending;
   pkv_profile totals{};
@@ -391,15 +396,14 @@ int pkv_append(pkv_pool* pool, const int32_t* block_tables, int max_blocks, int 
   return PKV_OK;
 }
 
-static int plan_for(pkv_pool* pool, int num_q_heads, int num_reqs, int num_tokens, int max_blocks,
-                    const pkv_host_meta* meta) {
+// Plans the batch into pool->plan unless the cached plan was built from
+// exactly the same parameters and host metadata (element-wise comparison).
+static int plan_for(pkv_pool* pool, int num_q_heads, int num_reqs, int num_tokens, const pkv_host_meta* meta) {
   if (!meta) return fail(PKV_EINVAL, "host_meta is NULL");
-  PlanParams pp{num_q_heads, pool->num_kv_heads, pool->head_dim, pool->num_sms, num_reqs, num_tokens, max_blocks,
+  PlanParams pp{num_q_heads, pool->num_kv_heads, pool->head_dim, pool->num_sms, num_reqs, num_tokens,
                 pool->elem_bytes};
-  const uint64_t sig = plan_signature(pp, *meta);
-  if (pool->plan.valid && pool->plan.signature == sig) return PKV_OK;
+  if (plan_matches(pool->plan, pp, *meta)) return PKV_OK;
   const char* err = "plan failed";
-  pool->plan.valid = false;
   int rc = build_plan(pp, *meta, &pool->plan, &err);
   if (rc) return fail(rc, err);
   return PKV_OK;
@@ -411,35 +415,45 @@ int pkv_paged_attn_workspace_size(pkv_pool* pool, int num_q_heads, int num_reqs,
   if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads) return fail(PKV_EINVAL, "num_q_heads must be a multiple of num_kv_heads");
   if (num_reqs < 0 || num_tokens < 0) return fail(PKV_EINVAL, "negative size");
   std::lock_guard<std::mutex> lk(pool->mu);
-  int rc = plan_for(pool, num_q_heads, num_reqs, num_tokens, 0, host_meta);
+  int rc = plan_for(pool, num_q_heads, num_reqs, num_tokens, host_meta);
   if (rc) return rc;
   *bytes = pool->plan.total;
   return PKV_OK;
 }
 
-int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t* q_positions,
-                   const int32_t* block_tables, int max_blocks, const int32_t* ctx_lens, const int32_t* cu_q_lens,
-                   int num_reqs, int num_tokens, const pkv_host_meta* host_meta, float scale, void* o, float* lse,
-                   void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   if (!pool) return fail(PKV_EINVAL, "pool is NULL");
-  if (num_tokens < 0 || num_reqs < 0) return fail(PKV_EINVAL, "negative size");
-  if (num_tokens == 0) return PKV_OK;
-  if (num_q_heads < 1 || num_q_heads % pool->num_kv_heads) return fail(PKV_EINVAL, "num_q_heads must be a multiple of num_kv_heads");
-  if (num_q_heads / pool->num_kv_heads > kTcRows) return fail(PKV_EUNSUPPORTED, "group size above 128");
-  if (num_reqs < 1 || max_blocks < 1) return fail(PKV_EINVAL, "num_reqs and max_blocks must be >= 1");
-  if (!q || !q_positions || !block_tables || !ctx_lens || !cu_q_lens || !o) return fail(PKV_EINVAL, "NULL device pointer");
-  if (!aligned16(q) || !aligned16(o)) return fail(PKV_EINVAL, "q and o must be 16-byte aligned");
-  if (!(scale > 0.f)) return fail(PKV_EINVAL, "scale must be positive");
-  int rc = finish_swap_in(pool, stream);
+  if (c.num_tokens < 0 || c.num_reqs < 0) return fail(PKV_EINVAL, "negative size");
+  if (c.num_tokens == 0) return PKV_OK;
+  if (c.num_q_heads < 1 || c.num_q_heads % pool->num_kv_heads)
+    return fail(PKV_EINVAL, "num_q_heads must be a multiple of num_kv_heads");
+  if (c.num_q_heads / pool->num_kv_heads > kTcRows) return fail(PKV_EUNSUPPORTED, "group size above 128");
+  if (c.num_reqs < 1 || c.max_blocks < 1) return fail(PKV_EINVAL, "num_reqs and max_blocks must be >= 1");
+  if (!c.q || !c.q_positions || !c.block_tables || !c.ctx_lens || !c.cu_q_lens || !c.o)
+    return fail(PKV_EINVAL, "NULL device pointer");
+  if (!aligned16(c.q) || !aligned16(c.o)) return fail(PKV_EINVAL, "q and o must be 16-byte aligned");
+  if (!(c.scale > 0.f)) return fail(PKV_EINVAL, "scale must be positive");
+  int rc = finish_swap_in(pool, c.stream);
   if (rc) return rc;
   std::lock_guard<std::mutex> lk(pool->mu);
-  rc = plan_for(pool, num_q_heads, num_reqs, num_tokens, max_blocks, host_meta);
+  rc = plan_for(pool, c.num_q_heads, c.num_reqs, c.num_tokens, c.host_meta);
   if (rc) return rc;
+  const char* err = "";
+  if ((rc = check_ctx_fits(*c.host_meta, c.num_reqs, c.max_blocks, &err))) return fail(rc, err);
   const Plan& pl = pool->plan;
   if (pool->elem_bytes == 1 && !pl.tc.empty())
     return fail(PKV_EUNSUPPORTED, "fp8 pools take decode-regime batches only: every request needs q_len * G <= 4");
-  if (!workspace || workspace_bytes < pl.total) return fail(PKV_EINVAL, "workspace missing or smaller than pkv_paged_attn_workspace_size()");
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(PKV_EINVAL, "workspace must be 256-byte aligned");
+  if (c.static_scratch) {
+    if (pl.total > c.workspace_bytes)
+      return fail(PKV_EINVAL, "pkv_paged_attn_static: this batch needs " + std::to_string(pl.total) +
+                                  " bytes of scratch, above the static limit of " + std::to_string(c.workspace_bytes) +
+                                  " bytes; use pkv_paged_attn with a caller workspace");
+  } else if (!c.workspace || c.workspace_bytes < pl.total) {
+    return fail(PKV_EINVAL, "workspace missing or smaller than pkv_paged_attn_workspace_size()");
+  }
+  if (reinterpret_cast<uintptr_t>(c.workspace) & 255u) return fail(PKV_EINVAL, "workspace must be 256-byte aligned");
 
   // Upload the work lists: through a pinned staging slot (asynchronous; the
   // slot is reused only after its previous upload has completed), or for an
@@ -447,10 +461,12 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   // copy runs on the pool's copy stream after the previous call's kernels, so
   // it overlaps whatever the caller queued on `stream` before this call.
   const size_t meta_bytes = pl.off_part_o;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+  uint8_t* ws = static_cast<uint8_t*>(c.workspace);
   if (meta_bytes) {
     PKV_CUDA(cudaStreamWaitEvent(pool->copy, pool->ws_free, 0), "upload wait");
+    // Scratch shared with other pools: also wait for the last call that used it.
+    if (c.scratch_free) PKV_CUDA(cudaStreamWaitEvent(pool->copy, static_cast<cudaEvent_t>(c.scratch_free), 0), "scratch wait");
     uint8_t* host = nullptr;
     const bool use_pinned = meta_bytes <= pkv_pool::kStagingBytes;
     if (use_pinned) {
@@ -476,24 +492,26 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
 
   AttnArgs a;
   a.pool = pool->view();
-  a.q = q;
-  a.num_q_heads = num_q_heads;
-  a.group = num_q_heads / pool->num_kv_heads;
-  a.q_positions = q_positions;
-  a.block_tables = block_tables;
-  a.max_blocks = max_blocks;
-  a.ctx_lens = ctx_lens;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.o = o;
-  a.lse = lse;
+  a.q = c.q;
+  a.num_q_heads = c.num_q_heads;
+  a.group = c.num_q_heads / pool->num_kv_heads;
+  a.q_positions = c.q_positions;
+  a.block_tables = c.block_tables;
+  a.max_blocks = c.max_blocks;
+  a.ctx_lens = c.ctx_lens;
+  a.scale_log2 = c.scale * 1.4426950408889634f;
+  a.o = c.o;
+  a.lse = c.lse;
   a.part_o = reinterpret_cast<float*>(ws + pl.off_part_o);
   a.part_lse = reinterpret_cast<float*>(ws + pl.off_part_lse);
   a.merge_dec = reinterpret_cast<const MergeItem*>(ws + pl.off_merge_dec);
   a.merge_cnt = reinterpret_cast<int*>(ws + pl.off_merge_cnt);
   a.q_box_tokens = 0;
+  a.wait_ns = pool->wait_ns;
+  a.withhold = pool->withhold;
   CUtensorMap tmap_q;
   if (!pl.tc.empty()) {
-    rc = make_q_tmap(&tmap_q, q, num_tokens, num_q_heads, pool->head_dim, a.group, &a.q_box_tokens);
+    rc = make_q_tmap(&tmap_q, c.q, c.num_tokens, c.num_q_heads, pool->head_dim, a.group, &a.q_box_tokens);
     if (rc) return rc;
   }
 
@@ -506,10 +524,12 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   // stream is dispatched first (the side stream waits on the fork event), so
   // the split-KV CTAs (three per SM) take the SMs and tensor-core CTAs (one SM
   // each) fill them as the split-KV work drains; that order measured as fast
-  // as or faster than the reverse on every mixed workload.
-  const bool fork = !pl.tc.empty() && !pl.decode.empty();
-  void* dec_stream = stream;
-  void* tc_stream = stream;
+  // as or faster than the reverse on every mixed workload.  In the serialised
+  // profiling mode both run on the caller's stream, one after the other, so
+  // that each kernel's timing events bracket its own execution only.
+  const bool fork = !pl.tc.empty() && !pl.decode.empty() && pool->prof_mode != 2;
+  void* dec_stream = c.stream;
+  void* tc_stream = c.stream;
   if (fork) {
     PKV_CUDA(cudaEventRecord(pool->fork, s), "fork record");
     PKV_CUDA(cudaStreamWaitEvent(pool->side, pool->fork, 0), "fork wait");
@@ -531,12 +551,40 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
     PKV_CUDA(cudaStreamWaitEvent(s, pool->join, 0), "join wait");
   }
   if (!pl.merge.empty()) {
-    rc = timed_launch(pool, 3, stream, [&] { return launch_merge(a, d_merge, static_cast<int>(pl.merge.size()), stream); });
+    rc = timed_launch(pool, 3, c.stream,
+                      [&] { return launch_merge(a, d_merge, static_cast<int>(pl.merge.size()), c.stream); });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "merge launch");
   }
   // The next call's upload may overwrite the work lists once these kernels are done.
   PKV_CUDA(cudaEventRecord(pool->ws_free, s), "workspace release");
+  if (c.scratch_free) PKV_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(c.scratch_free), s), "scratch release");
   return PKV_OK;
+}
+
+extern "C" {
+
+int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t* q_positions,
+                   const int32_t* block_tables, int max_blocks, const int32_t* ctx_lens, const int32_t* cu_q_lens,
+                   int num_reqs, int num_tokens, const pkv_host_meta* host_meta, float scale, void* o, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  AttnCall c;
+  c.q = q;
+  c.num_q_heads = num_q_heads;
+  c.q_positions = q_positions;
+  c.block_tables = block_tables;
+  c.max_blocks = max_blocks;
+  c.ctx_lens = ctx_lens;
+  c.cu_q_lens = cu_q_lens;
+  c.num_reqs = num_reqs;
+  c.num_tokens = num_tokens;
+  c.host_meta = host_meta;
+  c.scale = scale;
+  c.o = o;
+  c.lse = lse;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.stream = stream;
+  return paged_attn_call(pool, c);
 }
 
 int pkv_plan_inspect(int num_q_heads, int num_kv_heads, int head_dim, int num_sms, int num_reqs, int num_tokens,
@@ -546,7 +594,7 @@ int pkv_plan_inspect(int num_q_heads, int num_kv_heads, int head_dim, int num_sm
   if (head_dim != 64 && head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
   Plan plan;
   const char* err = "plan failed";
-  PlanParams pp{num_q_heads, num_kv_heads, head_dim, num_sms, num_reqs, num_tokens, 0};
+  PlanParams pp{num_q_heads, num_kv_heads, head_dim, num_sms, num_reqs, num_tokens};
   const int rc = build_plan(pp, *host_meta, &plan, &err);
   if (rc) return fail(rc, err);
   const int total = static_cast<int>(plan.decode.size() + plan.tc.size());
@@ -569,6 +617,7 @@ int pkv_last_plan_stats(const pkv_pool* pool, pkv_plan_stats* out) {
   if (!pool || !out) return fail(PKV_EINVAL, "pool/out is NULL");
   if (!pool->plan.valid) return fail(PKV_EINVAL, "no plan built yet");
   *out = pool->plan.stats;
+  out->plans_built = pool->plan.builds;
   return PKV_OK;
 }
 
@@ -674,29 +723,12 @@ int pkv_swap_in_finish(pkv_pool* pool, void* stream) {
   return finish_swap_in(pool, stream);
 }
 
-// Host memory's device address if it is pinned and mapped, else nullptr.
-static void* mapped_device_address(const void* host) {
-  cudaPointerAttributes attr{};
-  if (cudaPointerGetAttributes(&attr, host) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
-      attr.devicePointer != nullptr)
-    return attr.devicePointer;
-  cudaGetLastError();   // clear a failed query on pageable memory
-  return nullptr;
-}
-
-static int host_copy(void* dev, const void* host, size_t bytes, bool to_host, void* stream) {
+static int host_copy(void* dst, const void* src, size_t bytes, bool to_host, void* stream) {
   if (bytes == 0) return PKV_OK;
-  if (!dev || !host) return fail(PKV_EINVAL, "NULL pointer");
-  void* host_dev = mapped_device_address(host);
-  cudaError_t e;
-  if (host_dev) {
-    e = static_cast<cudaError_t>(to_host ? launch_host_copy(host_dev, dev, bytes, true, stream)
-                                         : launch_host_copy(dev, host_dev, bytes, false, stream));
-  } else {
-    e = cudaMemcpyAsync(to_host ? const_cast<void*>(host) : dev, to_host ? dev : host, bytes,
-                        to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
-  }
-  if (e != cudaSuccess) return cuda_fail(e, to_host ? "copy to host" : "copy to device");
+  if (!dst || !src) return fail(PKV_EINVAL, "NULL pointer");
+  PKV_CUDA(cudaMemcpyAsync(dst, src, bytes, to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice,
+                           static_cast<cudaStream_t>(stream)),
+           to_host ? "copy to host" : "copy to device");
   return PKV_OK;
 }
 
@@ -705,7 +737,7 @@ int pkv_copy_to_device(void* dst, const void* host_src, size_t bytes, void* stre
 }
 
 int pkv_copy_to_host(void* host_dst, const void* src, size_t bytes, void* stream) {
-  return host_copy(const_cast<void*>(src), host_dst, bytes, true, stream);
+  return host_copy(host_dst, src, bytes, true, stream);
 }
 
 int pkv_check_device_errors(pkv_pool* pool, void* stream, unsigned* flags) {
@@ -722,8 +754,27 @@ int pkv_check_device_errors(pkv_pool* pool, void* stream, unsigned* flags) {
 
 int pkv_profile_enable(pkv_pool* pool, int on) {
   if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  if (on < 0 || on > 2) return fail(PKV_EINVAL, "profile mode must be 0, 1 or 2");
   pool->prof_on = on != 0;
+  pool->prof_mode = on;
   return PKV_OK;
+}
+
+int pkv_debug_set(pkv_pool* pool, int what, int64_t value) {
+  if (!pool) return fail(PKV_EINVAL, "pool is NULL");
+  std::lock_guard<std::mutex> lk(pool->mu);
+  switch (what) {
+    case PKV_DEBUG_WAIT_LIMIT_NS:
+      if (value < 1000 || value > 60ll * 1000000000ll) return fail(PKV_EINVAL, "wait limit must be 1 us .. 60 s");
+      pool->wait_ns = static_cast<uint64_t>(value);
+      return PKV_OK;
+    case PKV_DEBUG_WITHHOLD_COPY:
+      if (value < 0 || value > 2) return fail(PKV_EINVAL, "withhold must be 0, 1 or 2");
+      pool->withhold = static_cast<int>(value);
+      return PKV_OK;
+    default:
+      return fail(PKV_EINVAL, "unknown debug setting");
+  }
 }
 
 int pkv_profile_read(pkv_pool* pool, pkv_profile* out, int reset) {

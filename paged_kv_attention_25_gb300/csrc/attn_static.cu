@@ -23,6 +23,9 @@ static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRAT
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_dev_addr[kMaxDevices] = {};
+// Recorded after each call's kernels; the next call's upload into the array
+// waits for it, so calls on any pools and streams follow one another.
+cudaEvent_t g_scratch_free[kMaxDevices] = {};
 
 }  // namespace
 
@@ -35,35 +38,46 @@ extern "C" int pkv_paged_attn_static(pkv_pool* pool, const void* q, int num_q_he
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return pkv::set_last_error(PKV_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return pkv::set_last_error(PKV_EUNSUPPORTED, "device index above 63");
-  void* scratch = nullptr;
-  {
-    // Host code cannot use g_static_scratch as an address: it names a host-side
-    // stand-in.  Look up the array's address on this device once, with the
-    // device current.
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_dev_addr[dev] == nullptr) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_static_scratch);
-      if (e != cudaSuccess || p == nullptr)
-        return pkv::set_last_error(PKV_ECUDA, std::string("cudaGetSymbolAddress(static scratch): ") +
-                                                  cudaGetErrorString(e));
-      g_scratch_dev_addr[dev] = p;
-    }
-    scratch = g_scratch_dev_addr[dev];
+  // Held for the whole call: the array's upload, kernels and release event of
+  // one call are enqueued before the next call's.
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_dev_addr[dev] == nullptr) {
+    // Host code cannot use g_static_scratch as an address: it names a
+    // host-side stand-in.  Look up the array's address on this device once,
+    // with the device current.
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return pkv::set_last_error(PKV_ECUDA, std::string("cudaGetSymbolAddress(static scratch): ") +
+                                                cudaGetErrorString(e));
+    cudaEvent_t ev = nullptr;
+    e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess)
+      return pkv::set_last_error(PKV_ECUDA, std::string("cudaEventCreate(static scratch): ") + cudaGetErrorString(e));
+    g_scratch_free[dev] = ev;
+    g_scratch_dev_addr[dev] = p;
   }
-  if (num_tokens > 0) {
-    size_t need = 0;
-    const int rc = pkv_paged_attn_workspace_size(pool, num_q_heads, num_reqs, num_tokens, host_meta, &need);
-    if (rc != PKV_OK) return rc;
-    if (need > PKV_STATIC_SCRATCH_BYTES)
-      return pkv::set_last_error(
-          PKV_EINVAL, "pkv_paged_attn_static: this batch needs " + std::to_string(need) +
-                          " bytes of scratch, above the static limit of " +
-                          std::to_string(static_cast<size_t>(PKV_STATIC_SCRATCH_BYTES)) +
-                          " bytes; use pkv_paged_attn with a caller workspace");
-  }
-  // The work lists are rewritten and every partial row is written by this
-  // call before it is read, so nothing left by an earlier call needs clearing.
-  return pkv_paged_attn(pool, q, num_q_heads, q_positions, block_tables, max_blocks, ctx_lens, cu_q_lens, num_reqs,
-                        num_tokens, host_meta, scale, o, lse, scratch, PKV_STATIC_SCRATCH_BYTES, stream);
+  // One plan serves the size check and the call: the work lists are rewritten
+  // and every partial row is written by this call before it is read, so
+  // nothing left by an earlier call needs clearing.
+  pkv::AttnCall c;
+  c.q = q;
+  c.num_q_heads = num_q_heads;
+  c.q_positions = q_positions;
+  c.block_tables = block_tables;
+  c.max_blocks = max_blocks;
+  c.ctx_lens = ctx_lens;
+  c.cu_q_lens = cu_q_lens;
+  c.num_reqs = num_reqs;
+  c.num_tokens = num_tokens;
+  c.host_meta = host_meta;
+  c.scale = scale;
+  c.o = o;
+  c.lse = lse;
+  c.workspace = g_scratch_dev_addr[dev];
+  c.workspace_bytes = PKV_STATIC_SCRATCH_BYTES;
+  c.stream = stream;
+  c.static_scratch = true;
+  c.scratch_free = g_scratch_free[dev];
+  return pkv::paged_attn_call(pool, c);
 }

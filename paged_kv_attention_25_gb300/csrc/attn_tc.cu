@@ -241,7 +241,10 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       // where B reaches that key tile, else tile A's.  Before a stage's first
       // use, parity 1 of a fresh barrier passes at once.
       const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile[1] ? kKSt : 0) + st : B::kVEmpty + st;
-      if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort)) return false;
+      if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
+      // Test hook: CTA 0 never issues its first K tile, so that the issuer's
+      // bounded wait for it runs out.
+      if (a.withhold == 2 && is_k && j == 0 && blockIdx.x == 0) return true;
       if (lane == 0) mbar_arrive_expect_tx(full, bytes);
       __syncwarp();
       if (y >= 0) {
@@ -268,7 +271,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
       *s_abort = 1;
       for (int i = max(0, nl - nst); i < nl; ++i)
-        (void)mbar_wait(&bars[(is_k ? B::kKFull : B::kVFull) + i % nst], (i / nst) & 1, nullptr);
+        (void)mbar_wait(&bars[(is_k ? B::kKFull : B::kVFull) + i % nst], (i / nst) & 1, nullptr, a.wait_ns);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
@@ -300,7 +303,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       }
     }
     __syncwarp();
-    bool ok = mbar_wait_warp(&bars[B::kQ], 0, s_abort) && mbar_wait_warp(&bars[B::kQ + 1], 0, s_abort);
+    bool ok = mbar_wait_warp(&bars[B::kQ], 0, s_abort, a.wait_ns) && mbar_wait_warp(&bars[B::kQ + 1], 0, s_abort, a.wait_ns);
     const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
     // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage).
     auto issue_s = [&](int t, int j) {
@@ -339,7 +342,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       if (lane == 0) tc_commit(&bars[bar]);
     };
     if (ok && ntiles > 0) {
-      if ((ok = mbar_wait_warp(&bars[B::kKFull], 0, s_abort))) {
+      if ((ok = mbar_wait_warp(&bars[B::kKFull], 0, s_abort, a.wait_ns))) {
         tc_fence_after();
         if (ntile[0] > 0) issue_s(0, 0);
         if (ntile[1] > 0) issue_s(1, 0);
@@ -347,7 +350,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     }
     for (int j = 0; ok && j < ntiles; ++j) {
       bool k_next = false;                // K(j+1) seen in its stage
-      if (!(ok = mbar_wait_warp(&bars[B::kVFull + j % kVSt], (j / kVSt) & 1, s_abort))) break;
+      if (!(ok = mbar_wait_warp(&bars[B::kVFull + j % kVSt], (j / kVSt) & 1, s_abort, a.wait_ns))) break;
       if (j == ntiles - 1 && last_nkeys < kNK) {
         // Keys past the item's end in its last tile: zero their V rows so that
         // 0 * stale data cannot produce NaN in the tensor core.
@@ -365,11 +368,11 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (j < ntile[t]) {
-          if (!(ok = mbar_wait_warp(&bars[B::kP + t], j & 1, s_abort))) break;
+          if (!(ok = mbar_wait_warp(&bars[B::kP + t], j & 1, s_abort, a.wait_ns))) break;
           tc_fence_after();
           issue_pv(t, j);
           if (j + 1 < ntile[t]) {
-            if (!k_next && !(ok = mbar_wait_warp(&bars[B::kKFull + (j + 1) % kKSt], ((j + 1) / kKSt) & 1, s_abort)))
+            if (!k_next && !(ok = mbar_wait_warp(&bars[B::kKFull + (j + 1) % kKSt], ((j + 1) / kKSt) & 1, s_abort, a.wait_ns)))
               break;
             k_next = true;
             // No tcgen05 fence: TMA data is ordered by the K barrier, and the P
@@ -388,7 +391,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     }
     // Drain: every MMA issued has completed before TMEM is released.
     release(B::kDrain);
-    (void)mbar_wait_warp(&bars[B::kDrain], 0, nullptr);
+    (void)mbar_wait_warp(&bars[B::kDrain], 0, nullptr, a.wait_ns);
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue of tile X
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -400,7 +403,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int key0 = it.kv_start + j * kNK;
-      if (!mbar_wait_warp(&bars[B::kS + X * kKSt + j % kKSt], (j / kKSt) & 1, s_abort)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars[B::kS + X * kKSt + j % kKSt], (j / kKSt) & 1, s_abort, a.wait_ns)) { ok = false; break; }
       tc_fence_after();
       float s[kNK];
 #pragma unroll
@@ -468,7 +471,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       mbar_arrive(&bars[B::kP + X]);
     }
     if (ok && nt > 0) {
-      if (!mbar_wait_warp(&bars[B::kPv + X], 0, s_abort)) ok = false;
+      if (!mbar_wait_warp(&bars[B::kPv + X], 0, s_abort, a.wait_ns)) ok = false;
       tc_fence_after();
     }
     if (!ok) {
@@ -532,8 +535,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   // The query-tile copies have landed before shared memory is released (at
   // once unless a wait above gave up before the issuer saw them).
   if (threadIdx.x == 0) {
-    (void)mbar_wait(&bars[B::kQ], 0, nullptr);
-    (void)mbar_wait(&bars[B::kQ + 1], 0, nullptr);
+    (void)mbar_wait(&bars[B::kQ], 0, nullptr, a.wait_ns);
+    (void)mbar_wait(&bars[B::kQ + 1], 0, nullptr, a.wait_ns);
   }
   tc_fence_before();
   __syncthreads();

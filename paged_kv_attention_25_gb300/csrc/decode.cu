@@ -179,7 +179,10 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     const int src_lane = j & 31;
     const int pb = (j >> 5) == win ? __shfl_sync(0xffffffffu, ids_cur, src_lane)
                                    : __shfl_sync(0xffffffffu, ids_next, src_lane);
-    if (lane == 0) {
+    // Test hook: CTA 0's warp 0 never issues its first copy, so that its
+    // bounded wait for that stage runs out.
+    const bool withheld = a.withhold == 1 && j == 0 && blockIdx.x == 0 && warp == 0;
+    if (lane == 0 && !withheld) {
       const int st = j % kStages;
       uint8_t* dst = my_ring + st * S::kStage;
       if (pb >= 0) {
@@ -216,7 +219,7 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
       ids_next = load_ids(i + 32);
     }
     const int st = i % kStages;
-    if (!mbar_wait_warp(&my_full[st], (i / kStages) & 1, s_abort)) {
+    if (!mbar_wait_warp(&my_full[st], (i / kStages) & 1, s_abort, a.wait_ns)) {
       aborted = true;
       break;
     }
@@ -362,7 +365,7 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     *s_abort = 1;
     // Let this warp's copies in flight land before the CTA's shared memory is released.
     for (int j = consumed; j < min(nb_w, consumed + kStages); ++j)
-      (void)mbar_wait_warp(&my_full[j % kStages], (j / kStages) & 1, nullptr);
+      (void)mbar_wait_warp(&my_full[j % kStages], (j / kStages) & 1, nullptr, a.wait_ns);
   }
 
   // This warp's (m, l, acc) states for the CTA-wide merge.

@@ -63,7 +63,6 @@ struct PlanParams {
   int num_sms;
   int num_reqs;
   int num_tokens;
-  int max_blocks;   // block-table row length; 0 = not checked (host-only planning)
   int kv_elem_bytes = 2;   // bytes per pool element (2 bf16, 1 fp8)
 };
 
@@ -76,8 +75,14 @@ struct Plan {
   pkv_plan_stats stats{};
   // Workspace layout (byte offsets, 256-aligned sections).
   size_t off_decode = 0, off_tc = 0, off_merge = 0, off_merge_dec = 0, off_merge_cnt = 0, off_part_o = 0, off_part_lse = 0, total = 0;
-  uint64_t signature = 0;
   bool valid = false;
+  int64_t builds = 0;   // plans built into this object so far
+  // Cache key: exact copies of the parameters and host metadata the plan was
+  // built from.  (The block-table row length is not part of a plan: it only
+  // bounds ctx_lens, which check_ctx_fits tests on every call.)
+  PlanParams key_pp{};
+  std::vector<int32_t> key_cu, key_ctx, key_pos;
+  bool key_has_pos = false;
   // Scratch of the longest-first ordering.  A pool re-plans into the same Plan
   // whenever the batch changes, so every vector keeps its capacity from one
   // plan to the next: no reallocation, and no fresh pages to fault in.
@@ -90,7 +95,11 @@ int set_last_error(int code, const std::string& msg);
 
 // Host planner.  Returns PKV_OK or PKV_EINVAL (message in *err).
 int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, const char** err);
-uint64_t plan_signature(const PlanParams& pp, const pkv_host_meta& meta);
+// True if `plan` was built from exactly these parameters and metadata (the
+// plan cache: an element-wise comparison, so distinct batches never share a plan).
+bool plan_matches(const Plan& plan, const PlanParams& pp, const pkv_host_meta& meta);
+// PKV_EINVAL unless every ctx_lens[r] <= max_blocks * block_size.
+int check_ctx_fits(const pkv_host_meta& meta, int num_reqs, int max_blocks, const char** err);
 
 // Kernel launchers (defined in the .cu files); return cudaError_t as int.
 struct PoolView {
@@ -108,8 +117,6 @@ struct SwapIds {
   int32_t id[kSwapIdsPerLaunch];
 };
 
-// dst / src device addresses (host memory through its device mapping); any sizes.
-int launch_host_copy(void* dst, const void* src, size_t bytes, bool to_host, void* stream);
 // Moves n pool blocks to / from `buf`, laid out [n][2][Hkv][B][D]: host memory
 // through its device mapping, or a device buffer.  max_ctas = 0 takes the
 // CTA count that saturates the CPU-GPU link in that direction.
@@ -137,7 +144,37 @@ struct AttnArgs {
   const MergeItem* merge_dec;   // merge items of split-KV groups (merged by their last split)
   int* merge_cnt;               // splits finished per such item (zeroed by the work-list upload)
   int q_box_tokens;             // tokens per query-tile copy of the tensor-core kernel's Q tensor map
+  uint64_t wait_ns;             // wall-clock limit of every bounded wait in the kernels
+  int withhold;                 // test hook: 1 / 2 = CTA 0 of the split-KV / tensor-core kernel
+                                // skips its first K copy, so that a bounded wait runs out
 };
+
+// One paged-attention call as the C ABI receives it (pkv_paged_attn and its
+// variants), handled by paged_attn_call in api.cu.
+struct AttnCall {
+  const void* q = nullptr;
+  int num_q_heads = 0;
+  const int32_t* q_positions = nullptr;
+  const int32_t* block_tables = nullptr;
+  int max_blocks = 0;
+  const int32_t* ctx_lens = nullptr;
+  const int32_t* cu_q_lens = nullptr;
+  int num_reqs = 0, num_tokens = 0;
+  const pkv_host_meta* host_meta = nullptr;
+  float scale = 0.f;
+  void* o = nullptr;
+  float* lse = nullptr;
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
+  void* stream = nullptr;
+  // Scratch shared by every pool (the static entry point): workspace is that
+  // scratch, an over-size plan is reported against its fixed limit, and the
+  // work-list upload waits on scratch_free, which the call records again on
+  // `stream` after its kernels (so calls on any pools follow one another).
+  bool static_scratch = false;
+  void* scratch_free = nullptr;   // cudaEvent_t
+};
+int paged_attn_call(pkv_pool* pool, const AttnCall& c);
 
 int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream);
 // tmap_q: Q viewed as [T][Hq][D] with a (64, G, q_box_tokens) box (128-byte

@@ -54,22 +54,43 @@ struct QGroup {
 
 }  // namespace
 
-uint64_t plan_signature(const PlanParams& pp, const pkv_host_meta& meta) {
-  uint64_t h = 1469598103934665603ull;
-  auto mix = [&h](const void* p, size_t n) {
-    const unsigned char* b = static_cast<const unsigned char*>(p);
-    for (size_t i = 0; i < n; ++i) {
-      h ^= b[i];
-      h *= 1099511628211ull;
-    }
+bool plan_matches(const Plan& plan, const PlanParams& pp, const pkv_host_meta& meta) {
+  if (!plan.valid || !meta.cu_q_lens || !meta.ctx_lens) return false;
+  const PlanParams& k = plan.key_pp;
+  if (k.num_q_heads != pp.num_q_heads || k.num_kv_heads != pp.num_kv_heads || k.head_dim != pp.head_dim ||
+      k.num_sms != pp.num_sms || k.num_reqs != pp.num_reqs || k.num_tokens != pp.num_tokens ||
+      k.kv_elem_bytes != pp.kv_elem_bytes || plan.key_has_pos != (meta.q_positions != nullptr))
+    return false;
+  auto same = [](const std::vector<int32_t>& a, const int32_t* b, size_t n) {
+    return a.size() == n && (n == 0 || std::memcmp(a.data(), b, n * sizeof(int32_t)) == 0);
   };
-  mix(&pp, sizeof pp);
-  if (meta.cu_q_lens) mix(meta.cu_q_lens, sizeof(int32_t) * (pp.num_reqs + 1));
-  if (meta.ctx_lens) mix(meta.ctx_lens, sizeof(int32_t) * pp.num_reqs);
-  int has_pos = meta.q_positions != nullptr;
-  mix(&has_pos, sizeof has_pos);
-  if (has_pos) mix(meta.q_positions, sizeof(int32_t) * pp.num_tokens);
-  return h;
+  return same(plan.key_cu, meta.cu_q_lens, static_cast<size_t>(pp.num_reqs) + 1) &&
+         same(plan.key_ctx, meta.ctx_lens, static_cast<size_t>(pp.num_reqs)) &&
+         (!plan.key_has_pos || same(plan.key_pos, meta.q_positions, static_cast<size_t>(pp.num_tokens)));
+}
+
+namespace {
+
+// The cache key of a plan: exact copies of everything it was built from.
+void remember_key(Plan* plan, const PlanParams& pp, const pkv_host_meta& meta) {
+  plan->key_pp = pp;
+  plan->key_cu.assign(meta.cu_q_lens, meta.cu_q_lens + pp.num_reqs + 1);
+  plan->key_ctx.assign(meta.ctx_lens, meta.ctx_lens + pp.num_reqs);
+  plan->key_has_pos = meta.q_positions != nullptr;
+  if (plan->key_has_pos) plan->key_pos.assign(meta.q_positions, meta.q_positions + pp.num_tokens);
+  else plan->key_pos.clear();
+}
+
+}  // namespace
+
+int check_ctx_fits(const pkv_host_meta& meta, int num_reqs, int max_blocks, const char** err) {
+  const int64_t cap = static_cast<int64_t>(max_blocks) * kBlockSize;
+  for (int r = 0; r < num_reqs; ++r)
+    if (meta.ctx_lens[r] > cap) {
+      *err = "plan: ctx_len exceeds max_blocks * block_size";
+      return PKV_EINVAL;
+    }
+  return PKV_OK;
 }
 
 int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, const char** err) {
@@ -82,7 +103,6 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   plan->stats = pkv_plan_stats{};
   plan->off_decode = plan->off_tc = plan->off_merge = plan->off_merge_dec = plan->off_merge_cnt = 0;
   plan->off_part_o = plan->off_part_lse = plan->total = 0;
-  plan->signature = 0;
   plan->valid = false;
   const int R = pp.num_reqs, T = pp.num_tokens, Hq = pp.num_q_heads, Hkv = pp.num_kv_heads, D = pp.head_dim;
   if (R < 0 || T < 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) {
@@ -112,10 +132,6 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
     }
     if (ctx[r] < 0 || (cu[r + 1] > cu[r] && ctx[r] < 1)) {
       *err = "plan: a request with query tokens needs ctx_len >= 1";
-      return PKV_EINVAL;
-    }
-    if (pp.max_blocks > 0 && static_cast<int64_t>(ctx[r]) > static_cast<int64_t>(pp.max_blocks) * kBlockSize) {
-      *err = "plan: ctx_len exceeds max_blocks * block_size";
       return PKV_EINVAL;
     }
     if (pos) {
@@ -356,7 +372,8 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   off = align256(off + size_t(part_rows) * sizeof(float));
   plan->total = std::max<size_t>(off, 256);
   st.workspace_bytes = plan->total;
-  plan->signature = plan_signature(pp, meta);
+  remember_key(plan, pp, meta);
+  ++plan->builds;
   plan->valid = true;
   return PKV_OK;
 }

@@ -7,7 +7,8 @@
 
 namespace pkv {
 
-// A bounded wait gives up after this many nanoseconds of wall-clock time.
+// A bounded wait gives up after this many nanoseconds of wall-clock time
+// unless the launch passes another limit.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -50,24 +51,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity.  Returns false if the wall-clock
-// limit ran out or *abort became non-zero (another thread gave up first).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Wait for the phase with the given parity.  Returns false if `limit_ns` of
+// wall-clock time ran out or *abort became non-zero (another thread gave up first).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
 }
 
 // Warp-uniform wait: every lane of the warp calls it and all get the same answer
 // (true only if every lane saw the phase complete).
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns) {
+  const bool ok = mbar_wait(bar, parity, abort, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -58,54 +58,7 @@ __global__ void __launch_bounds__(kSwapThreads) swap_kernel(uint4* __restrict__ 
   }
 }
 
-// A flat copy of n16 16-byte chunks (then `tail` bytes) in the swap kernel's
-// pattern: each thread moves kUnroll chunks per round, loads before stores.
-__global__ void __launch_bounds__(kSwapThreads) host_copy_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src,
-                                                                 int64_t n16, const uint8_t* __restrict__ tail_src,
-                                                                 uint8_t* __restrict__ tail_dst, int tail) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kSwapThreads;
-  int64_t c = static_cast<int64_t>(blockIdx.x) * kSwapThreads + threadIdx.x;
-  for (; c + (kUnroll - 1) * stride < n16; c += kUnroll * stride) {
-    uint4 v[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) v[u] = src[c + u * stride];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) dst[c + u * stride] = v[u];
-  }
-  for (; c < n16; c += stride) dst[c] = src[c];
-  if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < tail) tail_dst[threadIdx.x] = tail_src[threadIdx.x];
-}
-
-// Byte copy for ends that are not 16-byte aligned.
-__global__ void __launch_bounds__(kSwapThreads) host_copy_bytes_kernel(uint8_t* __restrict__ dst,
-                                                                       const uint8_t* __restrict__ src, int64_t n) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kSwapThreads + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * kSwapThreads)
-    dst[i] = src[i];
-}
-
 }  // namespace
-
-int launch_host_copy(void* dst, const void* src, size_t bytes, bool to_host, void* stream) {
-  if (bytes == 0) return cudaSuccess;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int cap = to_host ? kSwapCtasOut : kSwapCtasIn;
-  if (((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) & 15u) == 0) {
-    const int64_t n16 = static_cast<int64_t>(bytes / 16);
-    const int tail = static_cast<int>(bytes % 16);
-    const int64_t want = (n16 + kSwapThreads - 1) / kSwapThreads;
-    const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
-    host_copy_kernel<<<grid, kSwapThreads, 0, s>>>(static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16,
-                                                   static_cast<const uint8_t*>(src) + n16 * 16,
-                                                   static_cast<uint8_t*>(dst) + n16 * 16, tail);
-  } else {
-    const int64_t want = (static_cast<int64_t>(bytes) + kSwapThreads - 1) / kSwapThreads;
-    const int grid = static_cast<int>(want < cap ? want : cap);
-    host_copy_bytes_kernel<<<grid, kSwapThreads, 0, s>>>(static_cast<uint8_t*>(dst), static_cast<const uint8_t*>(src),
-                                                         static_cast<int64_t>(bytes));
-  }
-  return cudaGetLastError();
-}
 
 int launch_swap(const PoolView& pool, void* kp, void* vp, void* host_dev, const int32_t* ids, int n, bool to_host,
                 int max_ctas, void* stream) {

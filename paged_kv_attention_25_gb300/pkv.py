@@ -32,6 +32,8 @@ PKV_DEVERR_BLOCK_ID = 1
 PKV_DEVERR_POSITION = 2
 PKV_DEVERR_TIMEOUT = 4
 PKV_DEVERR_INTERNAL = 8
+PKV_DEBUG_WAIT_LIMIT_NS = 1
+PKV_DEBUG_WITHHOLD_COPY = 2
 
 KERNELS = ("append", "split_kv", "tensor_core", "merge", "swap")
 
@@ -42,7 +44,7 @@ EXPORTED = (
     "pkv_plan_inspect", "pkv_swap_out", "pkv_swap_in", "pkv_swap_in_ahead", "pkv_swap_in_finish",
     "pkv_check_device_errors",
     "pkv_profile_enable", "pkv_profile_read", "pkv_device_sm_count", "pkv_last_error",
-    "pkv_version", "pkv_copy_to_device", "pkv_copy_to_host",
+    "pkv_version", "pkv_copy_to_device", "pkv_copy_to_host", "pkv_debug_set",
     "pkv_cache_create", "pkv_cache_destroy", "pkv_cache_step", "pkv_cache_release", "pkv_cache_free_blocks",
 )
 
@@ -73,7 +75,7 @@ class pkv_plan_stats(ctypes.Structure):
                 ("decode_kv_bytes", ctypes.c_int64), ("tc_kv_bytes", ctypes.c_int64),
                 ("decode_flops", ctypes.c_int64), ("tc_flops", ctypes.c_int64),
                 ("decode_io_bytes", ctypes.c_int64), ("tc_io_bytes", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("plans_built", ctypes.c_int64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -123,6 +125,7 @@ def load_library():
             "pkv_swap_in_finish": [P, P],
             "pkv_check_device_errors": [P, P, ctypes.POINTER(ctypes.c_uint)],
             "pkv_profile_enable": [P, I],
+            "pkv_debug_set": [P, I, ctypes.c_int64],
             "pkv_profile_read": [P, ctypes.POINTER(pkv_profile), I],
             "pkv_device_sm_count": [ctypes.POINTER(I)],
             "pkv_copy_to_device": [P, P, ctypes.c_size_t, P],
@@ -318,10 +321,10 @@ def pkv_paged_attn_static(pool: Pool, q, q_positions, block_tables, ctx_lens, cu
 
     The library keeps the work lists and split partials in a static device
     array of PKV_STATIC_SCRATCH_BYTES; larger batches raise PkvError
-    (PKV_EINVAL).  Calls share that array, so calls that overlap on the GPU
-    race; run them on one stream.  The first call on a device should come
-    before any stream capture.  (This wrapper allocates `out` / `lse` with
-    torch only when they are not given.)
+    (PKV_EINVAL).  Calls share that array; the library orders them on the GPU
+    in call order, whatever their pools and streams.  The first call on a
+    device should come before any stream capture.  (This wrapper allocates
+    `out` / `lse` with torch only when they are not given.)
     """
     _dev_bf16(q, "q")
     _dev_i32(q_positions, "q_positions")
@@ -428,7 +431,7 @@ def _same_bytes(a: torch.Tensor, b: torch.Tensor):
 
 
 def pkv_copy_to_device(dst: torch.Tensor, host_src: torch.Tensor, stream=None):
-    """dst (CUDA) <- host_src (CPU; pinned for the kernel path), asynchronously on `stream`."""
+    """dst (CUDA) <- host_src (CPU; pinned for an asynchronous copy), by the copy engines on `stream`."""
     if not dst.is_cuda or host_src.is_cuda:
         raise TypeError("dst must be a CUDA tensor and host_src a CPU tensor")
     _check(load_library().pkv_copy_to_device(dst.data_ptr(), host_src.data_ptr(), _same_bytes(dst, host_src),
@@ -436,7 +439,7 @@ def pkv_copy_to_device(dst: torch.Tensor, host_src: torch.Tensor, stream=None):
 
 
 def pkv_copy_to_host(host_dst: torch.Tensor, src: torch.Tensor, stream=None):
-    """host_dst (CPU; pinned for the kernel path) <- src (CUDA), asynchronously on `stream`."""
+    """host_dst (CPU; pinned for an asynchronous copy) <- src (CUDA), by the copy engines on `stream`."""
     if host_dst.is_cuda or not src.is_cuda:
         raise TypeError("host_dst must be a CPU tensor and src a CUDA tensor")
     _check(load_library().pkv_copy_to_host(host_dst.data_ptr(), src.data_ptr(), _same_bytes(host_dst, src),
@@ -482,8 +485,14 @@ def pkv_check_device_errors(pool: Pool, stream=None) -> int:
     return flags.value
 
 
-def pkv_profile_enable(pool: Pool, on: bool = True):
-    _check(load_library().pkv_profile_enable(pool.handle, 1 if on else 0))
+def pkv_profile_enable(pool: Pool, on=True):
+    """on: False/0 off, True/1 on, 2 on with the two attention kernels of a call run one after the other."""
+    _check(load_library().pkv_profile_enable(pool.handle, int(on)))
+
+
+def pkv_debug_set(pool: Pool, what: int, value: int):
+    """Test settings: PKV_DEBUG_WAIT_LIMIT_NS (bounded-wait limit) or PKV_DEBUG_WITHHOLD_COPY (0, 1, 2)."""
+    _check(load_library().pkv_debug_set(pool.handle, int(what), int(value)))
 
 
 def pkv_profile_read(pool: Pool, reset: bool = False) -> dict:

@@ -312,7 +312,7 @@ def sampled_rows(batch, n, seed):
 @pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("nbytes,offset", [(1 << 20, 0), (12345, 0), (4099, 3), (16, 0), (0, 0)])
 def test_host_copies_bit_exact(pinned, nbytes, offset):
-    """pkv_copy_to_device / pkv_copy_to_host: every byte, aligned or not, kernel (pinned) or DMA path."""
+    """pkv_copy_to_device / pkv_copy_to_host: every byte, aligned or not, pinned or pageable host memory."""
     rng = np.random.default_rng(nbytes + offset)
     src = torch.from_numpy(rng.integers(0, 256, nbytes + offset + 8, dtype=np.uint8))
     if pinned:
@@ -344,3 +344,33 @@ def test_full_size_workloads_sampled(name):
     o_np = bf16_to_f64(o)[t, h]
     l_np = lse.cpu().numpy().astype(np.float64)[t, h]
     assert_close(o_np, l_np, O, L, name)
+
+
+def test_plan_cache_tells_apart_batches_of_one_shape():
+    """Two batches with the same request and token counts on one pool: the second differs only in
+    one decode's context length and position, so it must be planned again (the cached plan's key
+    ranges would read one key too many) and still match the oracle."""
+    a = wl.random_small(31, num_q_heads=4, num_kv_heads=2, head_dim=128, num_reqs=8, max_ctx=3000, max_q=60)
+    dec = [r for r in range(a.num_reqs) if a.cu_q_lens[r + 1] - a.cu_q_lens[r] == 1 and a.ctx_lens[r] > 2]
+    assert dec, "the batch needs a decode request"
+    run = GpuRun(a)
+    run.step()
+    built = pkv.pkv_last_plan_stats(run.pool)["plans_built"]
+    kp, vp = oracle_pools(a)
+    b = wl.Batch(**{**a.__dict__})
+    b.ctx_lens = a.ctx_lens.copy()
+    b.q_positions = a.q_positions.copy()
+    r = dec[0]
+    b.ctx_lens[r] -= 1
+    b.q_positions[a.cu_q_lens[r]] -= 1
+    d = wl.upload(b)
+    meta = pkv.HostMeta(b.cu_q_lens, b.ctx_lens, b.q_positions)
+    pkv.pkv_append(run.pool, d["block_tables"], d["cu_q_lens"], d["q_positions"], d["k_new"], d["v_new"])
+    o, lse = pkv.pkv_paged_attn(run.pool, d["q"], d["q_positions"], d["block_tables"], d["ctx_lens"],
+                                d["cu_q_lens"], meta, b.scale)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_errors(run.pool) == 0
+    assert pkv.pkv_last_plan_stats(run.pool)["plans_built"] == built + 1
+    oracle.append(kp, vp, b.block_tables, b.cu_q_lens, b.q_positions, b.k_new, b.v_new)
+    O, L = oracle.paged_attn(b.q, kp, vp, b.block_tables, b.ctx_lens, b.cu_q_lens, b.q_positions, b.scale)
+    assert_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O, L, "second batch")
