@@ -292,10 +292,9 @@ def oracle_sample(batch, budget_s: float, kp=None, vp=None, kv_dtype: str = "bf1
     dt = run(pilot)
     per_tok = dt / len(pilot)
     n = int(max(1, min(T, budget_s / max(per_tok, 1e-9))))
-    stride = max(1, T // n)
-    tokens = np.arange(0, T, stride)[:n]
+    tokens = np.unique(np.linspace(0, T - 1, n).round().astype(np.int64))   # spread over the whole batch
     dt = run(tokens)
-    desc = (f"{len(tokens)} of {T} query tokens (every {stride}th, all {Hq} heads) of {batch.name}; "
+    desc = (f"{len(tokens)} of {T} query tokens (evenly spaced, all {Hq} heads) of {batch.name}; "
             f"fp64 C oracle")
     return len(tokens) / dt, dt, len(tokens), oracle.num_threads(), desc
 
@@ -386,24 +385,31 @@ def measure_workload(B: Bench, name: str, headline: bool, rank: int, world: int)
     swapped = torch.cuda.Event()
 
     # The swap-out moves cached history that this step's append does not
-    # write, so it starts with the step, beside the append.
-    def step(di=d, meta_=meta, o=out, l_=lse):
+    # write, so it starts with the step, beside the append.  fused: one
+    # pkv_append_paged_attn call instead of pkv_append + pkv_paged_attn.
+    def step(di=d, meta_=meta, o=out, l_=lse, fused=False):
         begun.record(main)
         side.wait_event(begun)
         pkv.pkv_swap_out(pool, swap_ids, swap_host, stream=side)
         swapped.record(side)
-        pkv.pkv_append(pool, di["block_tables"], di["cu_q_lens"], di["q_positions"], di["k_new"], di["v_new"])
-        pkv.pkv_paged_attn(pool, di["q"], di["q_positions"], di["block_tables"], di["ctx_lens"], di["cu_q_lens"],
-                           meta_, batch.scale, out=o, lse=l_, workspace=ws)
+        if fused:
+            pkv.pkv_append_paged_attn(pool, di["q"], di["q_positions"], di["block_tables"], di["ctx_lens"],
+                                      di["cu_q_lens"], meta_, di["k_new"], di["v_new"], batch.scale, out=o, lse=l_,
+                                      workspace=ws)
+        else:
+            pkv.pkv_append(pool, di["block_tables"], di["cu_q_lens"], di["q_positions"], di["k_new"], di["v_new"])
+            pkv.pkv_paged_attn(pool, di["q"], di["q_positions"], di["block_tables"], di["ctx_lens"],
+                               di["cu_q_lens"], meta_, batch.scale, out=o, lse=l_, workspace=ws)
         main.wait_event(swapped)
 
     for _ in range(max(3, args.warmup)):
         step()
+        step(fused=True)
     torch.cuda.synchronize()
     if pkv.pkv_check_device_errors(pool) != 0:
         raise RuntimeError(f"{name}: device error word set during warm-up")
 
-    def timed_steps(n, mode):
+    def timed_steps(n, mode, fused=False):
         """n device-timed steps, L2 flushed between them; returns (per-step ms, kernel profile)."""
         pkv.pkv_profile_read(pool, reset=True)
         pkv.pkv_profile_enable(pool, mode)
@@ -414,7 +420,7 @@ def measure_workload(B: Bench, name: str, headline: bool, rank: int, world: int)
         for i in range(n):
             B.l2_flush()
             starts[i].record(main)
-            step()
+            step(fused=fused)
             ends[i].record(main)
         torch.cuda.synchronize()
         barrier()
@@ -436,6 +442,9 @@ def measure_workload(B: Bench, name: str, headline: bool, rank: int, world: int)
     st = pkv.pkv_last_plan_stats(pool)
     # ---- per-kernel durations: the same steps with the two attention kernels one after the other
     ser_ms, ser_prof = timed_steps(max(10, args.steps // 2), 2)
+    # ---- the fused step: pkv_append_paged_attn in place of the two calls
+    fused_ms, fused_prof = timed_steps(args.steps, 1, fused=True)
+    f_tok, f_sec = aggregate_ranks(float(T * args.steps), sum(fused_ms) / 1e3)
 
     # Host planning time for this batch, uncached (the step reuses its cached
     # plan while the batch metadata is unchanged): median of 5 plans.
@@ -562,6 +571,9 @@ def measure_workload(B: Bench, name: str, headline: bool, rank: int, world: int)
                 "path": "pkv_copy_to_device / pkv_copy_to_host from pinned host memory, copy engines"},
         "e2e_replan": {"value": replan_value, "unit": UNIT, "plans_built": int(replans), "steps": e2e_steps,
                        "variants": REPLAN_VARIANTS},
+        "fused": {"value": f_tok / f_sec, "unit": UNIT, "ms_per_step": 1e3 * f_sec / args.steps,
+                  "kernels": {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(1, v["launches"])}
+                              for k, v in fused_prof.items()}},
         "clocks": clk.summary(),
         "wall_s_timed": wall1 - wall0,
         "swap_out_bytes_per_step": swap_bytes,
@@ -696,8 +708,9 @@ def run_ours(args):
         names = []
     else:
         names = [n for n in args.workloads.split(",") if n]
-    per = {args.workload: {k: head[k] for k in ("value", "ms_per_step", "e2e", "e2e_replan", "roofline_per_kernel",
-                                                "kernels_one_at_a_time", "plan", "kv_gbs", "tflops")}}
+    keys = ("value", "ms_per_step", "e2e", "e2e_replan", "fused", "roofline_per_kernel", "kernels_one_at_a_time",
+            "plan", "kv_gbs", "tflops")
+    per = {args.workload: {k: head[k] for k in keys}}
     from paged_kv_attention_25_gb300 import pkv
     for n in names:
         if n == args.workload:
@@ -710,8 +723,7 @@ def run_ours(args):
             per[n] = {"unsupported": str(e)}
             torch.cuda.empty_cache()
             continue
-        per[n] = {k: r[k] for k in ("value", "ms_per_step", "e2e", "e2e_replan", "roofline_per_kernel",
-                                    "kernels_one_at_a_time", "plan", "kv_gbs", "tflops")}
+        per[n] = {k: r[k] for k in keys}
         per[n]["config"] = r["config"]
         torch.cuda.empty_cache()
 
@@ -730,7 +742,7 @@ def run_ours(args):
         "ms_per_step_one_at_a_time": head["ms_per_step_one_at_a_time"],
         "plan": head["plan"], "gpu_launches": head["gpu_launches"],
         "roofline": head["roofline"], "roofline_per_kernel": head["roofline_per_kernel"],
-        "e2e": head["e2e"], "e2e_replan": head["e2e_replan"],
+        "e2e": head["e2e"], "e2e_replan": head["e2e_replan"], "fused": head["fused"],
         "swap": swap, "swap_in_pipeline": pipe, "swap_out_bytes_per_step": head["swap_out_bytes_per_step"],
         "clocks": head["clocks"], "wall_s_timed": head["wall_s_timed"],
         "per_workload": per,

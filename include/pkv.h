@@ -74,11 +74,12 @@ extern "C" {
  * finite 448), one scale per pool for K and one for V: the value of a code c
  * is e4m3(c) * k_scale (or v_scale).  pkv_append quantises each new bf16
  * element x to the code nearest (ties to even) to the fp32 quotient x / scale,
- * finite values beyond 448 saturating to +-448.  Such pools are served by the
- * CUDA-core split-KV kernel only: pkv_paged_attn takes batches whose every
- * request has at most 4 query rows per KV head (q_len * G <= 4, the decode
- * regime) and returns PKV_EUNSUPPORTED otherwise.  Q, O and the new K/V given
- * to pkv_append stay bf16. */
+ * finite values beyond 448 saturating to +-448.  Attention reads the codes
+ * (half the bytes of bf16): the split-KV kernel multiplies them with bf16 q
+ * in fp32; the tensor-core kernel widens each K/V tile to f16 in shared
+ * memory (exact) and runs its MMAs with f16 operands, Q converted from bf16
+ * to f16 (exact for |q| within f16's range, below 65504) and P rounded to
+ * f16.  Q, O and the new K/V given to pkv_append stay bf16. */
 #define PKV_DTYPE_FP8_E4M3 1
 
 /* Bits of the device error word (pkv_check_device_errors). */
@@ -219,6 +220,32 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
                    const int32_t* cu_q_lens, int num_reqs, int num_tokens,
                    const pkv_host_meta* host_meta, float scale, void* o, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Fused paged KV append and attention (Pensieve abstract: one generalised
+ * kernel over a unified batch whose new input tokens join the conversation's
+ * cache and attend to it).  The result is that of
+ *   pkv_append(pool, block_tables, max_blocks, num_reqs, cu_q_lens,
+ *              q_positions, k_new, v_new, num_tokens, stream);
+ *   pkv_paged_attn(pool, q, ...same arguments..., stream);
+ * bit for bit in the pool, and O / LSE within the same rounding, but the
+ * attention kernels take the step's own keys and values from k_new / v_new
+ * ([num_tokens][num_kv_heads][head_dim] bf16, device, 16-byte aligned)
+ * instead of reading them back from the pool, so nothing waits for the pool
+ * write: CTAs of the split-KV launch write the new rows into the pool beside
+ * the attention work (one launch fewer than the two calls).
+ *   - host_meta->q_positions is required (the plan records, per request, the
+ *     runs of consecutive new positions); PKV_EINVAL without it.
+ *   - Workspace: pkv_paged_attn_workspace_size for the same batch.
+ *   - The pool's slots of the new tokens are written during the call; no
+ *     other work may read them until the call is complete on `stream`.
+ * Errors: those of pkv_append and pkv_paged_attn.
+ */
+int pkv_append_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t* q_positions,
+                          const int32_t* block_tables, int max_blocks, const int32_t* ctx_lens,
+                          const int32_t* cu_q_lens, int num_reqs, int num_tokens, const pkv_host_meta* host_meta,
+                          const void* k_new, const void* v_new, float scale, void* o, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /*
  * Paged attention for callers that cannot allocate device memory (a process

@@ -2,6 +2,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -150,13 +151,22 @@ int timed_launch(pkv_pool* pool, int kernel, void* stream, F&& fn) {
   return rc;
 }
 
-int make_tmap(CUtensorMap* map, void* base, int num_blocks, int hkv, int head_dim) {
+int make_tmap(CUtensorMap* map, void* base, int num_blocks, int hkv, int head_dim, bool fp8) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled unavailable (driver too old?)");
   const cuuint64_t chunks = static_cast<cuuint64_t>(num_blocks) * hkv;   // (block, head) chunks of 16 x D
   if (chunks * kBlockSize >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "pool too large for 32-bit TMA coordinates");
   CUresult r;
-  if (head_dim == 128) {
+  if (fp8) {
+    // FP8 codes: one (block, head) chunk per copy, 16 rows x D bytes, landing
+    // unswizzled ([16 keys][D] bytes); the kernel widens them to f16.
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), chunks * kBlockSize};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(head_dim), static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t estr[2] = {1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (head_dim == 128) {
     // One (block, head) chunk per copy, 16 rows x 256 bytes, landing as
     // [8-row group][64-column half][8 rows][128 bytes]: the 4-D view
     // (column within a half, row within a group, half, group) with strides
@@ -199,6 +209,40 @@ int make_q_tmap(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled (q) failed: " + std::to_string(static_cast<int>(r)));
   *box_tokens = bt;
+  return PKV_OK;
+}
+
+// The fused call's new K (or V) rows [T][Hkv][D] (bf16) for the tensor-core
+// kernel: a box of up to 8 tokens of one head lands as one 8-key group of a
+// K/V stage ([half][8 rows][128 bytes], 128-byte swizzle, the pool boxes'
+// layout); tokens past T read zeros.
+int make_new_tmap(CUtensorMap* map, const void* base, int num_tokens, int hkv, int head_dim, int* box_tokens) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled unavailable (driver too old?)");
+  const cuuint32_t bt = static_cast<cuuint32_t>(std::min(8, num_tokens));
+  const cuuint64_t row = static_cast<cuuint64_t>(hkv) * head_dim * 2;   // bytes per token
+  CUresult r;
+  if (head_dim == 128) {
+    // (column within a 64-column half, head, token, half)
+    cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(num_tokens), 2};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(head_dim) * 2, row, 128};
+    cuuint32_t box[4] = {64, 1, bt, 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(num_tokens)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2, row};
+    cuuint32_t box[3] = {64, 1, bt};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS)
+    return fail(PKV_ECUDA, "cuTensorMapEncodeTiled (new rows) failed: " + std::to_string(static_cast<int>(r)));
+  *box_tokens = static_cast<int>(bt);
   return PKV_OK;
 }
 
@@ -305,12 +349,11 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
       cudaEventCreateWithFlags(&p->ws_free, cudaEventDisableTiming) != cudaSuccess)
     return cleanup(fail(PKV_ECUDA, "cudaEventCreate upload"));
 
-  // The tensor-core kernel's block maps (bf16 pools only: fp8 pools are read
-  // by the split-KV kernel alone).
-  if (!fp8) {
-    int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim);
+  // The tensor-core kernel's block maps.
+  {
+    int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim, fp8);
     if (rc) return cleanup(rc);
-    rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim);
+    rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim, fp8);
     if (rc) return cleanup(rc);
   }
   e = cudaDeviceSynchronize();
@@ -435,6 +478,15 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
     return fail(PKV_EINVAL, "NULL device pointer");
   if (!aligned16(c.q) || !aligned16(c.o)) return fail(PKV_EINVAL, "q and o must be 16-byte aligned");
   if (!(c.scale > 0.f)) return fail(PKV_EINVAL, "scale must be positive");
+  const bool fused = c.k_new != nullptr || c.v_new != nullptr;
+  if (fused) {
+    if (!c.k_new || !c.v_new) return fail(PKV_EINVAL, "k_new and v_new are both required");
+    if (!aligned16(c.k_new) || !aligned16(c.v_new)) return fail(PKV_EINVAL, "k_new / v_new must be 16-byte aligned");
+    if (!c.host_meta || !c.host_meta->q_positions)
+      return fail(PKV_EINVAL, "the fused call needs host copies of q_positions in host_meta");
+    if (static_cast<int64_t>(c.num_tokens) * pool->num_kv_heads * (pool->head_dim / 8) >= (1ll << 31))
+      return fail(PKV_EUNSUPPORTED, "too many new rows for one fused call");
+  }
   int rc = finish_swap_in(pool, c.stream);
   if (rc) return rc;
   std::lock_guard<std::mutex> lk(pool->mu);
@@ -443,8 +495,6 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   const char* err = "";
   if ((rc = check_ctx_fits(*c.host_meta, c.num_reqs, c.max_blocks, &err))) return fail(rc, err);
   const Plan& pl = pool->plan;
-  if (pool->elem_bytes == 1 && !pl.tc.empty())
-    return fail(PKV_EUNSUPPORTED, "fp8 pools take decode-regime batches only: every request needs q_len * G <= 4");
   if (c.static_scratch) {
     if (pl.total > c.workspace_bytes)
       return fail(PKV_EINVAL, "pkv_paged_attn_static: this batch needs " + std::to_string(pl.total) +
@@ -484,6 +534,9 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
       std::memcpy(host + pl.off_merge_dec, pl.merge_dec.data(), pl.merge_dec.size() * sizeof(MergeItem));
       std::memset(host + pl.off_merge_cnt, 0, pl.merge_dec.size() * sizeof(int32_t));
     }
+    if (!pl.runs.empty()) std::memcpy(host + pl.off_runs, pl.runs.data(), pl.runs.size() * sizeof(RunDesc));
+    if (!pl.run_off.empty())
+      std::memcpy(host + pl.off_run_off, pl.run_off.data(), pl.run_off.size() * sizeof(int32_t));
     PKV_CUDA(cudaMemcpyAsync(ws, host, meta_bytes, cudaMemcpyHostToDevice, pool->copy), "upload work list");
     if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], pool->copy), "staging slot record");
     PKV_CUDA(cudaEventRecord(pool->up_done, pool->copy), "upload record");
@@ -509,10 +562,33 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   a.q_box_tokens = 0;
   a.wait_ns = pool->wait_ns;
   a.withhold = pool->withhold;
-  CUtensorMap tmap_q;
+  a.k_new = fused ? c.k_new : nullptr;
+  a.v_new = fused ? c.v_new : nullptr;
+  a.cu_q_lens = c.cu_q_lens;
+  a.num_reqs = c.num_reqs;
+  a.num_tokens = c.num_tokens;
+  a.n_append_ctas = 0;
+  a.kn_box_tokens = 0;
+  a.runs = reinterpret_cast<const RunDesc*>(ws + pl.off_runs);
+  a.run_off = reinterpret_cast<const int32_t*>(ws + pl.off_run_off);
+  if (fused) {
+    // Append CTAs of the split-KV launch: about 8 chunks a thread.
+    const int64_t chunks = static_cast<int64_t>(c.num_tokens) * pool->num_kv_heads * (pool->head_dim / 8);
+    a.n_append_ctas = static_cast<int>(std::min<int64_t>(std::max<int64_t>(1, (chunks + 1023) / 1024),
+                                                         static_cast<int64_t>(pool->num_sms) * 8));
+  }
+  CUtensorMap tmap_q, tmap_kn, tmap_vn;
   if (!pl.tc.empty()) {
     rc = make_q_tmap(&tmap_q, c.q, c.num_tokens, c.num_q_heads, pool->head_dim, a.group, &a.q_box_tokens);
     if (rc) return rc;
+    if (fused) {
+      rc = make_new_tmap(&tmap_kn, c.k_new, c.num_tokens, pool->num_kv_heads, pool->head_dim, &a.kn_box_tokens);
+      if (!rc) rc = make_new_tmap(&tmap_vn, c.v_new, c.num_tokens, pool->num_kv_heads, pool->head_dim, &a.kn_box_tokens);
+      if (rc) return rc;
+    } else {
+      tmap_kn = pool->tmap_k;   // unused by a plain call; any valid map
+      tmap_vn = pool->tmap_v;
+    }
   }
 
   const WorkItem* d_dec = reinterpret_cast<const WorkItem*>(ws + pl.off_decode);
@@ -527,7 +603,10 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   // as or faster than the reverse on every mixed workload.  In the serialised
   // profiling mode both run on the caller's stream, one after the other, so
   // that each kernel's timing events bracket its own execution only.
-  const bool fork = !pl.tc.empty() && !pl.decode.empty() && pool->prof_mode != 2;
+  // A fused call always launches the split-KV kernel: its append CTAs write
+  // the new rows into the pool.
+  const bool dec_launch = !pl.decode.empty() || a.n_append_ctas > 0;
+  const bool fork = !pl.tc.empty() && dec_launch && pool->prof_mode != 2;
   void* dec_stream = c.stream;
   void* tc_stream = c.stream;
   if (fork) {
@@ -535,14 +614,15 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
     PKV_CUDA(cudaStreamWaitEvent(pool->side, pool->fork, 0), "fork wait");
     tc_stream = pool->side;
   }
-  if (!pl.decode.empty()) {
+  if (dec_launch) {
     rc = timed_launch(pool, 1, dec_stream,
                       [&] { return launch_decode(a, d_dec, static_cast<int>(pl.decode.size()), dec_stream); });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "split-KV attention launch");
   }
   if (!pl.tc.empty()) {
     rc = timed_launch(pool, 2, tc_stream, [&] {
-      return launch_tc(a, &pool->tmap_k, &pool->tmap_v, &tmap_q, d_tc, static_cast<int>(pl.tc.size()), tc_stream);
+      return launch_tc(a, &pool->tmap_k, &pool->tmap_v, &tmap_q, &tmap_kn, &tmap_vn, d_tc,
+                       static_cast<int>(pl.tc.size()), tc_stream);
     });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "tensor-core attention launch");
   }
@@ -584,6 +664,34 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
   c.workspace = workspace;
   c.workspace_bytes = workspace_bytes;
   c.stream = stream;
+  return paged_attn_call(pool, c);
+}
+
+int pkv_append_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t* q_positions,
+                          const int32_t* block_tables, int max_blocks, const int32_t* ctx_lens,
+                          const int32_t* cu_q_lens, int num_reqs, int num_tokens, const pkv_host_meta* host_meta,
+                          const void* k_new, const void* v_new, float scale, void* o, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  AttnCall c;
+  c.q = q;
+  c.num_q_heads = num_q_heads;
+  c.q_positions = q_positions;
+  c.block_tables = block_tables;
+  c.max_blocks = max_blocks;
+  c.ctx_lens = ctx_lens;
+  c.cu_q_lens = cu_q_lens;
+  c.num_reqs = num_reqs;
+  c.num_tokens = num_tokens;
+  c.host_meta = host_meta;
+  c.scale = scale;
+  c.o = o;
+  c.lse = lse;
+  c.workspace = workspace;
+  c.workspace_bytes = workspace_bytes;
+  c.stream = stream;
+  c.k_new = k_new;
+  c.v_new = v_new;
+  if (!k_new || !v_new) return fail(PKV_EINVAL, "k_new and v_new are both required");
   return paged_attn_call(pool, c);
 }
 

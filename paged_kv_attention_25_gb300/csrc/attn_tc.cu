@@ -35,6 +35,9 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <cuda_fp8.h>
+
+#include "append.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -64,7 +67,7 @@ struct TcSmem {
   static constexpr int kOffK = 2 * kQ;
   static constexpr int kOffV = kOffK + kKSt * kKV;
   static constexpr int kOffBar = kOffV + kVSt * kKV;
-  static constexpr int kNumBars = 3 * kKSt + 2 * kVSt + 7;
+  static constexpr int kNumBars = 4 * kKSt + 3 * kVSt + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kTotal = kOffMisc + 64;
 };
@@ -80,6 +83,11 @@ struct Bars {
   static constexpr int kP = kQ + 2;            // + tile: P written, O rescaled (128 arrivals)
   static constexpr int kPv = kQ + 4;           // + tile: the tile's last PV done
   static constexpr int kDrain = kQ + 6;        // every MMA issued has completed
+  // Fused call: a tile with blocks to patch lands on these (one per K and V
+  // stage) instead; the producer patches the new keys in, then arrives on full.
+  static constexpr int kKLanded = kQ + 7, kVLanded = kQ + 7 + KS;
+  // FP8 pools: + tile: the tile's Q rows converted to f16 (128 arrivals).
+  static constexpr int kQc = kQ + 7 + KS + VS;
 };
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -102,10 +110,64 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
       : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
 }
 
+// Two e4m3 codes (low byte first) -> two f16 (low half first): exact, since
+// every e4m3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Writes 16 consecutive f16 values (two 16-byte chunks) of key r, starting at
+// element 16 * cc, into a K/V stage in the MMA operand layout:
+// [8-key group][64-column half][8 keys][128 bytes], 16-byte chunk c of a
+// key's 128-byte line at c ^ (key % 8) (128-byte swizzle).
 template <int D>
+__device__ __forceinline__ void store_f16x16(uint8_t* stage, int r, int cc, uint4 lo, uint4 hi) {
+  using S = TcSmem<D>;
+  const int c0 = 2 * cc, hf = c0 / 8, cw = c0 % 8, r8 = r % 8;
+  uint8_t* line = stage + (r / 8) * S::kGS + hf * S::kHS + r8 * 128;
+  *reinterpret_cast<uint4*>(line + ((cw ^ r8) * 16)) = lo;
+  *reinterpret_cast<uint4*>(line + (((cw + 1) ^ r8) * 16)) = hi;
+}
+
+// FP8 pools: a stage holds the tile's e4m3 codes, [128 keys][D] bytes, in its
+// upper half (as the TMA landed them); widen them in place to the f16
+// operand layout of the whole stage.  Keys 64..127 are read into registers
+// first, because their f16 rows overwrite the codes; keys 0..63 are widened
+// straight from shared memory (their rows fill the lower half).  One warp.
+template <int D>
+__device__ __forceinline__ void widen_stage(uint8_t* stage, int lane) {
+  using S = TcSmem<D>;
+  constexpr int kCpr = D / 16;              // 16-code chunks per key
+  constexpr int kHalfChunks = 64 * kCpr;    // chunks of keys 0..63
+  constexpr int kPer = kHalfChunks / 32;    // chunks of each half per lane
+  const uint8_t* codes = stage + S::kKV / 2;
+  auto widen = [&](int q, uint4 v) {
+    uint4 lo, hi;
+    lo.x = e4m3x2_to_f16x2(v.x); lo.y = e4m3x2_to_f16x2(v.x >> 16);
+    lo.z = e4m3x2_to_f16x2(v.y); lo.w = e4m3x2_to_f16x2(v.y >> 16);
+    hi.x = e4m3x2_to_f16x2(v.z); hi.y = e4m3x2_to_f16x2(v.z >> 16);
+    hi.z = e4m3x2_to_f16x2(v.w); hi.w = e4m3x2_to_f16x2(v.w >> 16);
+    store_f16x16<D>(stage, q / kCpr, q % kCpr, lo, hi);
+  };
+  uint4 hold[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) hold[i] = *reinterpret_cast<const uint4*>(codes + (kHalfChunks + i * 32 + lane) * 16);
+#pragma unroll 4
+  for (int i = 0; i < kPer; ++i) {
+    const int q = i * 32 + lane;
+    widen(q, *reinterpret_cast<const uint4*>(codes + q * 16));
+  }
+  __syncwarp();   // every lane has read the codes the rows below overwrite
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) widen(kHalfChunks + i * 32 + lane, hold[i]);
+}
+
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-               const __grid_constant__ CUtensorMap tmap_q, const WorkItem* __restrict__ items) {
+               const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kn,
+               const __grid_constant__ CUtensorMap tmap_vn, const WorkItem* __restrict__ items) {
   using S = TcSmem<D>;
   constexpr int kKSt = S::kKSt, kVSt = S::kVSt;
   using B = Bars<kKSt, kVSt>;
@@ -137,24 +199,32 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       mbar_init(&bars[B::kKFull + i], 1);
       mbar_init(&bars[B::kS + i], 1);
       mbar_init(&bars[B::kS + kKSt + i], 1);
+      mbar_init(&bars[B::kKLanded + i], 1);
     }
     for (int i = 0; i < kVSt; ++i) {
       mbar_init(&bars[B::kVFull + i], 1);
       mbar_init(&bars[B::kVEmpty + i], 1);
+      mbar_init(&bars[B::kVLanded + i], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[B::kQ + t], 1);
       mbar_init(&bars[B::kP + t], 128);
       mbar_init(&bars[B::kPv + t], 1);
+      mbar_init(&bars[B::kQc + t], 128);
     }
     mbar_init(&bars[B::kDrain], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
   if (warp == 9 && lane == 0) prefetch_tmap(&tmap_q);
+  const bool fused = a.k_new != nullptr;
   if (warp == 8 && lane == 0) {
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
+    if (fused) {
+      prefetch_tmap(&tmap_kn);
+      prefetch_tmap(&tmap_vn);
+    }
   }
   if (warp == 9) {
     tmem_alloc(s_tmem, kTmemCols);
@@ -193,9 +263,14 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     return pb;
   };
   int ids_cur = -1, ids_next = -1;
+  int run_b = 0, run_e = 0;   // fused call: the request's runs of new positions
   if (warp == 8 || warp == 10) {
     ids_cur = load_window(0);
     ids_next = load_window(1);
+    if (fused) {
+      run_b = __ldg(a.run_off + it.req);
+      run_e = __ldg(a.run_off + it.req + 1);
+    }
   }
   int qpos = -1;
   if (warp < 8 && row < rows[X]) qpos = __ldg(a.q_positions + tok0[X] + row / G);
@@ -229,13 +304,78 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       if (lane >= nblk) pb = -1;
       return pb < 0 ? -1 : pb * Hkv + g;
     };
+    // Fused call: the tokens of this step are not in the pool yet (the
+    // launch beside this one writes them), so their keys and values come from
+    // the new rows.  Run r says positions [p0, p0 + n) are tokens [t0, t0 + n).
+    auto run_at = [&](int r) {
+      const int4 v = __ldg(reinterpret_cast<const int4*>(a.runs) + r);
+      return RunDesc{v.x, v.y, v.z, v.w};
+    };
+    // Overwrites, in a landed stage, every slot of block `blk` (first key bp)
+    // that holds a new key below kv_end with that token's row (swizzled as
+    // the TMA lands it: 16-byte chunk c of row r at chunk c ^ (r % 8) of its
+    // 128-byte line).
+    auto patch_block = [&](uint8_t* blk, int bp, bool is_k) {
+      int tok = -1;
+      const int p = bp + (lane & 15);
+      if (p < kv_end) {
+        for (int r = run_b; r < run_e; ++r) {
+          const RunDesc rd = run_at(r);
+          if (rd.p0 > p) break;
+          if (p < rd.p0 + rd.n) {
+            tok = rd.t0 + (p - rd.p0);
+            break;
+          }
+        }
+      }
+      const uint8_t* src = static_cast<const uint8_t*>(is_k ? a.k_new : a.v_new);
+      constexpr int kCpr = D / 8;   // 16-byte chunks per row
+#pragma unroll
+      for (int idx = lane; idx < kBlockSize * kCpr; idx += 32) {
+        const int rr = idx / kCpr, c = idx % kCpr;
+        const int t = __shfl_sync(0xffffffffu, tok, rr);
+        if (t >= 0) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + ((static_cast<int64_t>(t) * Hkv + g) * D) * 2 + c * 16);
+          *reinterpret_cast<uint4*>(blk + (rr / 8) * S::kGS + (c / 8) * S::kHS + (rr % 8) * 128 +
+                                    (((c % 8) ^ (rr % 8)) * 16)) = v;
+        }
+      }
+    };
+    uint32_t landed_par = 0;   // bit st: parity of this warp's next wait on landed barrier st
     auto load = [&](int j, int y, bool is_k) -> bool {
       const int nst = is_k ? kKSt : kVSt;
       const int st = j % nst;
       const uint32_t ph = (j / nst) & 1;
       uint64_t* full = &bars[(is_k ? B::kKFull : B::kVFull) + st];
-      const int nvalid = __popc(__ballot_sync(0xffffffffu, y >= 0));
-      const uint32_t bytes = static_cast<uint32_t>(nvalid) * S::kHalves * (kBlockSize * 128);
+      // Where lane l's block (keys bp .. bp + 15) comes from: 1 the pool; 2
+      // the new rows, tokens src .. src + 15 (every key below kv_end belongs
+      // to one run); 3 the pool, then its new keys patched in; 0 nothing.
+      int cls = y >= 0 ? 1 : 0, src = -1;
+      if (fused) {
+        const int bp = it.kv_start + j * kNK + lane * kBlockSize;
+        if (lane < kBlk && bp < kv_end) {
+          const int live = min(bp + kBlockSize, kv_end);
+          int nnew = 0, nrun = 0;
+          for (int r = run_b; r < run_e; ++r) {
+            const RunDesc rd = run_at(r);
+            if (rd.p0 >= live) break;
+            const int lo = max(bp, rd.p0), hi = min(live, rd.p0 + rd.n);
+            if (lo < hi) {
+              nnew += hi - lo;
+              if (nrun++ == 0) src = rd.t0 + (bp - rd.p0);
+            }
+          }
+          if (nnew == live - bp && nrun == 1) cls = 2;
+          else if (nnew > 0 && y >= 0) cls = 3;
+        }
+      }
+      const bool patch = __any_sync(0xffffffffu, cls == 3);
+      // A pool box is a whole block; a box of new rows holds kn_box_tokens
+      // tokens (8, fewer only when the batch has fewer tokens).
+      const uint32_t my_bytes = cls == 2   ? 2u * a.kn_box_tokens * S::kHalves * 128u
+                                : cls != 0 ? static_cast<uint32_t>(S::kHalves * kBlockSize * 128)
+                                           : 0u;
+      const uint32_t bytes = __reduce_add_sync(0xffffffffu, my_bytes);
       // Free stage: V after the release that follows its tile's PVs; K after
       // the S commit of the tile that last read it (j - nst), i.e. tile B's
       // where B reaches that key tile, else tile A's.  Before a stage's first
@@ -245,38 +385,172 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       // Test hook: CTA 0 never issues its first K tile, so that the issuer's
       // bounded wait for it runs out.
       if (a.withhold == 2 && is_k && j == 0 && blockIdx.x == 0) return true;
-      if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+      uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
+      uint64_t* bar = patch ? landed : full;
+      if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
       __syncwarp();
-      if (y >= 0) {
-        uint8_t* dst = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + lane * S::kBlkBytes;
+      uint8_t* dst = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + lane * S::kBlkBytes;
+      if (cls == 2) {
+        // Two 8-token boxes of the new rows, one per 8-key group of the block.
+        const CUtensorMap* m = is_k ? &tmap_kn : &tmap_vn;
+        if constexpr (D == 128) {
+          tma_load_4d(dst, m, 0, g, src, 0, bar);
+          tma_load_4d(dst + S::kGS, m, 0, g, src + 8, 0, bar);
+        } else {
+          tma_load_3d(dst, m, 0, g, src, bar);
+          tma_load_3d(dst + S::kGS, m, 0, g, src + 8, bar);
+        }
+      } else if (cls != 0) {
         if constexpr (D == 128)
-          tma_load_4d(dst, is_k ? &tmap_k : &tmap_v, 0, 0, 0, 2 * y, full);
+          tma_load_4d(dst, is_k ? &tmap_k : &tmap_v, 0, 0, 0, 2 * y, bar);
         else
-          tma_load_2d(dst, is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, full);
+          tma_load_2d(dst, is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, bar);
+      }
+      if (patch) {
+        const uint32_t par = (landed_par >> st) & 1u;
+        landed_par ^= 1u << st;
+        if (!mbar_wait_warp(landed, par, s_abort, a.wait_ns)) {
+          (void)mbar_wait(landed, par, nullptr, a.wait_ns);   // let this tile's copies land
+          return false;
+        }
+        uint8_t* stage = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV;
+        uint32_t mm = __ballot_sync(0xffffffffu, cls == 3);
+        while (mm) {
+          const int b = __ffs(mm) - 1;
+          mm &= mm - 1;
+          patch_block(stage + b * S::kBlkBytes, it.kv_start + j * kNK + b * kBlockSize, is_k);
+        }
+        fence_proxy_async_smem();   // the patched slots are read by the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full);
       }
       return true;
     };
     // K and V stream from two warps, so that neither waits behind the
     // other's free stages: a K stage frees when its S MMAs finish, a V stage
     // only when both tiles' PV on it have finished.
+    // FP8 pools: tile j's codes land (on landed barrier j % nst) in the
+    // upper half of its stage; the warp widens the stage in place to f16,
+    // patches the fused call's new rows in (quantised as the append stores
+    // them) and arrives on full.  Copies run one tile ahead of the widening.
+    auto load_f8 = [&](int j, int y, bool is_k) -> bool {
+      const int nst = is_k ? kKSt : kVSt;
+      const int st = j % nst;
+      const uint32_t ph = (j / nst) & 1;
+      const uint32_t bytes = static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, y >= 0))) * (kBlockSize * D);
+      const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile[1] ? kKSt : 0) + st : B::kVEmpty + st;
+      if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
+      if (a.withhold == 2 && is_k && j == 0 && blockIdx.x == 0) return true;   // test hook (above)
+      uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
+      if (lane == 0) mbar_arrive_expect_tx(landed, bytes);
+      __syncwarp();
+      if (y >= 0)
+        tma_load_2d(smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + S::kKV / 2 + lane * (kBlockSize * D),
+                    is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, landed);
+      return true;
+    };
+    // The fused call's new rows of block b of a widened stage: each new key's
+    // row, quantised to codes (as the append stores it) and widened to f16.
+    auto patch_block_f8 = [&](uint8_t* stage, int b, int bp, bool is_k) {
+      int tok = -1;
+      const int p = bp + (lane & 15);
+      if (p < kv_end) {
+        for (int r = run_b; r < run_e; ++r) {
+          const RunDesc rd = run_at(r);
+          if (rd.p0 > p) break;
+          if (p < rd.p0 + rd.n) {
+            tok = rd.t0 + (p - rd.p0);
+            break;
+          }
+        }
+      }
+      const uint8_t* src = static_cast<const uint8_t*>(is_k ? a.k_new : a.v_new);
+      const float sc = is_k ? a.pool.k_scale : a.pool.v_scale;
+      constexpr int kC8 = D / 8;   // 8-element chunks per row
+#pragma unroll
+      for (int idx = lane; idx < kBlockSize * kC8; idx += 32) {
+        const int rr = idx / kC8, c = idx % kC8;
+        const int t = __shfl_sync(0xffffffffu, tok, rr);
+        if (t >= 0) {
+          const uint4 x = *reinterpret_cast<const uint4*>(src + ((static_cast<int64_t>(t) * Hkv + g) * D) * 2 + c * 16);
+          const uint32_t c0 = quant_e4m3x4(x.x, x.y, sc), c1 = quant_e4m3x4(x.z, x.w, sc);
+          const uint4 h = make_uint4(e4m3x2_to_f16x2(c0), e4m3x2_to_f16x2(c0 >> 16), e4m3x2_to_f16x2(c1),
+                                     e4m3x2_to_f16x2(c1 >> 16));
+          const int r = b * kBlockSize + rr, hf = c / 8, cw = c % 8, r8 = r % 8;
+          *reinterpret_cast<uint4*>(stage + (r / 8) * S::kGS + hf * S::kHS + r8 * 128 + ((cw ^ r8) * 16)) = h;
+        }
+      }
+    };
+    auto finish_f8 = [&](int j, bool is_k) -> bool {
+      const int nst = is_k ? kKSt : kVSt;
+      const int st = j % nst;
+      uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
+      if (!mbar_wait_warp(landed, (j / nst) & 1, s_abort, a.wait_ns)) return false;
+      uint8_t* stage = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV;
+      widen_stage<D>(stage, lane);
+      if (fused) {
+        __syncwarp();
+        const int key0 = it.kv_start + j * kNK;
+        const int bp = key0 + lane * kBlockSize;
+        bool has_new = false;
+        if (lane < kBlk && bp < kv_end) {
+          const int live = min(bp + kBlockSize, kv_end);
+          for (int r = run_b; r < run_e; ++r) {
+            const RunDesc rd = run_at(r);
+            if (rd.p0 >= live) break;
+            if (max(bp, rd.p0) < min(live, rd.p0 + rd.n)) has_new = true;
+          }
+        }
+        uint32_t mm = __ballot_sync(0xffffffffu, has_new);
+        while (mm) {
+          const int b = __ffs(mm) - 1;
+          mm &= mm - 1;
+          patch_block_f8(stage, b, key0 + b * kBlockSize, is_k);
+        }
+      }
+      fence_proxy_async_smem();   // the widened rows are read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[(is_k ? B::kKFull : B::kVFull) + st]);
+      return true;
+    };
     const bool is_k = warp == 8;
     const int nst = is_k ? kKSt : kVSt;
     bool ok = true;
     int nl = 0;   // tiles whose copies this warp has issued
-    for (int j = 0; j < ntiles; ++j) {
-      if (!(ok = load(j, block_chunk(j), is_k))) break;
-      nl = j + 1;
-    }
-    if (!ok) {   // gave up: flag it and let copies already issued land
-      if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
-      *s_abort = 1;
-      for (int i = max(0, nl - nst); i < nl; ++i)
-        (void)mbar_wait(&bars[(is_k ? B::kKFull : B::kVFull) + i % nst], (i / nst) & 1, nullptr, a.wait_ns);
+    if constexpr (F8) {
+      int nf = 0;   // tiles widened and handed to the issuer
+      for (int j = 0; j < ntiles; ++j) {
+        if (!(ok = load_f8(j, block_chunk(j), is_k))) break;
+        nl = j + 1;
+        if (j >= 1) {
+          if (!(ok = finish_f8(j - 1, is_k))) break;
+          nf = j;
+        }
+      }
+      if (ok && ntiles > 0 && (ok = finish_f8(ntiles - 1, is_k))) nf = ntiles;
+      if (!ok) {   // gave up: flag it and let copies already issued land
+        if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
+        *s_abort = 1;
+        for (int i = nf; i < nl; ++i)
+          (void)mbar_wait(&bars[(is_k ? B::kKLanded : B::kVLanded) + i % nst], (i / nst) & 1, nullptr, a.wait_ns);
+      }
+    } else {
+      for (int j = 0; j < ntiles; ++j) {
+        if (!(ok = load(j, block_chunk(j), is_k))) break;
+        nl = j + 1;
+      }
+      if (!ok) {   // gave up: flag it and let copies already issued land
+        if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
+        *s_abort = 1;
+        for (int i = max(0, nl - nst); i < nl; ++i)
+          (void)mbar_wait(&bars[(is_k ? B::kKFull : B::kVFull) + i % nst], (i / nst) & 1, nullptr, a.wait_ns);
+      }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc_s = make_idesc_bf16(128, kNK, false);
-    constexpr uint32_t idesc_o = make_idesc_bf16(128, D, true);
+    // FP8 pools: Q, the widened K / V and P are all f16.
+    constexpr uint32_t idesc_s = F8 ? make_idesc_f16(128, kNK, false) : make_idesc_bf16(128, kNK, false);
+    constexpr uint32_t idesc_o = F8 ? make_idesc_f16(128, D, true) : make_idesc_bf16(128, D, true);
     // Descriptors are built once; each MMA only advances the start-address
     // field (bits 0-13, in 16-byte units) by a constant offset.
     // K: K-major, 8-key groups kGS apart; V: MN-major, 64-dim halves kHS
@@ -303,7 +577,10 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       }
     }
     __syncwarp();
-    bool ok = mbar_wait_warp(&bars[B::kQ], 0, s_abort, a.wait_ns) && mbar_wait_warp(&bars[B::kQ + 1], 0, s_abort, a.wait_ns);
+    // FP8 pools: wait for the softmax warps' f16 conversion of the tiles instead.
+    constexpr int kQReady = F8 ? B::kQc : B::kQ;
+    bool ok = mbar_wait_warp(&bars[kQReady], 0, s_abort, a.wait_ns) &&
+              mbar_wait_warp(&bars[kQReady + 1], 0, s_abort, a.wait_ns);
     const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
     // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage).
     auto issue_s = [&](int t, int j) {
@@ -398,10 +675,36 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     const uint32_t colS = X * kNK, colO = kColO + X * 128;
     const int nrows = rows[X];
     const int nt = ntile[X];
-    const float sl2 = a.scale_log2;
+    // FP8 pools: S holds q . code, so k_scale joins the score scale (and
+    // v_scale the final 1/l).
+    const float sl2 = F8 ? a.scale_log2 * a.pool.k_scale : a.scale_log2;
     float m = -CUDART_INF_F, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
+    if constexpr (F8) {
+      // The widened K and V are f16, and both operands of an MMA share one
+      // type: convert this thread's Q row of its tile to f16 in place once the
+      // tile has landed (exact within f16's range).
+      ok = mbar_wait_warp(&bars[B::kQ + X], 0, s_abort, a.wait_ns);
+      if (ok) {
+        uint8_t* qrow = smem + S::kOffQ + X * S::kQ + row * 128;
+#pragma unroll
+        for (int hf = 0; hf < S::kHalves; ++hf) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4* q16 = reinterpret_cast<uint4*>(qrow + hf * (kTcRows * 128) + c * 16);
+            uint4 v = *q16;
+            v.x = pack_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x));
+            v.y = pack_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
+            v.z = pack_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z));
+            v.w = pack_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w));
+            *q16 = v;
+          }
+        }
+        fence_proxy_async_smem();   // read by the tensor cores
+      }
+      mbar_arrive(&bars[B::kQc + X]);
+    }
+    for (int j = 0; ok && j < nt; ++j) {
       const int key0 = it.kv_start + j * kNK;
       if (!mbar_wait_warp(&bars[B::kS + X * kKSt + j % kKSt], (j / kKSt) & 1, s_abort, a.wait_ns)) { ok = false; break; }
       tc_fence_after();
@@ -444,7 +747,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           fma2(x0, x1, sl2, neg_m);
           const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           add2(rs0[(c >> 1) & 3], rs1[(c >> 1) & 3], p0, p1);
-          pk[(c - cc) / 2] = pack_bf16x2(p0, p1);
+          pk[(c - cc) / 2] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
         tmem_st16(tmem + lane_base + colS + cc / 2, reinterpret_cast<const float*>(pk));
       }
@@ -483,7 +786,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     if (ok) {
       constexpr float kLn2 = 0.69314718055994530942f;
       const bool valid = row < nrows;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (F8 ? a.pool.v_scale : 1.f) / l : 0.f;
       const float lse = l > 0.f ? (m + fast_log2(l)) * kLn2 : -CUDART_INF_F;
       const int t = tok0[X] + (valid ? row / G : 0);
       const int h = g * G + row % G;
@@ -548,24 +851,32 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
 
 }  // namespace
 
-template <int D>
+template <int D, bool F8>
 static int launch_tc_d(const AttnArgs& a, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
-                       const WorkItem* items, int n_items, void* stream) {
+                       const CUtensorMap* tkn, const CUtensorMap* tvn, const WorkItem* items, int n_items,
+                       void* stream) {
   const int smem = TcSmem<D>::kTotal;
-  cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tc_attn_kernel<D><<<n_items, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, *tk, *tv, *tq, items);
+  tc_attn_kernel<D, F8><<<n_items, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, *tk, *tv, *tq, *tkn,
+                                                                                        *tvn, items);
   return cudaGetLastError();
 }
 
-int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const void* tmap_q, const WorkItem* items,
-              int n_items, void* stream) {
+int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const void* tmap_q, const void* tmap_kn,
+              const void* tmap_vn, const WorkItem* items, int n_items, void* stream) {
   if (n_items <= 0) return cudaSuccess;
   const CUtensorMap* tk = static_cast<const CUtensorMap*>(tmap_k);
   const CUtensorMap* tv = static_cast<const CUtensorMap*>(tmap_v);
   const CUtensorMap* tq = static_cast<const CUtensorMap*>(tmap_q);
-  if (a.pool.head_dim == 128) return launch_tc_d<128>(a, tk, tv, tq, items, n_items, stream);
-  return launch_tc_d<64>(a, tk, tv, tq, items, n_items, stream);
+  const CUtensorMap* tkn = static_cast<const CUtensorMap*>(tmap_kn);
+  const CUtensorMap* tvn = static_cast<const CUtensorMap*>(tmap_vn);
+  const bool f8 = a.pool.elem_bytes == 1;
+  if (a.pool.head_dim == 128)
+    return f8 ? launch_tc_d<128, true>(a, tk, tv, tq, tkn, tvn, items, n_items, stream)
+              : launch_tc_d<128, false>(a, tk, tv, tq, tkn, tvn, items, n_items, stream);
+  return f8 ? launch_tc_d<64, true>(a, tk, tv, tq, tkn, tvn, items, n_items, stream)
+            : launch_tc_d<64, false>(a, tk, tv, tq, tkn, tvn, items, n_items, stream);
 }
 
 }  // namespace pkv

@@ -27,6 +27,7 @@
 
 #include <type_traits>
 
+#include "append.cuh"
 #include "internal.h"
 #include "merge.cuh"
 #include "ptx.cuh"
@@ -172,6 +173,12 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     return pb;
   };
   int ids_cur = load_ids(0), ids_next = load_ids(32), win = 0;
+  // Fused call: positions of the item's tokens (the request's new tokens),
+  // whose keys and values come from the new rows rather than the pool.
+  const bool fused = a.k_new != nullptr;
+  int tpos[kDecodeMaxRows];
+#pragma unroll
+  for (int k = 0; k < kDecodeMaxRows; ++k) tpos[k] = fused && k < it.q_count ? __ldg(a.q_positions + it.q_start + k) : -1;
   __syncthreads();   // barrier initialisation visible (the id loads above are already in flight)
 
   auto issue = [&](int j) {
@@ -223,11 +230,50 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
       aborted = true;
       break;
     }
-    const uint8_t* kb = my_ring + st * S::kStage;
-    const uint8_t* vb = kb + S::kChunk;
+    uint8_t* kb = my_ring + st * S::kStage;
+    uint8_t* vb = kb + S::kChunk;
     const int key0 = (blk0 + warp + kWarps * i) * kBlockSize;
     constexpr int kRowBytes = D * (F8 ? 1 : 2);
     constexpr int kLaneBytes = kDPL * (F8 ? 1 : 2);
+    if (fused) {
+      // The block's slots of this step's tokens may not be written yet (the
+      // launch's append CTAs write them): take those rows from the new K/V,
+      // quantised as the append stores them.  Each lane rewrites its own
+      // slice of the row, the slice it reads below.
+#pragma unroll
+      for (int k = 0; k < kDecodeMaxRows; ++k) {
+        const int rr = tpos[k] - key0;
+        if (rr >= 0 && rr < kBlockSize) {
+          const int64_t src = (static_cast<int64_t>(it.q_start + k) * Hkv + g) * D + lane * kDPL;   // elements
+          const uint16_t* kn = static_cast<const uint16_t*>(a.k_new) + src;
+          const uint16_t* vn = static_cast<const uint16_t*>(a.v_new) + src;
+          uint8_t* kd = kb + rr * kRowBytes + lane * kLaneBytes;
+          uint8_t* vd = vb + rr * kRowBytes + lane * kLaneBytes;
+          if constexpr (F8) {
+            if constexpr (kDPL == 4) {
+              const uint2 kx = *reinterpret_cast<const uint2*>(kn), vx = *reinterpret_cast<const uint2*>(vn);
+              *reinterpret_cast<uint32_t*>(kd) = quant_e4m3x4(kx.x, kx.y, a.pool.k_scale);
+              *reinterpret_cast<uint32_t*>(vd) = quant_e4m3x4(vx.x, vx.y, a.pool.v_scale);
+            } else {
+              *reinterpret_cast<uint16_t*>(kd) =
+                  static_cast<uint16_t>(quant_e4m3x2(*reinterpret_cast<const uint32_t*>(kn), a.pool.k_scale));
+              *reinterpret_cast<uint16_t*>(vd) =
+                  static_cast<uint16_t>(quant_e4m3x2(*reinterpret_cast<const uint32_t*>(vn), a.pool.v_scale));
+            }
+          } else {
+            if constexpr (kDPL == 4) {
+              *reinterpret_cast<uint2*>(kd) = *reinterpret_cast<const uint2*>(kn);
+              *reinterpret_cast<uint2*>(vd) = *reinterpret_cast<const uint2*>(vn);
+            } else {
+              *reinterpret_cast<uint32_t*>(kd) = *reinterpret_cast<const uint32_t*>(kn);
+              *reinterpret_cast<uint32_t*>(vd) = *reinterpret_cast<const uint32_t*>(vn);
+            }
+          }
+          // These generic writes precede the next bulk copy into the stage.
+          fence_proxy_async_smem();
+        }
+      }
+    }
 
     // q . k for 16 keys, this lane's dims.
     float part[R][kBlockSize];
@@ -383,9 +429,30 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
   }
 }
 
+// The fused call's append CTAs (after the work items in the grid): CTA c of n
+// writes chunks c*128 + tid, stepping by n*128, of the batch's new K/V rows
+// into the pool.  The attention items of the launch never read those slots
+// from the pool (they take the rows from the new K/V), so nothing orders the
+// two inside the launch.
+template <bool F8>
+__device__ __forceinline__ void append_role(const AttnArgs& a, int c, int n) {
+  const int cpr_log2 = a.pool.head_dim == 128 ? 4 : 3;
+  const uint32_t total = static_cast<uint32_t>(a.num_tokens) * a.pool.num_kv_heads << cpr_log2;
+  for (uint32_t i = static_cast<uint32_t>(c) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<uint32_t>(n) * blockDim.x)
+    append_chunk<uint32_t, F8>(i, const_cast<void*>(a.pool.k), const_cast<void*>(a.pool.v), a.pool.num_blocks,
+                               a.pool.num_kv_heads, cpr_log2, a.block_tables, a.max_blocks, a.num_reqs, a.cu_q_lens,
+                               a.q_positions, static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new),
+                               a.pool.err, a.pool.k_scale, a.pool.v_scale);
+}
+
 template <int D, bool F8>
 __global__ void __launch_bounds__(kWarps * 32, 3)
-decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
+decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items, int n_items) {
+  if (static_cast<int>(blockIdx.x) >= n_items) {
+    append_role<F8>(a, blockIdx.x - n_items, gridDim.x - n_items);
+    return;
+  }
   using S = DecodeSmem<D, F8>;
   constexpr int kStages = S::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -485,12 +552,13 @@ static int launch_decode_d(const AttnArgs& a, const WorkItem* items, int n_items
   const int smem = DecodeSmem<D, F8>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, F8><<<n_items, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(a, items);
+  decode_kernel<D, F8><<<n_items + a.n_append_ctas, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(
+      a, items, n_items);
   return cudaGetLastError();
 }
 
 int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream) {
-  if (n_items <= 0) return cudaSuccess;
+  if (n_items + a.n_append_ctas <= 0) return cudaSuccess;
   const bool f8 = a.pool.elem_bytes == 1;
   if (a.pool.head_dim == 128)
     return f8 ? launch_decode_d<128, true>(a, items, n_items, stream) : launch_decode_d<128, false>(a, items, n_items, stream);

@@ -56,6 +56,16 @@ struct MergeItem {
 };
 static_assert(sizeof(MergeItem) == 32, "MergeItem layout");
 
+// A run of a request's query tokens with consecutive positions: positions
+// [p0, p0 + n) are tokens [t0, t0 + n).  The fused call's attention kernels
+// take these keys and values from the new rows instead of the pool.
+struct alignas(16) RunDesc {
+  int32_t p0;
+  int32_t t0;
+  int32_t n;
+  int32_t pad;
+};
+
 struct PlanParams {
   int num_q_heads;
   int num_kv_heads;
@@ -71,10 +81,15 @@ struct Plan {
   std::vector<WorkItem> tc;       // tensor-core kernel
   std::vector<MergeItem> merge;        // merged by the merge kernel (tensor-core groups)
   std::vector<MergeItem> merge_dec;    // merged inside the split-KV kernel
+  // Runs of new positions per request (host positions only), sorted by p0:
+  // request r's are runs[run_off[r] .. run_off[r + 1]).
+  std::vector<RunDesc> runs;
+  std::vector<int32_t> run_off;
   int num_partial_rows = 0;
   pkv_plan_stats stats{};
   // Workspace layout (byte offsets, 256-aligned sections).
-  size_t off_decode = 0, off_tc = 0, off_merge = 0, off_merge_dec = 0, off_merge_cnt = 0, off_part_o = 0, off_part_lse = 0, total = 0;
+  size_t off_decode = 0, off_tc = 0, off_merge = 0, off_merge_dec = 0, off_merge_cnt = 0, off_runs = 0, off_run_off = 0;
+  size_t off_part_o = 0, off_part_lse = 0, total = 0;
   bool valid = false;
   int64_t builds = 0;   // plans built into this object so far
   // Cache key: exact copies of the parameters and host metadata the plan was
@@ -144,6 +159,18 @@ struct AttnArgs {
   const MergeItem* merge_dec;   // merge items of split-KV groups (merged by their last split)
   int* merge_cnt;               // splits finished per such item (zeroed by the work-list upload)
   int q_box_tokens;             // tokens per query-tile copy of the tensor-core kernel's Q tensor map
+  // Fused append (pkv_append_paged_attn); k_new is nullptr in a plain call.
+  // The attention kernels read the new tokens' keys and values from k_new /
+  // v_new ([T][Hkv][D] bf16), never from the pool, and n_append_ctas extra
+  // CTAs of the split-KV launch write them into the pool.
+  const void* k_new;
+  const void* v_new;
+  const int32_t* cu_q_lens;     // device
+  int num_reqs, num_tokens;
+  int n_append_ctas;
+  int kn_box_tokens;            // tokens per box of the new-row tensor maps (min(8, T))
+  const RunDesc* runs;          // the plan's runs of new positions (device copy)
+  const int32_t* run_off;
   uint64_t wait_ns;             // wall-clock limit of every bounded wait in the kernels
   int withhold;                 // test hook: 1 / 2 = CTA 0 of the split-KV / tensor-core kernel
                                 // skips its first K copy, so that a bounded wait runs out
@@ -173,14 +200,19 @@ struct AttnCall {
   // `stream` after its kernels (so calls on any pools follow one another).
   bool static_scratch = false;
   void* scratch_free = nullptr;   // cudaEvent_t
+  // Fused append (pkv_append_paged_attn): the new rows [T][Hkv][D] bf16.
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
 };
 int paged_attn_call(pkv_pool* pool, const AttnCall& c);
 
 int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream);
 // tmap_q: Q viewed as [T][Hq][D] with a (64, G, q_box_tokens) box (128-byte
 // swizzle), built per call by make_q_tmap.
-int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const void* tmap_q, const WorkItem* items,
-              int n_items, void* stream);
+// tmap_kn / tmap_vn: the fused call's new K / V rows viewed as [T][Hkv][D] with
+// an 8-token box (make_new_tmap); any valid map when a.k_new is nullptr.
+int launch_tc(const AttnArgs& a, const void* tmap_k, const void* tmap_v, const void* tmap_q, const void* tmap_kn,
+              const void* tmap_vn, const WorkItem* items, int n_items, void* stream);
 int launch_merge(const AttnArgs& a, const MergeItem* items, int n_items, void* stream);
 
 }  // namespace pkv

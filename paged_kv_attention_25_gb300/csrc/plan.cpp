@@ -99,9 +99,12 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   plan->tc.clear();
   plan->merge.clear();
   plan->merge_dec.clear();
+  plan->runs.clear();
+  plan->run_off.clear();
   plan->num_partial_rows = 0;
   plan->stats = pkv_plan_stats{};
   plan->off_decode = plan->off_tc = plan->off_merge = plan->off_merge_dec = plan->off_merge_cnt = 0;
+  plan->off_runs = plan->off_run_off = 0;
   plan->off_part_o = plan->off_part_lse = plan->total = 0;
   plan->valid = false;
   const int R = pp.num_reqs, T = pp.num_tokens, Hq = pp.num_q_heads, Hkv = pp.num_kv_heads, D = pp.head_dim;
@@ -354,7 +357,27 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   st.tc_io_bytes = io_bytes(tc_groups);
 
 
-  // 5. Workspace layout.
+  // 5. Runs of consecutive positions per request, sorted by first position
+  // (the fused call's kernels look up which keys are new tokens).
+  if (pos) {
+    plan->run_off.resize(static_cast<size_t>(R) + 1);
+    for (int r = 0; r < R; ++r) {
+      plan->run_off[r] = static_cast<int32_t>(plan->runs.size());
+      const size_t first = plan->runs.size();
+      for (int t = cu[r]; t < cu[r + 1]; ++t) {
+        if (t > cu[r] && pos[t] == pos[t - 1] + 1) {
+          ++plan->runs.back().n;
+        } else {
+          plan->runs.push_back(RunDesc{pos[t], t, 1, 0});
+        }
+      }
+      std::sort(plan->runs.begin() + first, plan->runs.end(),
+                [](const RunDesc& x, const RunDesc& y) { return x.p0 < y.p0; });
+    }
+    plan->run_off[R] = static_cast<int32_t>(plan->runs.size());
+  }
+
+  // 6. Workspace layout.
   size_t off = 0;
   plan->off_decode = off;
   off = align256(off + plan->decode.size() * sizeof(WorkItem));
@@ -366,6 +389,10 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   off = align256(off + plan->merge_dec.size() * sizeof(MergeItem));
   plan->off_merge_cnt = off;   // counters, uploaded as zeros with the work lists
   off = align256(off + plan->merge_dec.size() * sizeof(int32_t));
+  plan->off_runs = off;
+  off = align256(off + plan->runs.size() * sizeof(RunDesc));
+  plan->off_run_off = off;
+  off = align256(off + plan->run_off.size() * sizeof(int32_t));
   plan->off_part_o = off;
   off = align256(off + size_t(part_rows) * D * sizeof(float));
   plan->off_part_lse = off;

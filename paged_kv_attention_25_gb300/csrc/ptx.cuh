@@ -204,6 +204,14 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_m
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// The same for f16 A/B (both operands f16: A and B of one kind::f16 MMA share a type).
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                   // D format: f32
+         | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness (A, B formats 0: f16)
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.  `saddr` is the shared
 // address of the (sub)matrix start; swizzle atoms must be 1024-byte aligned.
 //   K-major:  SBO = byte distance between 8-row groups; LBO unused (16).
@@ -226,6 +234,12 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) { return __uint_
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

@@ -40,7 +40,8 @@ KERNELS = ("append", "split_kv", "tensor_core", "merge", "swap")
 # Every symbol include/pkv.h declares (checked by the CPU test suite).
 EXPORTED = (
     "pkv_pool_create", "pkv_pool_destroy", "pkv_pool_kv_ptrs", "pkv_append",
-    "pkv_paged_attn_workspace_size", "pkv_paged_attn", "pkv_paged_attn_static", "pkv_last_plan_stats",
+    "pkv_paged_attn_workspace_size", "pkv_paged_attn", "pkv_append_paged_attn", "pkv_paged_attn_static",
+    "pkv_last_plan_stats",
     "pkv_plan_inspect", "pkv_swap_out", "pkv_swap_in", "pkv_swap_in_ahead", "pkv_swap_in_finish",
     "pkv_check_device_errors",
     "pkv_profile_enable", "pkv_profile_read", "pkv_device_sm_count", "pkv_last_error",
@@ -115,6 +116,8 @@ def load_library():
                                               ctypes.POINTER(ctypes.c_size_t)],
             "pkv_paged_attn": [P, P, I, P, P, I, P, P, I, I, ctypes.POINTER(pkv_host_meta), F, P, P, P,
                                ctypes.c_size_t, P],
+            "pkv_append_paged_attn": [P, P, I, P, P, I, P, P, I, I, ctypes.POINTER(pkv_host_meta), P, P, F, P, P, P,
+                                      ctypes.c_size_t, P],
             "pkv_paged_attn_static": [P, P, I, P, P, I, P, P, I, I, ctypes.POINTER(pkv_host_meta), F, P, P, P],
             "pkv_last_plan_stats": [P, ctypes.POINTER(pkv_plan_stats)],
             "pkv_plan_inspect": [I, I, I, I, I, I, ctypes.POINTER(pkv_host_meta), ctypes.POINTER(pkv_work_desc),
@@ -309,6 +312,36 @@ def pkv_paged_attn(pool: Pool, q, q_positions, block_tables, ctx_lens, cu_q_lens
                               block_tables.shape[1], _ptr(ctx_lens), _ptr(cu_q_lens), R, T, ctypes.byref(meta.c),
                               float(scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                               _stream(stream)))
+    return out, lse
+
+
+def pkv_append_paged_attn(pool: Pool, q, q_positions, block_tables, ctx_lens, cu_q_lens, meta: HostMeta,
+                          k_new, v_new, scale: float, out=None, lse=None, workspace=None, stream=None,
+                          want_lse=True):
+    """pkv_append followed by pkv_paged_attn in one call (the kernels take the new K/V from k_new / v_new);
+    meta must hold host q_positions.  Returns (O, LSE)."""
+    _dev_bf16(q, "q")
+    _dev_i32(q_positions, "q_positions")
+    _dev_i32(block_tables, "block_tables")
+    _dev_i32(ctx_lens, "ctx_lens")
+    _dev_i32(cu_q_lens, "cu_q_lens")
+    _dev_bf16(k_new, "k_new")
+    _dev_bf16(v_new, "v_new")
+    T, Hq, D = q.shape
+    if k_new.shape != (T, pool.num_kv_heads, pool.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [T, num_kv_heads, head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev_bf16(out, "out")
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    if workspace is None:
+        workspace = pool.workspace(pkv_paged_attn_workspace_size(pool, Hq, meta))
+    _check(lib.pkv_append_paged_attn(pool.handle, _ptr(q), Hq, _ptr(q_positions), _ptr(block_tables),
+                                     block_tables.shape[1], _ptr(ctx_lens), _ptr(cu_q_lens), ctx_lens.shape[0], T,
+                                     ctypes.byref(meta.c), _ptr(k_new), _ptr(v_new), float(scale), _ptr(out),
+                                     _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)))
     return out, lse
 
 

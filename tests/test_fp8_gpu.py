@@ -4,8 +4,9 @@ Bars: the quantising append leaves the pools bit-identical to the oracle's
 (every code of every block, saturating and subnormal quotients included); swaps
 move the code bytes exactly; split-KV attention over FP8 pools is within
 |gpu - ref| <= 2e-2 + 1e-2 |ref| (O) and 1e-3 (LSE) of the fp64 oracle on the
-dequantised values; batches that need the tensor-core kernel are refused with
-PKV_EUNSUPPORTED.
+dequantised values, and so is tensor-core attention over FP8 pools (codes
+widened to f16 in shared memory) on prefill, recompute and grouped-query
+batches.
 """
 import numpy as np
 import pytest
@@ -55,7 +56,7 @@ def test_fp8_append_bit_exact_whole_pool(hkv, d, ks, vs):
     pool.close()
 
 
-def check_attention(b, ks, vs, rows=None):
+def check_attention(b, ks, vs, rows=None, want_tc=False):
     pool = fp8_pool(b, ks, vs)
     dv = wl.upload(b)
     append(pool, dv)
@@ -65,7 +66,7 @@ def check_attention(b, ks, vs, rows=None):
     torch.cuda.synchronize()
     assert pkv.pkv_check_device_errors(pool) == 0
     st = pkv.pkv_last_plan_stats(pool)
-    assert st["num_tc_items"] == 0
+    assert (st["num_tc_items"] > 0) == want_tc
     k8, v8 = wl.fp8_pool_arrays(b)
     oracle.append_fp8(k8, v8, np.float32(ks), np.float32(vs), b.block_tables, b.cu_q_lens, b.q_positions,
                       b.k_new, b.v_new)
@@ -124,15 +125,37 @@ def test_fp8_swap_bit_exact():
     pool.close()
 
 
-def test_fp8_pool_refuses_tensor_core_batches():
-    b = wl.random_small(71, num_q_heads=4, num_kv_heads=2, head_dim=64)   # holds prefill requests
-    pool = fp8_pool(b, 1.0, 1.0)
-    dv = wl.upload(b)
-    meta = pkv.HostMeta(b.cu_q_lens, b.ctx_lens, b.q_positions)
-    with pytest.raises(pkv.PkvError) as e:
-        pkv.pkv_paged_attn(pool, dv["q"], dv["q_positions"], dv["block_tables"], dv["ctx_lens"], dv["cu_q_lens"],
-                           meta, b.scale)
-    assert e.value.code == pkv.PKV_EUNSUPPORTED
+@pytest.mark.parametrize("maker,ks,vs", [
+    (lambda: wl.random_small(71, num_q_heads=4, num_kv_heads=2, head_dim=64), 2.0 ** -6, 0.0217),
+    (lambda: wl.random_small(72, num_q_heads=4, num_kv_heads=4, head_dim=128, max_ctx=2000, max_q=300), 0.0123, 0.5),
+    (lambda: wl.random_small(73, num_q_heads=16, num_kv_heads=2, head_dim=128, max_ctx=1500, max_q=100),
+     2.0 ** -6, 2.0 ** -6),
+    (lambda: wl.random_small(74, num_q_heads=10, num_kv_heads=2, head_dim=128, max_ctx=900, max_q=60),
+     2.0 ** -12, 2.0 ** 10),   # saturating K codes, subnormal V codes
+])
+def test_fp8_tensor_core_attention_matches_oracle(maker, ks, vs):
+    check_attention(maker(), ks, vs, want_tc=True)
+
+
+@pytest.mark.parametrize("G,D", [(1, 128), (8, 128), (2, 64)])
+def test_fp8_tensor_core_edge_shapes(G, D):
+    tq = 128 // G
+    reqs = [wl._decode(63), wl._new_turn(0, tq - 1), wl._new_turn(7, tq), wl._new_turn(64, tq + 1),
+            wl._new_turn(1, 2 * tq + 3), wl._recompute(200, 17, 5), wl._recompute(129, 128, 1)]
+    b = wl.build_batch(f"fp8_edges_G{G}_D{D}", reqs, num_q_heads=2 * G, num_kv_heads=2, head_dim=D, seed=80 + G + D)
+    check_attention(b, 2.0 ** -6, 2.0 ** -6, want_tc=True)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["llama13b_mixed", "llama70b_gqa", "long_skewed_evict"])
+def test_fp8_full_size_mixed_workloads_sampled(name):
+    b = wl.WORKLOADS[name]()
+    rng = np.random.default_rng(10)
+    rt = rng.integers(0, b.num_tokens, size=400).astype(np.int32)
+    rh = rng.integers(0, b.num_q_heads, size=400).astype(np.int32)
+    check_attention(b, 2.0 ** -6, 2.0 ** -6, rows=(rt, rh), want_tc=True)
+
+
+def test_fp8_pool_rejects_bad_scales():
     with pytest.raises(pkv.PkvError):
         pkv.Pool(16, 2, 64, dtype="fp8_e4m3", k_scale=0.0, v_scale=1.0)
-    pool.close()
