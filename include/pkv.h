@@ -201,12 +201,10 @@ int pkv_paged_attn_workspace_size(pkv_pool* pool, int num_q_heads, int num_reqs,
  * workspace: device memory of at least pkv_paged_attn_workspace_size() bytes,
  * 256-byte aligned, owned by the caller and not used by other work in flight.
  * The split-KV partials and the uploaded work list live there.  The work-list
- * upload runs on a copy stream owned by the pool, ordered after this pool's
- * previous attention call (whatever its stream) but not after other work on
- * `stream`: at the time of the call, the workspace must not be in use by
- * work other than this pool's earlier attention calls.
- * Streams: the kernels run after the upload and after the work already on
- * `stream`.  When the batch has both split-KV and tensor-core work, the
+ * upload runs on `stream`, after the work already queued there and after
+ * this pool's previous attention call (whatever its stream); other work on
+ * other streams must not use the workspace while the call runs.
+ * Streams: the kernels run after the upload.  When the batch has both split-KV and tensor-core work, the
  * split-KV kernel runs on `stream` and the tensor-core kernel on a second
  * stream owned by the pool, forked from `stream` (event) and joined back into
  * it before the merge; every effect of the call is complete once `stream`

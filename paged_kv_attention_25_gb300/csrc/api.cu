@@ -88,11 +88,9 @@ struct pkv_pool {
   // kernel on the caller's stream (fork / join through the two events).
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
-  // Work-list uploads run on `copy`, ordered only after the previous call's
-  // kernels (ws_free), so that they overlap the caller's work queued before
-  // the attention call (the append, typically); the kernels wait on up_done.
-  cudaStream_t copy = nullptr;
-  cudaEvent_t up_done = nullptr, ws_free = nullptr;
+  // Recorded after each attention call's kernels: the next call's work-list
+  // upload (on its own stream) waits for it before rewriting the workspace.
+  cudaEvent_t ws_free = nullptr;
   // Ahead-of-time swap-in: the copy engines bring the blocks into a device
   // staging buffer on the caller's copy stream (swap_ready), and the pool's
   // next call scatters them into place on its own stream (staged_free).
@@ -300,8 +298,6 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
     if (p->side) cudaStreamDestroy(p->side);
     if (p->fork) cudaEventDestroy(p->fork);
     if (p->join) cudaEventDestroy(p->join);
-    if (p->copy) cudaStreamDestroy(p->copy);
-    if (p->up_done) cudaEventDestroy(p->up_done);
     if (p->ws_free) cudaEventDestroy(p->ws_free);
     delete p;
     return rc;
@@ -341,12 +337,7 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
   if (cudaEventCreateWithFlags(&p->fork, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->join, cudaEventDisableTiming) != cudaSuccess)
     return cleanup(fail(PKV_ECUDA, "cudaEventCreate fork/join"));
-  if (cudaStreamCreateWithFlags(&p->copy, cudaStreamNonBlocking) != cudaSuccess) {
-    p->copy = nullptr;
-    return cleanup(fail(PKV_ECUDA, "cudaStreamCreate copy"));
-  }
-  if (cudaEventCreateWithFlags(&p->up_done, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&p->ws_free, cudaEventDisableTiming) != cudaSuccess)
+  if (cudaEventCreateWithFlags(&p->ws_free, cudaEventDisableTiming) != cudaSuccess)
     return cleanup(fail(PKV_ECUDA, "cudaEventCreate upload"));
 
   // The tensor-core kernel's block maps.
@@ -377,8 +368,6 @@ int pkv_pool_destroy(pkv_pool* pool) {
   cudaStreamDestroy(pool->side);
   cudaEventDestroy(pool->fork);
   cudaEventDestroy(pool->join);
-  cudaStreamDestroy(pool->copy);
-  cudaEventDestroy(pool->up_done);
   cudaEventDestroy(pool->ws_free);
   if (pool->swap_staging) cudaFree(pool->swap_staging);
   for (cudaEvent_t e : {pool->swap_ready, pool->swap_staged_free, pool->swap_after})
@@ -508,15 +497,17 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   // Upload the work lists: through a pinned staging slot (asynchronous; the
   // slot is reused only after its previous upload has completed), or for an
   // unusually large list through pageable memory (free again on return).  The
-  // copy runs on the pool's copy stream after the previous call's kernels, so
-  // it overlaps whatever the caller queued on `stream` before this call.
+  // copy runs on `stream`, after the work the caller queued there (which may
+  // still use the workspace's memory: a caching allocator hands out memory
+  // whose last reader is queued on the same stream) and after this pool's
+  // previous attention call, whatever its stream.
   const size_t meta_bytes = pl.off_part_o;
   cudaStream_t s = static_cast<cudaStream_t>(c.stream);
   uint8_t* ws = static_cast<uint8_t*>(c.workspace);
   if (meta_bytes) {
-    PKV_CUDA(cudaStreamWaitEvent(pool->copy, pool->ws_free, 0), "upload wait");
+    PKV_CUDA(cudaStreamWaitEvent(s, pool->ws_free, 0), "upload wait");
     // Scratch shared with other pools: also wait for the last call that used it.
-    if (c.scratch_free) PKV_CUDA(cudaStreamWaitEvent(pool->copy, static_cast<cudaEvent_t>(c.scratch_free), 0), "scratch wait");
+    if (c.scratch_free) PKV_CUDA(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(c.scratch_free), 0), "scratch wait");
     uint8_t* host = nullptr;
     const bool use_pinned = meta_bytes <= pkv_pool::kStagingBytes;
     if (use_pinned) {
@@ -537,10 +528,8 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
     if (!pl.runs.empty()) std::memcpy(host + pl.off_runs, pl.runs.data(), pl.runs.size() * sizeof(RunDesc));
     if (!pl.run_off.empty())
       std::memcpy(host + pl.off_run_off, pl.run_off.data(), pl.run_off.size() * sizeof(int32_t));
-    PKV_CUDA(cudaMemcpyAsync(ws, host, meta_bytes, cudaMemcpyHostToDevice, pool->copy), "upload work list");
-    if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], pool->copy), "staging slot record");
-    PKV_CUDA(cudaEventRecord(pool->up_done, pool->copy), "upload record");
-    PKV_CUDA(cudaStreamWaitEvent(s, pool->up_done, 0), "upload join");
+    PKV_CUDA(cudaMemcpyAsync(ws, host, meta_bytes, cudaMemcpyHostToDevice, s), "upload work list");
+    if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], s), "staging slot record");
   }
 
   AttnArgs a;

@@ -130,8 +130,13 @@ def test_fp8_swap_bit_exact():
     (lambda: wl.random_small(72, num_q_heads=4, num_kv_heads=4, head_dim=128, max_ctx=2000, max_q=300), 0.0123, 0.5),
     (lambda: wl.random_small(73, num_q_heads=16, num_kv_heads=2, head_dim=128, max_ctx=1500, max_q=100),
      2.0 ** -6, 2.0 ** -6),
-    (lambda: wl.random_small(74, num_q_heads=10, num_kv_heads=2, head_dim=128, max_ctx=900, max_q=60),
-     2.0 ** -12, 2.0 ** 10),   # saturating K codes, subnormal V codes
+    # Saturating K codes and subnormal V codes: every key is a new token, so every code comes from
+    # quantising N(0,1) values (history codes times a scale of 2^10 would give values near 1e5,
+    # where the rounding of P alone exceeds an absolute tolerance of 2e-2).
+    (lambda: wl.build_batch("fp8_extreme", [wl._new_turn(0, n) for n in (37, 130, 250, 61)], num_q_heads=10,
+                            num_kv_heads=2, head_dim=128, seed=74), 2.0 ** -12, 2.0 ** 10),
+    (lambda: wl.random_small(75, num_q_heads=10, num_kv_heads=2, head_dim=128, max_ctx=900, max_q=60),
+     2.0 ** -6, 2.0 ** -6),
 ])
 def test_fp8_tensor_core_attention_matches_oracle(maker, ks, vs):
     check_attention(maker(), ks, vs, want_tc=True)
