@@ -191,8 +191,13 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   const int G = a.group;
   const int g = it.kv_head;
   const int Hkv = a.pool.num_kv_heads;
-  const int rows[2] = {it.q_count * G, it.q_count2 * G};
-  const int tok0[2] = {it.q_start, it.q_start + it.q_count};
+  // Per-tile values are scalars selected by tile (not arrays: an array indexed
+  // by the warp's tile would live in local memory, and the issuer's loop would
+  // pay its latency).
+  const int rows0 = it.q_count * G, rows1 = it.q_count2 * G;
+  const int tok00 = it.q_start, tok01 = it.q_start + it.q_count;
+  auto rows_of = [&](int t) { return t ? rows1 : rows0; };
+  auto tok0_of = [&](int t) { return t ? tok01 : tok00; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKSt; ++i) {
@@ -234,16 +239,12 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
   const int row = threadIdx.x & 127;        // its row within the tile (TMEM lane)
   // Key range of each tile from the planner's position bounds, so that the
   // block-table reads need not wait for the device positions.
-  int ntile[2], min_pos[2];
-  int kv_end = it.kv_start;
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int e = min(it.kv_end, it.pos_max[t] + 1);        // keys tile t can see
-    ntile[t] = e > it.kv_start ? (e - it.kv_start + kNK - 1) / kNK : 0;
-    min_pos[t] = it.pos_min[t];
-    kv_end = max(kv_end, e);
-  }
-  const int ntiles = max(ntile[0], ntile[1]);
+  const int e0 = min(it.kv_end, it.pos_max[0] + 1), e1 = min(it.kv_end, it.pos_max[1] + 1);   // keys each tile sees
+  const int ntile0 = e0 > it.kv_start ? (e0 - it.kv_start + kNK - 1) / kNK : 0;
+  const int ntile1 = e1 > it.kv_start ? (e1 - it.kv_start + kNK - 1) / kNK : 0;
+  const int kv_end = max(it.kv_start, max(e0, e1));
+  auto ntile_of = [&](int t) { return t ? ntile1 : ntile0; };
+  const int ntiles = max(ntile0, ntile1);
   // Round trips that only need the item are issued before the barrier: the
   // producer's first two windows of block ids and the softmax threads' query
   // positions.
@@ -273,7 +274,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     }
   }
   int qpos = -1;
-  if (warp < 8 && row < rows[X]) qpos = __ldg(a.q_positions + tok0[X] + row / G);
+  if (warp < 8 && row < rows_of(X)) qpos = __ldg(a.q_positions + tok0_of(X) + row / G);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -380,7 +381,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       // the S commit of the tile that last read it (j - nst), i.e. tile B's
       // where B reaches that key tile, else tile A's.  Before a stage's first
       // use, parity 1 of a fresh barrier passes at once.
-      const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile[1] ? kKSt : 0) + st : B::kVEmpty + st;
+      const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile1 ? kKSt : 0) + st : B::kVEmpty + st;
       if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
       // Test hook: CTA 0 never issues its first K tile, so that the issuer's
       // bounded wait for it runs out.
@@ -438,7 +439,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const int st = j % nst;
       const uint32_t ph = (j / nst) & 1;
       const uint32_t bytes = static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, y >= 0))) * (kBlockSize * D);
-      const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile[1] ? kKSt : 0) + st : B::kVEmpty + st;
+      const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile1 ? kKSt : 0) + st : B::kVEmpty + st;
       if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
       if (a.withhold == 2 && is_k && j == 0 && blockIdx.x == 0) return true;   // test hook (above)
       uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
@@ -565,12 +566,12 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     if (lane == 0) {
       const uint32_t qbytes = static_cast<uint32_t>(D * 2 * G * a.q_box_tokens);
       for (int t = 0; t < 2; ++t) {
-        if (rows[t] > 0) {
+        if (rows_of(t) > 0) {
           mbar_arrive_expect_tx(&bars[B::kQ + t], qbytes);
           uint8_t* qt = smem + S::kOffQ + t * S::kQ;
 #pragma unroll
           for (int hf = 0; hf < S::kHalves; ++hf)
-            tma_load_3d(qt + hf * (kTcRows * 128), &tmap_q, hf * 64, g * G, tok0[t], &bars[B::kQ + t]);
+            tma_load_3d(qt + hf * (kTcRows * 128), &tmap_q, hf * 64, g * G, tok0_of(t), &bars[B::kQ + t]);
         } else {
           mbar_arrive(&bars[B::kQ + t]);
         }
@@ -582,11 +583,16 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     bool ok = mbar_wait_warp(&bars[kQReady], 0, s_abort, a.wait_ns) &&
               mbar_wait_warp(&bars[kQReady + 1], 0, s_abort, a.wait_ns);
     const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
-    // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage).
-    auto issue_s = [&](int t, int j) {
+    // Descriptors that do not change in the loop are built here, and each
+    // step's stage descriptors once per step (not per tile): work between
+    // MMAs in the issuing thread measurably slows their issue.
+    const uint64_t dqA = make_sdesc_sw128(sQ, 16, 1024), dqB = make_sdesc_sw128(sQ + S::kQ, 16, 1024);
+    auto k_desc = [&](int j) { return dk + static_cast<uint64_t>(((j % kKSt) * S::kKV) >> 4); };
+    auto v_desc = [&](int j) { return dv + static_cast<uint64_t>(((j % kVSt) * S::kKV) >> 4); };
+    // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage, kd).
+    auto issue_s = [&](int t, int j, uint64_t kd) {
       if (lane == 0) {
-        const uint64_t dq = make_sdesc_sw128(sQ + t * S::kQ, 16, 1024);
-        const uint64_t kd = dk + static_cast<uint64_t>(((j % kKSt) * S::kKV) >> 4);
+        const uint64_t dq = t ? dqB : dqA;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int hf = ks / 4, kk = ks % 4;
@@ -596,17 +602,16 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         tc_commit(&bars[B::kS + t * kKSt + j % kKSt]);
       }
     };
-    // O_t += P_t(j) V(j), P_t(j) from TMEM (over S_t(j)).
-    auto issue_pv = [&](int t, int j) {
+    // O_t += P_t(j) V(j), P_t(j) from TMEM (over S_t(j)); V(j) in its stage, vd.
+    auto issue_pv = [&](int t, int j, uint64_t vd) {
       if (lane == 0) {
-        const uint64_t vd = dv + static_cast<uint64_t>(((j % kVSt) * S::kKV) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kNK / 16; ++ks)
           tc_mma_ts(tmem + kColO + t * 128, tmem + t * kNK + ks * 8, vd + static_cast<uint64_t>((ks * 2 * S::kGS) >> 4),
                     idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
         // Only the epilogue waits for PV: earlier PVs are covered by the next
         // S commit of the tile (the tensor pipe completes one thread's MMAs in order).
-        if (j == ntile[t] - 1) tc_commit(&bars[B::kPv + t]);
+        if (j == ntile_of(t) - 1) tc_commit(&bars[B::kPv + t]);
       }
     };
     // Each V stage is released once per tile, and only after its tile has
@@ -621,12 +626,13 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     if (ok && ntiles > 0) {
       if ((ok = mbar_wait_warp(&bars[B::kKFull], 0, s_abort, a.wait_ns))) {
         tc_fence_after();
-        if (ntile[0] > 0) issue_s(0, 0);
-        if (ntile[1] > 0) issue_s(1, 0);
+        if (ntile0 > 0) issue_s(0, 0, dk);
+        if (ntile1 > 0) issue_s(1, 0, dk);
       }
     }
     for (int j = 0; ok && j < ntiles; ++j) {
       bool k_next = false;                // K(j+1) seen in its stage
+      const uint64_t vd = v_desc(j), kd_next = k_desc(j + 1);
       if (!(ok = mbar_wait_warp(&bars[B::kVFull + j % kVSt], (j / kVSt) & 1, s_abort, a.wait_ns))) break;
       if (j == ntiles - 1 && last_nkeys < kNK) {
         // Keys past the item's end in its last tile: zero their V rows so that
@@ -644,18 +650,18 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (j < ntile[t]) {
+        if (j < ntile_of(t)) {
           if (!(ok = mbar_wait_warp(&bars[B::kP + t], j & 1, s_abort, a.wait_ns))) break;
           tc_fence_after();
-          issue_pv(t, j);
-          if (j + 1 < ntile[t]) {
+          issue_pv(t, j, vd);
+          if (j + 1 < ntile_of(t)) {
             if (!k_next && !(ok = mbar_wait_warp(&bars[B::kKFull + (j + 1) % kKSt], ((j + 1) / kKSt) & 1, s_abort, a.wait_ns)))
               break;
             k_next = true;
             // No tcgen05 fence: TMA data is ordered by the K barrier, and the P
             // wait above already ordered the softmax's TMEM writes before this
             // thread's MMAs, which the tensor pipe runs in issue order.
-            issue_s(t, j + 1);
+            issue_s(t, j + 1, kd_next);
           }
         }
       }
@@ -673,8 +679,9 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     // ------------------------------------------------------------ softmax / epilogue of tile X
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t colS = X * kNK, colO = kColO + X * 128;
-    const int nrows = rows[X];
-    const int nt = ntile[X];
+    const int nrows = rows_of(X);
+    const int nt = ntile_of(X);
+    const int min_pos = X ? it.pos_min[1] : it.pos_min[0];
     // FP8 pools: S holds q . code, so k_scale joins the score scale (and
     // v_scale the final 1/l).
     const float sl2 = F8 ? a.scale_log2 * a.pool.k_scale : a.scale_log2;
@@ -712,7 +719,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
 #pragma unroll
       for (int c = 0; c < kNK; c += 16) tmem_ld16(tmem + lane_base + colS + c, s + c);
       tmem_wait_ld();
-      if (key0 + kNK - 1 > min_pos[X] || key0 + kNK > kv_end) {
+      if (key0 + kNK - 1 > min_pos || key0 + kNK > kv_end) {
         // The row sees keys [0, min(qpos + 1, kv_end)): a prefix of the tile.
         const int lim = min(qpos + 1, kv_end) - key0;
 #pragma unroll
@@ -788,9 +795,9 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const bool valid = row < nrows;
       const float inv = l > 0.f ? (F8 ? a.pool.v_scale : 1.f) / l : 0.f;
       const float lse = l > 0.f ? (m + fast_log2(l)) * kLn2 : -CUDART_INF_F;
-      const int t = tok0[X] + (valid ? row / G : 0);
+      const int t = tok0_of(X) + (valid ? row / G : 0);
       const int h = g * G + row % G;
-      const int prow = it.part + (X == 0 ? row : rows[0] + row);
+      const int prow = it.part + (X == 0 ? row : rows0 + row);
       uint4* dst_o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D);
       float4* dst_p = it.part >= 0 ? reinterpret_cast<float4*>(a.part_o + static_cast<int64_t>(prow) * D) : nullptr;
       // O in 64-column batches: four TMEM loads in flight per wait.

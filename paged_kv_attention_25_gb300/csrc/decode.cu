@@ -18,10 +18,12 @@
 // SFU, fp32 accumulation; O rounded to bf16 once at the end.
 //
 // FP8 pools (F8): the chunks are e4m3 codes, half the bytes, so each warp
-// keeps twice the stages in flight.  The codes are widened to bf16 bit
-// patterns by byte moves and multiplied with mixed-precision FMAs (see
-// load_row_bf16); k_scale goes into each score's scale and v_scale into the
-// final 1/l.
+// keeps twice the stages in flight.  The codes are widened to f16 by the
+// conversion instruction (exact) and multiplied with mixed-precision FMAs
+// (f16 operands, fp32 accumulation; see load_row_f16); q and p are f16,
+// k_scale goes into each score's scale and v_scale into the final 1/l.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -61,43 +63,35 @@ __device__ __forceinline__ void load_row(const uint8_t* p, float* f) {
     f[0] = bf16lo_to_f32(v); f[1] = bf16hi_to_f32(v);
   }
 }
-// The same dims of one row of e4m3 codes as bf16 bit patterns, two per 32-bit
-// word (lowest element in the low half).  Byte moves put each code's sign in
-// bit 15 and its 4 exponent and 3 mantissa bits at the low end of bf16's
-// exponent field and the top of its mantissa (subnormal codes land on bf16
-// subnormals), which reads the code as exactly its value times 2^-120 (bf16's
-// exponent bias is 127, e4m3's 7).  The 2^120 is restored outside the inner
-// loops by exact power-of-two factors (kF8Pre on each score and on p, kF8Post
-// in the score scale and in 1/l), so that the sums stay in the normal range.
-// The inner loops multiply these patterns with mixed-precision FMAs: bf16
-// operands, exact products, fp32 accumulation.
+// The same dims of one row of e4m3 codes as f16 values, two per 32-bit word
+// (lowest element in the low half): the conversion instruction widens each
+// pair of codes exactly (every e4m3 value is an f16 value), on the
+// conversion pipe rather than the integer ALU.
 template <int kDPL>
-__device__ __forceinline__ void load_row_bf16(const uint8_t* p, uint32_t* w) {
+__device__ __forceinline__ void load_row_f16(const uint8_t* p, uint32_t* w) {
   const uint32_t v = kDPL == 4 ? *reinterpret_cast<const uint32_t*>(p) : *reinterpret_cast<const uint16_t*>(p);
-  const uint32_t y01 = __byte_perm(v, 0u, 0x1404);   // code 1 in bits 24..31, code 0 in bits 8..15
-  w[0] = (y01 & 0x80008000u) | ((y01 >> 4) & 0x07F007F0u);
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xffffu), __NV_E4M3);
+  w[0] = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
   if constexpr (kDPL == 4) {
-    const uint32_t y23 = __byte_perm(v, 0u, 0x3424);
-    w[1] = (y23 & 0x80008000u) | ((y23 >> 4) & 0x07F007F0u);
+    h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v >> 16), __NV_E4M3);
+    w[1] = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
   }
 }
-// c0 += lo(a) * lo(b), c1 += hi(a) * hi(b).
-__device__ __forceinline__ void fma_bf16x2(float& c0, float& c1, uint32_t a, uint32_t b) {
+// c0 += lo(a) * lo(b), c1 += hi(a) * hi(b): f16 operands, exact products,
+// fp32 accumulation.
+__device__ __forceinline__ void fma_f16x2(float& c0, float& c1, uint32_t a, uint32_t b) {
   asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
-      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %1, ah, bh, %1;\n\t}"
       : "+f"(c0), "+f"(c1)
       : "r"(a), "r"(b));
 }
-// c0 += p * lo(b), c1 += p * hi(b), p a bf16.
-__device__ __forceinline__ void fma_bf16_bcast(float& c0, float& c1, uint16_t p, uint32_t b) {
+// c0 += p * lo(b), c1 += p * hi(b), p an f16.
+__device__ __forceinline__ void fma_f16_bcast(float& c0, float& c1, uint16_t p, uint32_t b) {
   asm("{\n\t.reg .b16 bl, bh;\n\tmov.b32 {bl, bh}, %3;\n\t"
-      "fma.rn.f32.bf16 %0, %2, bl, %0;\n\tfma.rn.f32.bf16 %1, %2, bh, %1;\n\t}"
+      "fma.rn.f32.f16 %0, %2, bl, %0;\n\tfma.rn.f32.f16 %1, %2, bh, %1;\n\t}"
       : "+f"(c0), "+f"(c1)
       : "h"(p), "r"(b));
 }
-
-constexpr float kF8Pre = 18446744073709551616.0f;   // 2^64
-constexpr float kF8Post = 72057594037927936.0f;     // 2^56; kF8Pre * kF8Post = 2^120
 
 // The streaming part of one item for items of at most R query rows (R = 1, 2
 // or 4: the row loops are unrolled for R, so a one-row decode item issues no
@@ -115,11 +109,11 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
   const int Hkv = a.pool.num_kv_heads;
   const int g = it.kv_head;
 
-  // Per-row query (pre-scaled by scale*log2 e, and k_scale * kF8Pre for fp8)
-  // and position; rows >= `rows` are inert.
-  // F8: q stays bf16 (qw) and the whole scale goes onto each score instead.
+  // Per-row query (pre-scaled by scale*log2 e) and position; rows >= `rows`
+  // are inert.  F8: q is held as f16 pairs (qw; exact for |q| within f16's
+  // range) and the whole scale, k_scale included, goes onto each score.
   const float qs = a.scale_log2;
-  const float s_scale = a.scale_log2 * a.pool.k_scale * kF8Post;
+  const float s_scale = a.scale_log2 * a.pool.k_scale;
   float q[R][kDPL];
   uint32_t qw[R][kDPL / 2];
   int qpos[R];
@@ -137,7 +131,10 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
       const uint16_t* src = static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D + lane * kDPL;
       if constexpr (F8) {
 #pragma unroll
-        for (int j = 0; j < kDPL / 2; ++j) qw[r][j] = reinterpret_cast<const uint32_t*>(src)[j];
+        for (int j = 0; j < kDPL / 2; ++j) {
+          const uint32_t w = reinterpret_cast<const uint32_t*>(src)[j];
+          qw[r][j] = pack_f16x2(bf16lo_to_f32(w), bf16hi_to_f32(w));
+        }
       } else {
         float qf[kDPL];
         load_row<kDPL>(reinterpret_cast<const uint8_t*>(src), qf);
@@ -186,9 +183,9 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     const int src_lane = j & 31;
     const int pb = (j >> 5) == win ? __shfl_sync(0xffffffffu, ids_cur, src_lane)
                                    : __shfl_sync(0xffffffffu, ids_next, src_lane);
-    // Test hook: CTA 0's warp 0 never issues its first copy, so that its
-    // bounded wait for that stage runs out.
-    const bool withheld = a.withhold == 1 && j == 0 && blockIdx.x == 0 && warp == 0;
+    // Test hook: the first work item's warp 0 never issues its first copy,
+    // so that its bounded wait for that stage runs out.
+    const bool withheld = a.withhold == 1 && j == 0 && blockIdx.x == a.n_append_ctas && warp == 0;
     if (lane == 0 && !withheld) {
       const int st = j % kStages;
       uint8_t* dst = my_ring + st * S::kStage;
@@ -281,12 +278,12 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     for (int k = 0; k < kBlockSize; ++k) {
       if constexpr (F8) {
         uint32_t kw[kDPL / 2];
-        load_row_bf16<kDPL>(kb + k * kRowBytes + lane * kLaneBytes, kw);
+        load_row_f16<kDPL>(kb + k * kRowBytes + lane * kLaneBytes, kw);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-          for (int j = 0; j < kDPL / 2; ++j) fma_bf16x2(s0, s1, qw[r][j], kw[j]);
+          for (int j = 0; j < kDPL / 2; ++j) fma_f16x2(s0, s1, qw[r][j], kw[j]);
           part[r][k] = s0 + s1;
         }
       } else {
@@ -333,7 +330,7 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
         v1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
       }
       float s = v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
-      if constexpr (F8) s = (s * kF8Pre) * s_scale;
+      if constexpr (F8) s = s * s_scale;
       const int key = key0 + (lane >> 1);
       if (key > qpos[r] || key >= kv_end) s = -CUDART_INF_F;
       float mx = s;
@@ -351,9 +348,9 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
 #pragma unroll
       for (int d = 0; d < kDPL; ++d) acc[r][d] *= alpha;
       if ((lane & 1) == 0) {
-        if constexpr (F8)   // bf16 p (times kF8Pre) for the mixed-precision PV FMAs
+        if constexpr (F8)   // f16 p for the mixed-precision PV FMAs
           reinterpret_cast<uint16_t*>(my_p)[r * kBlockSize + (lane >> 1)] =
-              static_cast<uint16_t>(pack_bf16x2(p * kF8Pre, 0.f) & 0xffffu);
+              static_cast<uint16_t>(pack_f16x2(p, 0.f) & 0xffffu);
         else
           my_p[r * kBlockSize + (lane >> 1)] = p;
       }
@@ -368,7 +365,7 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
       for (int k = 0; k < kBlockSize; ++k) {
         if constexpr (F8) {
           uint32_t vw[kDPL / 2];
-          load_row_bf16<kDPL>(vb + k * kRowBytes + lane * kLaneBytes, vw);
+          load_row_f16<kDPL>(vb + k * kRowBytes + lane * kLaneBytes, vw);
           if constexpr (decltype(masked)::value) {
             const bool live = key0 + k < kv_end;
 #pragma unroll
@@ -379,7 +376,7 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
             if (r >= rows) break;
             const uint16_t p = reinterpret_cast<const uint16_t*>(my_p)[r * kBlockSize + k];
 #pragma unroll
-            for (int j = 0; j < kDPL / 2; ++j) fma_bf16_bcast(acc[r][2 * j], acc[r][2 * j + 1], p, vw[j]);
+            for (int j = 0; j < kDPL / 2; ++j) fma_f16_bcast(acc[r][2 * j], acc[r][2 * j + 1], p, vw[j]);
           }
         } else {
           float vf[kDPL];
@@ -429,11 +426,12 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
   }
 }
 
-// The fused call's append CTAs (after the work items in the grid): CTA c of n
-// writes chunks c*128 + tid, stepping by n*128, of the batch's new K/V rows
-// into the pool.  The attention items of the launch never read those slots
-// from the pool (they take the rows from the new K/V), so nothing orders the
-// two inside the launch.
+// The fused call's append CTAs (the first n CTAs of the grid, so that they
+// are dispatched before the attention items and finish while the SMs are
+// shared): CTA c of n writes chunks c*128 + tid, stepping by n*128, of the
+// batch's new K/V rows into the pool.  The attention items of the launch
+// never read those slots from the pool (they take the rows from the new K/V),
+// so nothing orders the two inside the launch.
 template <bool F8>
 __device__ __forceinline__ void append_role(const AttnArgs& a, int c, int n) {
   const int cpr_log2 = a.pool.head_dim == 128 ? 4 : 3;
@@ -448,9 +446,9 @@ __device__ __forceinline__ void append_role(const AttnArgs& a, int c, int n) {
 
 template <int D, bool F8>
 __global__ void __launch_bounds__(kWarps * 32, 3)
-decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items, int n_items) {
-  if (static_cast<int>(blockIdx.x) >= n_items) {
-    append_role<F8>(a, blockIdx.x - n_items, gridDim.x - n_items);
+decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
+  if (static_cast<int>(blockIdx.x) < a.n_append_ctas) {
+    append_role<F8>(a, blockIdx.x, a.n_append_ctas);
     return;
   }
   using S = DecodeSmem<D, F8>;
@@ -466,7 +464,7 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items, int n_items)
   // round trip before the first copy is paid by every CTA.  Once any wait in
   // this launch has given up, the remaining CTAs do nothing (__syncthreads_or
   // makes the decision the same for every thread).
-  const WorkItem it = items[blockIdx.x];
+  const WorkItem it = items[blockIdx.x - a.n_append_ctas];
   const unsigned err0 = *reinterpret_cast<volatile unsigned*>(a.pool.err);
   if (__syncthreads_or((err0 & PKV_DEVERR_TIMEOUT) != 0)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -506,7 +504,7 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items, int n_items)
         o1 += src[d + 1] * f;
       }
     }
-    const float inv = lsum > 0.f ? (F8 ? a.pool.v_scale * kF8Post : 1.f) / lsum : 0.f;
+    const float inv = lsum > 0.f ? (F8 ? a.pool.v_scale : 1.f) / lsum : 0.f;
     o0 *= inv;
     o1 *= inv;
     const float lse = lsum > 0.f ? (mstar + fast_log2(lsum)) * kLn2 : -CUDART_INF_F;
@@ -552,8 +550,7 @@ static int launch_decode_d(const AttnArgs& a, const WorkItem* items, int n_items
   const int smem = DecodeSmem<D, F8>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, F8><<<n_items + a.n_append_ctas, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(
-      a, items, n_items);
+  decode_kernel<D, F8><<<n_items + a.n_append_ctas, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(a, items);
   return cudaGetLastError();
 }
 
