@@ -141,8 +141,9 @@ typedef struct {
 } pkv_profile;
 
 /* Create a KV block pool.  Allocates the pools (unless caller storage is
- * given), a device error word, and builds the TMA descriptors the
- * tensor-core kernel uses.  Synchronous.  Errors: PKV_EINVAL (bad desc),
+ * given), a device error word, a 4 MiB device buffer for the attention
+ * calls' work lists with two pinned 4 MiB host staging buffers, and builds
+ * the TMA descriptors the tensor-core kernel uses.  Synchronous.  Errors: PKV_EINVAL (bad desc),
  * PKV_EUNSUPPORTED (block_size != 16, head_dim not 64/128), PKV_ENOMEM,
  * PKV_ECUDA (no device, driver too old). */
 int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out);
@@ -200,11 +201,16 @@ int pkv_paged_attn_workspace_size(pkv_pool* pool, int num_q_heads, int num_reqs,
  * copies of cu_q_lens / ctx_lens (and optionally q_positions) for planning.
  * workspace: device memory of at least pkv_paged_attn_workspace_size() bytes,
  * 256-byte aligned, owned by the caller and not used by other work in flight.
- * The split-KV partials and the uploaded work list live there.  The work-list
- * upload runs on `stream`, after the work already queued there and after
- * this pool's previous attention call (whatever its stream); other work on
- * other streams must not use the workspace while the call runs.
- * Streams: the kernels run after the upload.  When the batch has both split-KV and tensor-core work, the
+ * The split-KV partials live there (and the work lists, for a batch whose
+ * lists exceed the pool's 4 MiB work-list buffer).  The work lists are
+ * uploaded into a device buffer the pool owns, on a copy stream of the pool,
+ * ordered after this pool's previous attention call (whatever its stream),
+ * so the upload overlaps the caller's earlier work; lists larger than that
+ * buffer go into the workspace on `stream`, after the work already queued
+ * there.  Other work on other streams must not use the workspace while the
+ * call runs.
+ * Streams: the kernels run after the upload and after the work already on
+ * `stream`.  When the batch has both split-KV and tensor-core work, the
  * split-KV kernel runs on `stream` and the tensor-core kernel on a second
  * stream owned by the pool, forked from `stream` (event) and joined back into
  * it before the merge; every effect of the call is complete once `stream`

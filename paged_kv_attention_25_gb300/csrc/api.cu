@@ -89,8 +89,23 @@ struct pkv_pool {
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   // Recorded after each attention call's kernels: the next call's work-list
-  // upload (on its own stream) waits for it before rewriting the workspace.
+  // upload waits for it before rewriting the work lists.
   cudaEvent_t ws_free = nullptr;
+  // Device copy of the work lists, owned by the pool (kStagingBytes): the
+  // upload into it runs on the pool's copy stream, ordered after the previous
+  // call's kernels only, so it overlaps the caller's earlier work (the
+  // append, the next step's input copies) and never queues behind it.  The
+  // caller's workspace, whose memory may still be in use by work queued on
+  // the caller's stream, is written only by kernels on that stream.
+  // Two buffers, used by alternate calls (with the pinned staging slots): an
+  // upload then waits only for the call before the previous one, long done,
+  // so it is ready to run when it is submitted and does not queue on the
+  // copy engine behind transfers submitted after it (a serving loop's next
+  // inputs).
+  uint8_t* d_wl[2] = {nullptr, nullptr};
+  cudaEvent_t wl_free[2] = {nullptr, nullptr};
+  cudaStream_t copy = nullptr;
+  cudaEvent_t up_done = nullptr;
   // Ahead-of-time swap-in: the copy engines bring the blocks into a device
   // staging buffer on the caller's copy stream (swap_ready), and the pool's
   // next call scatters them into place on its own stream (staged_free).
@@ -299,6 +314,12 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
     if (p->fork) cudaEventDestroy(p->fork);
     if (p->join) cudaEventDestroy(p->join);
     if (p->ws_free) cudaEventDestroy(p->ws_free);
+    for (int i = 0; i < 2; ++i) {
+      if (p->d_wl[i]) cudaFree(p->d_wl[i]);
+      if (p->wl_free[i]) cudaEventDestroy(p->wl_free[i]);
+    }
+    if (p->copy) cudaStreamDestroy(p->copy);
+    if (p->up_done) cudaEventDestroy(p->up_done);
     delete p;
     return rc;
   };
@@ -337,8 +358,23 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
   if (cudaEventCreateWithFlags(&p->fork, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&p->join, cudaEventDisableTiming) != cudaSuccess)
     return cleanup(fail(PKV_ECUDA, "cudaEventCreate fork/join"));
-  if (cudaEventCreateWithFlags(&p->ws_free, cudaEventDisableTiming) != cudaSuccess)
+  if (cudaEventCreateWithFlags(&p->ws_free, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&p->up_done, cudaEventDisableTiming) != cudaSuccess)
     return cleanup(fail(PKV_ECUDA, "cudaEventCreate upload"));
+  if (cudaStreamCreateWithFlags(&p->copy, cudaStreamNonBlocking) != cudaSuccess) {
+    p->copy = nullptr;
+    return cleanup(fail(PKV_ECUDA, "cudaStreamCreate copy"));
+  }
+  for (int i = 0; i < 2; ++i) {
+    if (cudaMalloc(&p->d_wl[i], pkv_pool::kStagingBytes) != cudaSuccess) {
+      p->d_wl[i] = nullptr;
+      return cleanup(fail(PKV_ENOMEM, "cudaMalloc work lists"));
+    }
+    if (cudaEventCreateWithFlags(&p->wl_free[i], cudaEventDisableTiming) != cudaSuccess) {
+      p->wl_free[i] = nullptr;
+      return cleanup(fail(PKV_ECUDA, "cudaEventCreate work lists"));
+    }
+  }
 
   // The tensor-core kernel's block maps.
   {
@@ -369,6 +405,12 @@ int pkv_pool_destroy(pkv_pool* pool) {
   cudaEventDestroy(pool->fork);
   cudaEventDestroy(pool->join);
   cudaEventDestroy(pool->ws_free);
+  for (int i = 0; i < 2; ++i) {
+    cudaFree(pool->d_wl[i]);
+    cudaEventDestroy(pool->wl_free[i]);
+  }
+  cudaStreamDestroy(pool->copy);
+  cudaEventDestroy(pool->up_done);
   if (pool->swap_staging) cudaFree(pool->swap_staging);
   for (cudaEvent_t e : {pool->swap_ready, pool->swap_staged_free, pool->swap_after})
     if (e) cudaEventDestroy(e);
@@ -496,18 +538,26 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
 
   // Upload the work lists: through a pinned staging slot (asynchronous; the
   // slot is reused only after its previous upload has completed), or for an
-  // unusually large list through pageable memory (free again on return).  The
-  // copy runs on `stream`, after the work the caller queued there (which may
-  // still use the workspace's memory: a caching allocator hands out memory
-  // whose last reader is queued on the same stream) and after this pool's
-  // previous attention call, whatever its stream.
+  // unusually large list through pageable memory (free again on return).
+  // Into the pool's own device buffer on the pool's copy stream (after the
+  // pool's previous call, whatever its stream), or, for the static scratch
+  // and for lists larger than that buffer, into the workspace on `stream`,
+  // after the work the caller queued there (which may still use the
+  // workspace's memory: a caching allocator hands out memory whose last
+  // reader is queued on the same stream).
   const size_t meta_bytes = pl.off_part_o;
   cudaStream_t s = static_cast<cudaStream_t>(c.stream);
   uint8_t* ws = static_cast<uint8_t*>(c.workspace);
+  const bool own = !c.static_scratch && meta_bytes <= pkv_pool::kStagingBytes;
+  const int slot = pool->pinned_slot ^ 1;   // this call's staging slot and device buffer
+  uint8_t* wl = own ? pool->d_wl[slot] : ws;   // where the work lists live on the device
+  cudaStream_t up = own ? pool->copy : s;
   if (meta_bytes) {
-    PKV_CUDA(cudaStreamWaitEvent(s, pool->ws_free, 0), "upload wait");
+    // The buffer's last reader: the call two back (own buffers), or the
+    // previous call (the workspace).
+    PKV_CUDA(cudaStreamWaitEvent(up, own ? pool->wl_free[slot] : pool->ws_free, 0), "upload wait");
     // Scratch shared with other pools: also wait for the last call that used it.
-    if (c.scratch_free) PKV_CUDA(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(c.scratch_free), 0), "scratch wait");
+    if (c.scratch_free) PKV_CUDA(cudaStreamWaitEvent(up, static_cast<cudaEvent_t>(c.scratch_free), 0), "scratch wait");
     uint8_t* host = nullptr;
     const bool use_pinned = meta_bytes <= pkv_pool::kStagingBytes;
     if (use_pinned) {
@@ -528,8 +578,12 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
     if (!pl.runs.empty()) std::memcpy(host + pl.off_runs, pl.runs.data(), pl.runs.size() * sizeof(RunDesc));
     if (!pl.run_off.empty())
       std::memcpy(host + pl.off_run_off, pl.run_off.data(), pl.run_off.size() * sizeof(int32_t));
-    PKV_CUDA(cudaMemcpyAsync(ws, host, meta_bytes, cudaMemcpyHostToDevice, s), "upload work list");
-    if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], s), "staging slot record");
+    PKV_CUDA(cudaMemcpyAsync(wl, host, meta_bytes, cudaMemcpyHostToDevice, up), "upload work list");
+    if (use_pinned) PKV_CUDA(cudaEventRecord(pool->pinned_done[pool->pinned_slot], up), "staging slot record");
+    if (own) {
+      PKV_CUDA(cudaEventRecord(pool->up_done, up), "upload record");
+      PKV_CUDA(cudaStreamWaitEvent(s, pool->up_done, 0), "upload join");
+    }
   }
 
   AttnArgs a;
@@ -546,8 +600,8 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   a.lse = c.lse;
   a.part_o = reinterpret_cast<float*>(ws + pl.off_part_o);
   a.part_lse = reinterpret_cast<float*>(ws + pl.off_part_lse);
-  a.merge_dec = reinterpret_cast<const MergeItem*>(ws + pl.off_merge_dec);
-  a.merge_cnt = reinterpret_cast<int*>(ws + pl.off_merge_cnt);
+  a.merge_dec = reinterpret_cast<const MergeItem*>(wl + pl.off_merge_dec);
+  a.merge_cnt = reinterpret_cast<int*>(wl + pl.off_merge_cnt);
   a.q_box_tokens = 0;
   a.wait_ns = pool->wait_ns;
   a.withhold = pool->withhold;
@@ -558,8 +612,8 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   a.num_tokens = c.num_tokens;
   a.n_append_ctas = 0;
   a.kn_box_tokens = 0;
-  a.runs = reinterpret_cast<const RunDesc*>(ws + pl.off_runs);
-  a.run_off = reinterpret_cast<const int32_t*>(ws + pl.off_run_off);
+  a.runs = reinterpret_cast<const RunDesc*>(wl + pl.off_runs);
+  a.run_off = reinterpret_cast<const int32_t*>(wl + pl.off_run_off);
   if (fused) {
     // Append CTAs of the split-KV launch: about 8 chunks a thread.
     const int64_t chunks = static_cast<int64_t>(c.num_tokens) * pool->num_kv_heads * (pool->head_dim / 8);
@@ -580,9 +634,9 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
     }
   }
 
-  const WorkItem* d_dec = reinterpret_cast<const WorkItem*>(ws + pl.off_decode);
-  const WorkItem* d_tc = reinterpret_cast<const WorkItem*>(ws + pl.off_tc);
-  const MergeItem* d_merge = reinterpret_cast<const MergeItem*>(ws + pl.off_merge);
+  const WorkItem* d_dec = reinterpret_cast<const WorkItem*>(wl + pl.off_decode);
+  const WorkItem* d_tc = reinterpret_cast<const WorkItem*>(wl + pl.off_tc);
+  const MergeItem* d_merge = reinterpret_cast<const MergeItem*>(wl + pl.off_merge);
   // The two attention kernels are independent (disjoint outputs and workspace
   // regions): with both present, the split-KV kernel runs on the caller's
   // stream and the tensor-core kernel on the pool's side stream.  The caller's
@@ -624,8 +678,9 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
                       [&] { return launch_merge(a, d_merge, static_cast<int>(pl.merge.size()), c.stream); });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "merge launch");
   }
-  // The next call's upload may overwrite the work lists once these kernels are done.
+  // The next calls' uploads may overwrite the work lists once these kernels are done.
   PKV_CUDA(cudaEventRecord(pool->ws_free, s), "workspace release");
+  if (own) PKV_CUDA(cudaEventRecord(pool->wl_free[slot], s), "work-list release");
   if (c.scratch_free) PKV_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(c.scratch_free), s), "scratch release");
   return PKV_OK;
 }

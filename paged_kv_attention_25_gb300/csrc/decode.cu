@@ -183,9 +183,9 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
     const int src_lane = j & 31;
     const int pb = (j >> 5) == win ? __shfl_sync(0xffffffffu, ids_cur, src_lane)
                                    : __shfl_sync(0xffffffffu, ids_next, src_lane);
-    // Test hook: the first work item's warp 0 never issues its first copy,
-    // so that its bounded wait for that stage runs out.
-    const bool withheld = a.withhold == 1 && j == 0 && blockIdx.x == a.n_append_ctas && warp == 0;
+    // Test hook: CTA 0's warp 0 never issues its first copy, so that its
+    // bounded wait for that stage runs out.
+    const bool withheld = a.withhold == 1 && j == 0 && blockIdx.x == 0 && warp == 0;
     if (lane == 0 && !withheld) {
       const int st = j % kStages;
       uint8_t* dst = my_ring + st * S::kStage;
@@ -426,12 +426,13 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
   }
 }
 
-// The fused call's append CTAs (the first n CTAs of the grid, so that they
-// are dispatched before the attention items and finish while the SMs are
-// shared): CTA c of n writes chunks c*128 + tid, stepping by n*128, of the
-// batch's new K/V rows into the pool.  The attention items of the launch
-// never read those slots from the pool (they take the rows from the new K/V),
-// so nothing orders the two inside the launch.
+// The fused call's append CTAs (the last n CTAs of the grid: placed first,
+// their wave of CTAs with the attention CTAs' shared-memory footprint kept
+// other work, such as a concurrent swap, off the SMs): CTA c of n writes
+// chunks c*128 + tid, stepping by n*128, of the batch's new K/V rows into the
+// pool.  The attention items of the launch never read those slots from the
+// pool (they take the rows from the new K/V), so nothing orders the two
+// inside the launch.
 template <bool F8>
 __device__ __forceinline__ void append_role(const AttnArgs& a, int c, int n) {
   const int cpr_log2 = a.pool.head_dim == 128 ? 4 : 3;
@@ -446,9 +447,9 @@ __device__ __forceinline__ void append_role(const AttnArgs& a, int c, int n) {
 
 template <int D, bool F8>
 __global__ void __launch_bounds__(kWarps * 32, 3)
-decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
-  if (static_cast<int>(blockIdx.x) < a.n_append_ctas) {
-    append_role<F8>(a, blockIdx.x, a.n_append_ctas);
+decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items, int n_items) {
+  if (static_cast<int>(blockIdx.x) >= n_items) {
+    append_role<F8>(a, blockIdx.x - n_items, a.n_append_ctas);
     return;
   }
   using S = DecodeSmem<D, F8>;
@@ -464,7 +465,7 @@ decode_kernel(const AttnArgs a, const WorkItem* __restrict__ items) {
   // round trip before the first copy is paid by every CTA.  Once any wait in
   // this launch has given up, the remaining CTAs do nothing (__syncthreads_or
   // makes the decision the same for every thread).
-  const WorkItem it = items[blockIdx.x - a.n_append_ctas];
+  const WorkItem it = items[blockIdx.x];
   const unsigned err0 = *reinterpret_cast<volatile unsigned*>(a.pool.err);
   if (__syncthreads_or((err0 & PKV_DEVERR_TIMEOUT) != 0)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -550,7 +551,8 @@ static int launch_decode_d(const AttnArgs& a, const WorkItem* items, int n_items
   const int smem = DecodeSmem<D, F8>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, F8><<<n_items + a.n_append_ctas, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(a, items);
+  decode_kernel<D, F8><<<n_items + a.n_append_ctas, kWarps * 32, smem, static_cast<cudaStream_t>(stream)>>>(
+      a, items, n_items);
   return cudaGetLastError();
 }
 
