@@ -337,7 +337,11 @@ class Bench:
         import torch
         self.args, self.dev = args, dev
         self.main = torch.cuda.current_stream()
-        self.side = torch.cuda.Stream(device=dev)
+        # The swap-out frees HBM for the next step, so a serving loop gives it
+        # priority: its few CTAs are dispatched ahead of the attention CTAs
+        # still waiting for an SM, and the copy runs beside the attention
+        # instead of after it.
+        self.side = torch.cuda.Stream(device=dev, priority=-1)
         self.flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
         self.flush_r = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
         self.flush_sum = torch.empty((), dtype=torch.float32, device=dev)
@@ -445,6 +449,7 @@ def measure_workload(B: Bench, name: str, headline: bool, rank: int, world: int)
     # ---- the fused step: pkv_append_paged_attn in place of the two calls
     fused_ms, fused_prof = timed_steps(args.steps, 1, fused=True)
     f_tok, f_sec = aggregate_ranks(float(T * args.steps), sum(fused_ms) / 1e3)
+    fser_ms, fser_prof = timed_steps(max(10, args.steps // 2), 2, fused=True)
 
     # Host planning time for this batch, uncached (the step reuses its cached
     # plan while the batch metadata is unchanged): median of 5 plans.
@@ -573,7 +578,11 @@ def measure_workload(B: Bench, name: str, headline: bool, rank: int, world: int)
                        "variants": REPLAN_VARIANTS},
         "fused": {"value": f_tok / f_sec, "unit": UNIT, "ms_per_step": 1e3 * f_sec / args.steps,
                   "kernels": {k: {"launches": v["launches"], "avg_us": 1e3 * v["total_ms"] / max(1, v["launches"])}
-                              for k, v in fused_prof.items()}},
+                              for k, v in fused_prof.items()},
+                  "kernels_one_at_a_time": {k: {"launches": v["launches"],
+                                                "avg_us": 1e3 * v["total_ms"] / max(1, v["launches"])}
+                                            for k, v in fser_prof.items()},
+                  "ms_per_step_one_at_a_time": float(np.mean(fser_ms))},
         "clocks": clk.summary(),
         "wall_s_timed": wall1 - wall0,
         "swap_out_bytes_per_step": swap_bytes,

@@ -238,6 +238,10 @@ int pkv_paged_attn(pkv_pool* pool, const void* q, int num_q_heads, const int32_t
  * instead of reading them back from the pool, so nothing waits for the pool
  * write: CTAs of the split-KV launch write the new rows into the pool beside
  * the attention work (one launch fewer than the two calls).
+ *   - FP8 pools whose batch has tensor-core work: the call appends first (its
+ *     own launch on `stream`), then attends to the pool.  Every tensor-core
+ *     CTA that reads a new row would otherwise quantise it again; the result
+ *     is the same.
  *   - host_meta->q_positions is required (the plan records, per request, the
  *     runs of consecutive new positions); PKV_EINVAL without it.
  *   - Workspace: pkv_paged_attn_workspace_size for the same batch.

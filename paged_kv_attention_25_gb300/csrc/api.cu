@@ -75,6 +75,8 @@ struct pkv_pool {
   int device = 0, num_sms = 0;
   CUtensorMap tmap_k;  // 64-byte aligned by its type
   CUtensorMap tmap_v;
+  CUtensorMap dmap_k;  // split-KV kernel's maps (FP8, D = 128); copies of tmap_* otherwise
+  CUtensorMap dmap_v;
   std::mutex mu;
   Plan plan;
   // Pinned, double-buffered staging for work-list uploads (allocated at
@@ -164,13 +166,25 @@ int timed_launch(pkv_pool* pool, int kernel, void* stream, F&& fn) {
   return rc;
 }
 
-int make_tmap(CUtensorMap* map, void* base, int num_blocks, int hkv, int head_dim, bool fp8) {
+// swizzle: only for FP8 pools with D = 128 (the split-KV kernel's map, whose
+// 128-byte rows land with 128-byte swizzle); the tensor-core kernel's FP8
+// map lands unswizzled.
+int make_tmap(CUtensorMap* map, void* base, int num_blocks, int hkv, int head_dim, bool fp8, bool swizzle = false) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled unavailable (driver too old?)");
   const cuuint64_t chunks = static_cast<cuuint64_t>(num_blocks) * hkv;   // (block, head) chunks of 16 x D
   if (chunks * kBlockSize >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "pool too large for 32-bit TMA coordinates");
   CUresult r;
-  if (fp8) {
+  if (fp8 && swizzle) {
+    // FP8 codes, D = 128: the chunk's 16 rows of 128 bytes land with
+    // 128-byte swizzle (16-byte chunk x of row r at chunk x ^ (r % 8)).
+    cuuint64_t dims[2] = {128, chunks * kBlockSize};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t estr[2] = {1, 1};
+    r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (fp8) {
     // FP8 codes: one (block, head) chunk per copy, 16 rows x D bytes, landing
     // unswizzled ([16 keys][D] bytes); the kernel widens them to f16.
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), chunks * kBlockSize};
@@ -376,12 +390,20 @@ int pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out) {
     }
   }
 
-  // The tensor-core kernel's block maps.
+  // The attention kernels' block maps.
   {
     int rc = make_tmap(&p->tmap_k, p->k, p->num_blocks, p->num_kv_heads, p->head_dim, fp8);
     if (rc) return cleanup(rc);
     rc = make_tmap(&p->tmap_v, p->v, p->num_blocks, p->num_kv_heads, p->head_dim, fp8);
     if (rc) return cleanup(rc);
+    p->dmap_k = p->tmap_k;
+    p->dmap_v = p->tmap_v;
+    if (fp8 && p->head_dim == 128) {
+      rc = make_tmap(&p->dmap_k, p->k, p->num_blocks, p->num_kv_heads, 128, true, true);
+      if (rc) return cleanup(rc);
+      rc = make_tmap(&p->dmap_v, p->v, p->num_blocks, p->num_kv_heads, 128, true, true);
+      if (rc) return cleanup(rc);
+    }
   }
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cleanup(cuda_fail(e, "cudaDeviceSynchronize"));
@@ -605,8 +627,25 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   a.q_box_tokens = 0;
   a.wait_ns = pool->wait_ns;
   a.withhold = pool->withhold;
-  a.k_new = fused ? c.k_new : nullptr;
-  a.v_new = fused ? c.v_new : nullptr;
+  // A fused call over an FP8 pool with tensor-core items appends first, on
+  // the caller's stream, and attends to the pool as a plain call does.  In
+  // the fused form every tensor-core CTA that reads a new row would quantise
+  // it again (correctly rounded divisions by the scale, as the append does,
+  // so that the codes match the pool's) on its producer warp: measured about
+  // seven times the attention's time on recompute-heavy batches.  The result
+  // is the same either way.
+  const bool append_first = fused && pool->elem_bytes == 1 && !pl.tc.empty();
+  const bool in_kernel = fused && !append_first;
+  if (append_first) {
+    PoolView pv = pool->view();
+    rc = timed_launch(pool, 0, c.stream, [&] {
+      return launch_append(pv, pool->k, pool->v, c.block_tables, c.max_blocks, c.num_reqs, c.cu_q_lens, c.q_positions,
+                           c.k_new, c.v_new, c.num_tokens, c.stream);
+    });
+    if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "append launch");
+  }
+  a.k_new = in_kernel ? c.k_new : nullptr;
+  a.v_new = in_kernel ? c.v_new : nullptr;
   a.cu_q_lens = c.cu_q_lens;
   a.num_reqs = c.num_reqs;
   a.num_tokens = c.num_tokens;
@@ -614,7 +653,7 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   a.kn_box_tokens = 0;
   a.runs = reinterpret_cast<const RunDesc*>(wl + pl.off_runs);
   a.run_off = reinterpret_cast<const int32_t*>(wl + pl.off_run_off);
-  if (fused) {
+  if (in_kernel) {
     // Append CTAs of the split-KV launch: about 8 chunks a thread.
     const int64_t chunks = static_cast<int64_t>(c.num_tokens) * pool->num_kv_heads * (pool->head_dim / 8);
     a.n_append_ctas = static_cast<int>(std::min<int64_t>(std::max<int64_t>(1, (chunks + 1023) / 1024),
@@ -624,7 +663,7 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   if (!pl.tc.empty()) {
     rc = make_q_tmap(&tmap_q, c.q, c.num_tokens, c.num_q_heads, pool->head_dim, a.group, &a.q_box_tokens);
     if (rc) return rc;
-    if (fused) {
+    if (in_kernel) {
       rc = make_new_tmap(&tmap_kn, c.k_new, c.num_tokens, pool->num_kv_heads, pool->head_dim, &a.kn_box_tokens);
       if (!rc) rc = make_new_tmap(&tmap_vn, c.v_new, c.num_tokens, pool->num_kv_heads, pool->head_dim, &a.kn_box_tokens);
       if (rc) return rc;
@@ -659,7 +698,8 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   }
   if (dec_launch) {
     rc = timed_launch(pool, 1, dec_stream,
-                      [&] { return launch_decode(a, d_dec, static_cast<int>(pl.decode.size()), dec_stream); });
+                      [&] { return launch_decode(a, &pool->dmap_k, &pool->dmap_v, d_dec, static_cast<int>(pl.decode.size()),
+                                           dec_stream); });
     if (rc != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(rc), "split-KV attention launch");
   }
   if (!pl.tc.empty()) {

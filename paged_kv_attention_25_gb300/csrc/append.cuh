@@ -34,15 +34,13 @@ __device__ __forceinline__ uint32_t quant_e4m3x2(uint32_t w, float scale) {
 //   pool[block_tables[r][p / 16]][g][p % 16][chunk]
 // for the token's request r (binary search of cu_q_lens) and position p
 // (fixed-size blocks in non-contiguous memory, "LLM上下文缓存与状态复用机制的
-// 分析和探索", section 3.1).  Out-of-range positions and block ids are skipped
-// and flagged in the error word.  F8: the chunk is quantised to 8 codes.
-template <typename Idx, bool F8>
-__device__ __forceinline__ void append_chunk(Idx i, void* __restrict__ kp, void* __restrict__ vp, int num_blocks,
-                                             int hkv, int cpr_log2, const int32_t* __restrict__ bt, int max_blocks,
-                                             int num_reqs, const int32_t* __restrict__ cu,
-                                             const int32_t* __restrict__ pos, const uint4* __restrict__ k_new,
-                                             const uint4* __restrict__ v_new, unsigned* err, float k_scale,
-                                             float v_scale) {
+// 分析和探索", section 3.1).  append_dst returns that slot's chunk index, or
+// -1 for an out-of-range position or block id (flagged in the error word).
+template <typename Idx>
+__device__ __forceinline__ int64_t append_dst(Idx i, int num_blocks, int hkv, int cpr_log2,
+                                              const int32_t* __restrict__ bt, int max_blocks, int num_reqs,
+                                              const int32_t* __restrict__ cu, const int32_t* __restrict__ pos,
+                                              unsigned* err) {
   const int chunks_per_row = 1 << cpr_log2;
   const int c = static_cast<int>(i & static_cast<Idx>(chunks_per_row - 1));
   const Idx row = i >> cpr_log2;   // t * hkv + g
@@ -56,22 +54,39 @@ __device__ __forceinline__ void append_chunk(Idx i, void* __restrict__ kp, void*
   const int p = __ldg(pos + t);
   if (p < 0 || p >= max_blocks * kBlockSize) {
     if (c == 0) atomicOr(err, PKV_DEVERR_POSITION);
-    return;
+    return -1;
   }
   const int pb = __ldg(bt + static_cast<int64_t>(lo) * max_blocks + p / kBlockSize);
   if (pb < 0 || pb >= num_blocks) {
     if (c == 0) atomicOr(err, PKV_DEVERR_BLOCK_ID);
-    return;
+    return -1;
   }
-  const int64_t dst = ((static_cast<int64_t>(pb) * hkv + g) * kBlockSize + (p % kBlockSize)) * chunks_per_row + c;
+  return ((static_cast<int64_t>(pb) * hkv + g) * kBlockSize + (p % kBlockSize)) * chunks_per_row + c;
+}
+
+// Stores one chunk (8 bf16 of K and of V) at chunk index dst of the pool.
+// F8: quantised to 8 codes each.
+template <bool F8>
+__device__ __forceinline__ void append_store(void* __restrict__ kp, void* __restrict__ vp, int64_t dst, uint4 kx,
+                                             uint4 vx, float k_scale, float v_scale) {
   if constexpr (F8) {
-    const uint4 kx = __ldg(k_new + i), vx = __ldg(v_new + i);
     static_cast<uint2*>(kp)[dst] = make_uint2(quant_e4m3x4(kx.x, kx.y, k_scale), quant_e4m3x4(kx.z, kx.w, k_scale));
     static_cast<uint2*>(vp)[dst] = make_uint2(quant_e4m3x4(vx.x, vx.y, v_scale), quant_e4m3x4(vx.z, vx.w, v_scale));
   } else {
-    static_cast<uint4*>(kp)[dst] = __ldg(k_new + i);
-    static_cast<uint4*>(vp)[dst] = __ldg(v_new + i);
+    static_cast<uint4*>(kp)[dst] = kx;
+    static_cast<uint4*>(vp)[dst] = vx;
   }
+}
+
+template <typename Idx, bool F8>
+__device__ __forceinline__ void append_chunk(Idx i, void* __restrict__ kp, void* __restrict__ vp, int num_blocks,
+                                             int hkv, int cpr_log2, const int32_t* __restrict__ bt, int max_blocks,
+                                             int num_reqs, const int32_t* __restrict__ cu,
+                                             const int32_t* __restrict__ pos, const uint4* __restrict__ k_new,
+                                             const uint4* __restrict__ v_new, unsigned* err, float k_scale,
+                                             float v_scale) {
+  const int64_t dst = append_dst<Idx>(i, num_blocks, hkv, cpr_log2, bt, max_blocks, num_reqs, cu, pos, err);
+  if (dst >= 0) append_store<F8>(kp, vp, dst, __ldg(k_new + i), __ldg(v_new + i), k_scale, v_scale);
 }
 
 }  // namespace pkv

@@ -863,7 +863,7 @@ static int launch_tc_d(const AttnArgs& a, const CUtensorMap* tk, const CUtensorM
                        const CUtensorMap* tkn, const CUtensorMap* tvn, const WorkItem* items, int n_items,
                        void* stream) {
   const int smem = TcSmem<D>::kTotal;
-  cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = smem_attr_once<tc_attn_kernel<D, F8>>(smem);
   if (e != cudaSuccess) return e;
   tc_attn_kernel<D, F8><<<n_items, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, *tk, *tv, *tq, *tkn,
                                                                                         *tvn, items);

@@ -1,5 +1,6 @@
 // Internal types shared by the host API, the planner and the kernels.
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <string>
@@ -206,7 +207,30 @@ struct AttnCall {
 };
 int paged_attn_call(pkv_pool* pool, const AttnCall& c);
 
-int launch_decode(const AttnArgs& a, const WorkItem* items, int n_items, void* stream);
+// Raises Kernel's dynamic shared-memory limit to `bytes` once per device
+// (devices 0-63; the attribute call costs host time on every launch
+// otherwise, time that lands inside a step whenever the GPU waits on the
+// host).
+#ifdef __CUDACC__
+template <auto Kernel>
+cudaError_t smem_attr_once(int bytes) {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+#endif
+
+// dmap_k / dmap_v: the pool's decode maps (FP8 pools with D = 128: codes
+// viewed as [chunks * 16][D], (D, 16) box, 128-byte swizzle; any valid map
+// otherwise), built with the pool.
+int launch_decode(const AttnArgs& a, const void* dmap_k, const void* dmap_v, const WorkItem* items, int n_items,
+                  void* stream);
 // tmap_q: Q viewed as [T][Hq][D] with a (64, G, q_box_tokens) box (128-byte
 // swizzle), built per call by make_q_tmap.
 // tmap_kn / tmap_vn: the fused call's new K / V rows viewed as [T][Hkv][D] with
