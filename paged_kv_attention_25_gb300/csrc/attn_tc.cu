@@ -589,40 +589,39 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     const uint64_t dqA = make_sdesc_sw128(sQ, 16, 1024), dqB = make_sdesc_sw128(sQ + S::kQ, 16, 1024);
     auto k_desc = [&](int j) { return dk + static_cast<uint64_t>(((j % kKSt) * S::kKV) >> 4); };
     auto v_desc = [&](int j) { return dv + static_cast<uint64_t>(((j % kVSt) * S::kKV) >> 4); };
+    // The warp stays converged through the MMA issue: every lane computes the
+    // same descriptors and executes the issue instructions, predicated so
+    // that only the elected lane issues (one thread's MMAs, in order).  A
+    // lane-0 branch around the issue measured a 129-cycle MMA cadence in the
+    // steady state, against 64 cycles of tensor work per MMA.
+    const uint32_t lead = elect_one();
     // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage, kd).
     auto issue_s = [&](int t, int j, uint64_t kd) {
-      if (lane == 0) {
-        const uint64_t dq = t ? dqB : dqA;
+      const uint64_t dq = t ? dqB : dqA;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int hf = ks / 4, kk = ks % 4;
-          tc_mma(tmem + t * kNK, dq + static_cast<uint64_t>((hf * (kTcRows * 128) + kk * 32) >> 4),
-                 kd + static_cast<uint64_t>((hf * S::kHS + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(&bars[B::kS + t * kKSt + j % kKSt]);
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int hf = ks / 4, kk = ks % 4;
+        tc_mma_lead(lead, tmem + t * kNK, dq + static_cast<uint64_t>((hf * (kTcRows * 128) + kk * 32) >> 4),
+                    kd + static_cast<uint64_t>((hf * S::kHS + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
       }
+      tc_commit_lead(lead, &bars[B::kS + t * kKSt + j % kKSt]);
     };
     // O_t += P_t(j) V(j), P_t(j) from TMEM (over S_t(j)); V(j) in its stage, vd.
     auto issue_pv = [&](int t, int j, uint64_t vd) {
-      if (lane == 0) {
 #pragma unroll
-        for (int ks = 0; ks < kNK / 16; ++ks)
-          tc_mma_ts(tmem + kColO + t * 128, tmem + t * kNK + ks * 8, vd + static_cast<uint64_t>((ks * 2 * S::kGS) >> 4),
-                    idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-        // Only the epilogue waits for PV: earlier PVs are covered by the next
-        // S commit of the tile (the tensor pipe completes one thread's MMAs in order).
-        if (j == ntile_of(t) - 1) tc_commit(&bars[B::kPv + t]);
-      }
+      for (int ks = 0; ks < kNK / 16; ++ks)
+        tc_mma_ts_lead(lead, tmem + kColO + t * 128, tmem + t * kNK + ks * 8,
+                       vd + static_cast<uint64_t>((ks * 2 * S::kGS) >> 4), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+      // Only the epilogue waits for PV: earlier PVs are covered by the next
+      // S commit of the tile (the tensor pipe completes one thread's MMAs in order).
+      if (j == ntile_of(t) - 1) tc_commit_lead(lead, &bars[B::kPv + t]);
     };
     // Each V stage is released once per tile, and only after its tile has
     // landed: an mbarrier does not keep phases apart, so a release for a later
     // use of a stage must never arrive before the current use is complete.
     // (A K stage is freed by the S commits, which follow its landing.)
-    // Only lane 0 issues MMAs and commits; the other lanes meet it again at
-    // the next warp-wide wait, which converges the warp.
-    auto release = [&](int bar) {
-      if (lane == 0) tc_commit(&bars[bar]);
-    };
+    // Commits, like the MMAs, come from the elected lane of the converged warp.
+    auto release = [&](int bar) { tc_commit_lead(lead, &bars[bar]); };
     if (ok && ntiles > 0) {
       if ((ok = mbar_wait_warp(&bars[B::kKFull], 0, s_abort, a.wait_ns))) {
         tc_fence_after();

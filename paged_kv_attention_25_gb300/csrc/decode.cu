@@ -607,37 +607,74 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
 // their wave, with the attention CTAs' shared-memory footprint, kept other
 // work such as a concurrent swap off the SMs.)  The attention items of the
 // launch never read the slots these CTAs write (they take the rows from the
-// new K/V), so nothing orders the two inside the launch.  These CTAs inherit
-// the attention's shared memory, so only 12 warps share an SM: CTA c takes
-// chunks [U*128*c, U*128*(c+1)) (then the same range n CTAs on), and each
-// thread first loads all U of its chunks, then finds their slots, then
-// stores, so that no load waits behind another chunk's lookup or store.
+// new K/V), so nothing orders the two inside the launch.
+//
+// The slot of chunk i is that of append_dst (the same arithmetic, checks and
+// error flags), found in phases.  These CTAs inherit the attention's shared
+// memory, so only 12 warps share an SM, and a chunk's lookup is a chain of
+// dependent loads (request, position, block id); each thread therefore takes
+// U chunks at once and runs each phase over all of them before the next:
+// the new rows, then the tokens' positions, then their requests (one binary
+// search of cu_q_lens per thread; the later chunks' tokens are not smaller,
+// so a short forward walk finds theirs), then the block ids, then the stores.
 template <bool F8>
 __device__ __forceinline__ void append_role(const AttnArgs& a, int c, int n) {
   constexpr int U = 8;
   const int cpr_log2 = a.pool.head_dim == 128 ? 4 : 3;
-  const uint32_t total = static_cast<uint32_t>(a.num_tokens) * a.pool.num_kv_heads << cpr_log2;
+  const int cpr = 1 << cpr_log2;
+  const int hkv = a.pool.num_kv_heads;
+  const uint32_t total = static_cast<uint32_t>(a.num_tokens) * hkv << cpr_log2;
   const uint32_t span = U * blockDim.x;
   const uint4* kn = static_cast<const uint4*>(a.k_new);
   const uint4* vn = static_cast<const uint4*>(a.v_new);
   for (uint32_t base = static_cast<uint32_t>(c) * span + threadIdx.x; base < total;
        base += static_cast<uint32_t>(n) * span) {
     uint4 kx[U], vx[U];
+    int t[U], p[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const uint32_t i = base + u * blockDim.x;
+      t[u] = -1;
       if (i < total) {
         kx[u] = __ldg(kn + i);
         vx[u] = __ldg(vn + i);
+        t[u] = static_cast<int>((i >> cpr_log2) / static_cast<uint32_t>(hkv));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) p[u] = t[u] >= 0 ? __ldg(a.q_positions + t[u]) : -1;
+    int r[U];
+    {
+      int lo = 0, hi = a.num_reqs - 1;   // last r with cu[r] <= t[0] (t[0] >= 0: base < total)
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.cu_q_lens + mid) <= t[0]) lo = mid; else hi = mid - 1;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (t[u] >= 0)
+          while (lo + 1 < a.num_reqs && __ldg(a.cu_q_lens + lo + 1) <= t[u]) ++lo;
+        r[u] = lo;
       }
     }
     int64_t dst[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+      dst[u] = -1;
+      if (t[u] < 0) continue;
       const uint32_t i = base + u * blockDim.x;
-      dst[u] = i < total ? append_dst<uint32_t>(i, a.pool.num_blocks, a.pool.num_kv_heads, cpr_log2, a.block_tables,
-                                                a.max_blocks, a.num_reqs, a.cu_q_lens, a.q_positions, a.pool.err)
-                         : -1;
+      const int ch = static_cast<int>(i & static_cast<uint32_t>(cpr - 1));
+      if (p[u] < 0 || p[u] >= a.max_blocks * kBlockSize) {
+        if (ch == 0) atomicOr(a.pool.err, PKV_DEVERR_POSITION);
+        continue;
+      }
+      const int pb = __ldg(a.block_tables + static_cast<int64_t>(r[u]) * a.max_blocks + p[u] / kBlockSize);
+      if (pb < 0 || pb >= a.pool.num_blocks) {
+        if (ch == 0) atomicOr(a.pool.err, PKV_DEVERR_BLOCK_ID);
+        continue;
+      }
+      const int g = static_cast<int>((i >> cpr_log2) % static_cast<uint32_t>(hkv));
+      dst[u] = ((static_cast<int64_t>(pb) * hkv + g) * kBlockSize + (p[u] % kBlockSize)) * cpr + ch;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u)
