@@ -591,7 +591,10 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
       host = pool->staging.data();
     }
     if (!pl.decode.empty()) std::memcpy(host + pl.off_decode, pl.decode.data(), pl.decode.size() * sizeof(WorkItem));
-    if (!pl.tc.empty()) std::memcpy(host + pl.off_tc, pl.tc.data(), pl.tc.size() * sizeof(WorkItem));
+    if (!pl.tc.empty()) {
+      std::memcpy(host + pl.off_tc, pl.tc.data(), pl.tc.size() * sizeof(WorkItem));
+      std::memset(host + pl.off_tc_next, 0, sizeof(int32_t));
+    }
     if (!pl.merge.empty()) std::memcpy(host + pl.off_merge, pl.merge.data(), pl.merge.size() * sizeof(MergeItem));
     if (!pl.merge_dec.empty()) {
       std::memcpy(host + pl.off_merge_dec, pl.merge_dec.data(), pl.merge_dec.size() * sizeof(MergeItem));
@@ -624,6 +627,8 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   a.part_lse = reinterpret_cast<float*>(ws + pl.off_part_lse);
   a.merge_dec = reinterpret_cast<const MergeItem*>(wl + pl.off_merge_dec);
   a.merge_cnt = reinterpret_cast<int*>(wl + pl.off_merge_cnt);
+  a.tc_next = reinterpret_cast<int*>(wl + pl.off_tc_next);
+  a.tc_ctas = static_cast<int>(std::min<size_t>(pl.tc.size(), static_cast<size_t>(std::max(1, pool->num_sms))));
   a.q_box_tokens = 0;
   a.wait_ns = pool->wait_ns;
   a.withhold = pool->withhold;

@@ -32,6 +32,7 @@
 //
 // TMEM columns: S_A/P_A [0,128)  S_B/P_B [128,256)  O_A [256,384)  O_B [384,512).
 #include <cuda.h>
+#include <climits>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -67,7 +68,7 @@ struct TcSmem {
   static constexpr int kOffK = 2 * kQ;
   static constexpr int kOffV = kOffK + kKSt * kKV;
   static constexpr int kOffBar = kOffV + kVSt * kKV;
-  static constexpr int kNumBars = 4 * kKSt + 3 * kVSt + 9;
+  static constexpr int kNumBars = 3 * kKSt + 3 * kVSt + 17;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kTotal = kOffMisc + 64;
 };
@@ -75,20 +76,54 @@ static_assert(TcSmem<128>::kTotal <= 232448, "shared memory of the D=128 kernel"
 
 template <int KS, int VS>
 struct Bars {
-  // S of query tile t from K stage s ready in TMEM: kS + t * KS + s.  The same
-  // commit frees the K stage once the stage's last S (tile B's, where B has
-  // that key tile) has completed, so K stages need no release of their own.
-  static constexpr int kKFull = 0, kS = KS, kVFull = 3 * KS, kVEmpty = 3 * KS + VS;
-  static constexpr int kQ = 3 * KS + 2 * VS;   // + tile: Q in shared memory (TMA)
-  static constexpr int kP = kQ + 2;            // + tile: P written, O rescaled (128 arrivals)
-  static constexpr int kPv = kQ + 4;           // + tile: the tile's last PV done
-  static constexpr int kDrain = kQ + 6;        // every MMA issued has completed
-  // Fused call: a tile with blocks to patch lands on these (one per K and V
-  // stage) instead; the producer patches the new keys in, then arrives on full.
-  static constexpr int kKLanded = kQ + 7, kVLanded = kQ + 7 + KS;
-  // FP8 pools: + tile: the tile's Q rows converted to f16 (128 arrivals).
-  static constexpr int kQc = kQ + 7 + KS + VS;
+  // The kernel is persistent: one CTA per SM takes work items one after
+  // another, so every barrier below is reused across items and its phases are
+  // counted by running counters, never by an item's own tile index.
+  static constexpr int kKFull = 0, kKEmpty = KS, kKLanded = 2 * KS;
+  static constexpr int kVFull = 3 * KS, kVEmpty = 3 * KS + VS, kVLanded = 3 * KS + 2 * VS;
+  static constexpr int kT = 3 * KS + 3 * VS;
+  static constexpr int kS = kT;            // + tile: S_t of the tile's current key tile in TMEM
+  static constexpr int kP = kT + 2;        // + tile: P written, O rescaled (128 arrivals)
+  static constexpr int kPv = kT + 4;       // + tile: the tile's last PV of the item done
+  static constexpr int kQFull = kT + 6;    // + tile: the item's query tile in shared memory (TMA)
+  static constexpr int kQEmpty = kT + 8;   // + tile: the item's last S MMA of the tile done (Q reusable)
+  static constexpr int kQc = kT + 10;      // + tile: FP8 pools: the tile's Q rows converted to f16 (128 arrivals)
+  static constexpr int kItemFull = kT + 12;    // + slot: next item index written
+  static constexpr int kItemEmpty = kT + 14;   // + slot: every role has read it
+  static constexpr int kDrain = kT + 16;       // every MMA issued has completed
+  static constexpr int kCount = kT + 17;
+  // Roles that read each item index from the ring: the V producer, the MMA
+  // issuer and the eight softmax warps (one arrival per warp).
+  static constexpr int kItemReaders = 10;
 };
+
+// Per-item values every role derives from the work item (scalars, not arrays
+// indexed by tile: those would live in local memory).
+struct TcItem {
+  WorkItem it;
+  int rows0, rows1;       // query rows of tile A / B (tokens x grouped heads)
+  int tok00, tok01;       // first token of tile A / B
+  int ntile0, ntile1;     // key tiles each query tile sees
+  int ntiles, kv_end;     // key tiles of the item and its key range end
+};
+
+__device__ __forceinline__ TcItem tc_item(const WorkItem* items, int w, int G) {
+  TcItem v;
+  v.it = items[w];
+  const WorkItem& it = v.it;
+  v.rows0 = it.q_count * G;
+  v.rows1 = it.q_count2 * G;
+  v.tok00 = it.q_start;
+  v.tok01 = it.q_start + it.q_count;
+  // Key range of each tile from the planner's position bounds, so that the
+  // block-table reads need not wait for the device positions.
+  const int e0 = min(it.kv_end, it.pos_max[0] + 1), e1 = min(it.kv_end, it.pos_max[1] + 1);
+  v.ntile0 = e0 > it.kv_start ? (e0 - it.kv_start + kNK - 1) / kNK : 0;
+  v.ntile1 = e1 > it.kv_start ? (e1 - it.kv_start + kNK - 1) / kNK : 0;
+  v.kv_end = max(it.kv_start, max(e0, e1));
+  v.ntiles = max(v.ntile0, v.ntile1);
+  return v;
+}
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
@@ -167,43 +202,34 @@ template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kn,
-               const __grid_constant__ CUtensorMap tmap_vn, const WorkItem* __restrict__ items) {
+               const __grid_constant__ CUtensorMap tmap_vn, const WorkItem* __restrict__ items, int n_items) {
   using S = TcSmem<D>;
   constexpr int kKSt = S::kKSt, kVSt = S::kVSt;
   using B = Bars<kKSt, kVSt>;
+  static_assert(B::kCount == S::kNumBars, "barrier count");
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {   // swizzle atoms need 1024-byte alignment
     if (threadIdx.x == 0) atomicOr(a.pool.err, PKV_DEVERR_INTERNAL);
     return;
   }
-  // The work item and the launch's error word are read together: every global
-  // round trip before the first K/V copy is paid by every CTA.  Once any wait
-  // in this launch has given up, the remaining CTAs do nothing
+  // Once any wait in this launch has given up, later CTAs do nothing
   // (__syncthreads_or makes the decision the same for every thread).
-  const WorkItem it = items[blockIdx.x];
   const unsigned err0 = *reinterpret_cast<volatile unsigned*>(a.pool.err);
   if (__syncthreads_or((err0 & PKV_DEVERR_TIMEOUT) != 0)) return;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 32);
+  volatile int* s_item = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 40);   // two slots
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.group;
-  const int g = it.kv_head;
   const int Hkv = a.pool.num_kv_heads;
-  // Per-tile values are scalars selected by tile (not arrays: an array indexed
-  // by the warp's tile would live in local memory, and the issuer's loop would
-  // pay its latency).
-  const int rows0 = it.q_count * G, rows1 = it.q_count2 * G;
-  const int tok00 = it.q_start, tok01 = it.q_start + it.q_count;
-  auto rows_of = [&](int t) { return t ? rows1 : rows0; };
-  auto tok0_of = [&](int t) { return t ? tok01 : tok00; };
+  const bool fused = a.k_new != nullptr;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKSt; ++i) {
       mbar_init(&bars[B::kKFull + i], 1);
-      mbar_init(&bars[B::kS + i], 1);
-      mbar_init(&bars[B::kS + kKSt + i], 1);
+      mbar_init(&bars[B::kKEmpty + i], 1);
       mbar_init(&bars[B::kKLanded + i], 1);
     }
     for (int i = 0; i < kVSt; ++i) {
@@ -212,18 +238,21 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       mbar_init(&bars[B::kVLanded + i], 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars[B::kQ + t], 1);
+      mbar_init(&bars[B::kS + t], 1);
       mbar_init(&bars[B::kP + t], 128);
       mbar_init(&bars[B::kPv + t], 1);
+      mbar_init(&bars[B::kQFull + t], 1);
+      mbar_init(&bars[B::kQEmpty + t], 1);
       mbar_init(&bars[B::kQc + t], 128);
+      mbar_init(&bars[B::kItemFull + t], 1);
+      mbar_init(&bars[B::kItemEmpty + t], B::kItemReaders);
     }
     mbar_init(&bars[B::kDrain], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 9 && lane == 0) prefetch_tmap(&tmap_q);
-  const bool fused = a.k_new != nullptr;
   if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
     if (fused) {
@@ -235,316 +264,359 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
-  const int X = (warp >> 2) & 1;            // query tile of a softmax warp (0 = A, 1 = B)
-  const int row = threadIdx.x & 127;        // its row within the tile (TMEM lane)
-  // Key range of each tile from the planner's position bounds, so that the
-  // block-table reads need not wait for the device positions.
-  const int e0 = min(it.kv_end, it.pos_max[0] + 1), e1 = min(it.kv_end, it.pos_max[1] + 1);   // keys each tile sees
-  const int ntile0 = e0 > it.kv_start ? (e0 - it.kv_start + kNK - 1) / kNK : 0;
-  const int ntile1 = e1 > it.kv_start ? (e1 - it.kv_start + kNK - 1) / kNK : 0;
-  const int kv_end = max(it.kv_start, max(e0, e1));
-  auto ntile_of = [&](int t) { return t ? ntile1 : ntile0; };
-  const int ntiles = max(ntile0, ntile1);
-  // Round trips that only need the item are issued before the barrier: the
-  // producer's first two windows of block ids and the softmax threads' query
-  // positions.
-  const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
-  const int blk_first = it.kv_start / kBlockSize;
-  const int blk_end = (kv_end + kBlockSize - 1) / kBlockSize;
-  auto load_window = [&](int w) -> int {   // lane l: id of block blk_first + 32 w + l (-1: none)
-    const int col = blk_first + w * 32 + lane;
-    int pb = -1;
-    if (col < blk_end) {
-      pb = col < a.max_blocks ? __ldg(bt_row + col) : -1;
-      if (pb < 0 || pb >= a.pool.num_blocks) {
-        atomicOr(a.pool.err, PKV_DEVERR_BLOCK_ID);
-        pb = -1;
-      }
-    }
-    return pb;
-  };
-  int ids_cur = -1, ids_next = -1;
-  int run_b = 0, run_e = 0;   // fused call: the request's runs of new positions
-  if (warp == 8 || warp == 10) {
-    ids_cur = load_window(0);
-    ids_next = load_window(1);
-    if (fused) {
-      run_b = __ldg(a.run_off + it.req);
-      run_e = __ldg(a.run_off + it.req + 1);
-    }
-  }
-  int qpos = -1;
-  if (warp < 8 && row < rows_of(X)) qpos = __ldg(a.q_positions + tok0_of(X) + row / G);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-
   const uint32_t sQ = smem_u32(smem + S::kOffQ);
   const uint32_t sK = smem_u32(smem + S::kOffK);
   const uint32_t sV = smem_u32(smem + S::kOffV);
 
+  // Item r of this CTA is in ring slot r % 2.  take_item: every reading role
+  // waits for it, reads it and releases the slot (one arrival per warp);
+  // the index n_items means no more items.
+  auto take_item = [&](int r, int& w) -> bool {
+    const int slot = r & 1;
+    if (!mbar_wait_warp(&bars[B::kItemFull + slot], (r >> 1) & 1, s_abort, a.wait_ns)) return false;
+    w = s_item[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[B::kItemEmpty + slot]);
+    return true;
+  };
+
   if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ producers: warp 8 K, warp 10 V
-    constexpr int kBlk = kNK / kBlockSize;   // blocks per key tile (8)
-    constexpr int kWin = 32 / kBlk;          // key tiles per window of 32 block ids
-    // Block ids are read a window ahead: lane l holds the id of block
-    // (first block of the item) + 32 w + l, and the next window is in flight
-    // while the current one is used.
-    int win = 0;
-    // (block, head) chunk index of this lane's block in tile j (-1: none).
-    auto block_chunk = [&](int j) -> int {
-      if (j / kWin != win) {
-        win = j / kWin;
-        ids_cur = ids_next;
-        ids_next = load_window(win + 1);
-      }
-      const int key0 = it.kv_start + j * kNK;
-      const int nblk = (min(kNK, kv_end - key0) + kBlockSize - 1) / kBlockSize;
-      int pb = __shfl_sync(0xffffffffu, ids_cur, (j % kWin) * kBlk + (lane % kBlk));
-      if (lane >= nblk) pb = -1;
-      return pb < 0 ? -1 : pb * Hkv + g;
-    };
-    // Fused call: the tokens of this step are not in the pool yet (the
-    // launch beside this one writes them), so their keys and values come from
-    // the new rows.  Run r says positions [p0, p0 + n) are tokens [t0, t0 + n).
-    auto run_at = [&](int r) {
-      const int4 v = __ldg(reinterpret_cast<const int4*>(a.runs) + r);
-      return RunDesc{v.x, v.y, v.z, v.w};
-    };
-    // Overwrites, in a landed stage, every slot of block `blk` (first key bp)
-    // that holds a new key below kv_end with that token's row (swizzled as
-    // the TMA lands it: 16-byte chunk c of row r at chunk c ^ (r % 8) of its
-    // 128-byte line).
-    auto patch_block = [&](uint8_t* blk, int bp, bool is_k) {
-      int tok = -1;
-      const int p = bp + (lane & 15);
-      if (p < kv_end) {
-        for (int r = run_b; r < run_e; ++r) {
-          const RunDesc rd = run_at(r);
-          if (rd.p0 > p) break;
-          if (p < rd.p0 + rd.n) {
-            tok = rd.t0 + (p - rd.p0);
-            break;
-          }
-        }
-      }
-      const uint8_t* src = static_cast<const uint8_t*>(is_k ? a.k_new : a.v_new);
-      constexpr int kCpr = D / 8;   // 16-byte chunks per row
-#pragma unroll
-      for (int idx = lane; idx < kBlockSize * kCpr; idx += 32) {
-        const int rr = idx / kCpr, c = idx % kCpr;
-        const int t = __shfl_sync(0xffffffffu, tok, rr);
-        if (t >= 0) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + ((static_cast<int64_t>(t) * Hkv + g) * D) * 2 + c * 16);
-          *reinterpret_cast<uint4*>(blk + (rr / 8) * S::kGS + (c / 8) * S::kHS + (rr % 8) * 128 +
-                                    (((c % 8) ^ (rr % 8)) * 16)) = v;
-        }
-      }
-    };
-    uint32_t landed_par = 0;   // bit st: parity of this warp's next wait on landed barrier st
-    auto load = [&](int j, int y, bool is_k) -> bool {
-      const int nst = is_k ? kKSt : kVSt;
-      const int st = j % nst;
-      const uint32_t ph = (j / nst) & 1;
-      uint64_t* full = &bars[(is_k ? B::kKFull : B::kVFull) + st];
-      // Where lane l's block (keys bp .. bp + 15) comes from: 1 the pool; 2
-      // the new rows, tokens src .. src + 15 (every key below kv_end belongs
-      // to one run); 3 the pool, then its new keys patched in; 0 nothing.
-      int cls = y >= 0 ? 1 : 0, src = -1;
-      if (fused) {
-        const int bp = it.kv_start + j * kNK + lane * kBlockSize;
-        if (lane < kBlk && bp < kv_end) {
-          const int live = min(bp + kBlockSize, kv_end);
-          int nnew = 0, nrun = 0;
-          for (int r = run_b; r < run_e; ++r) {
-            const RunDesc rd = run_at(r);
-            if (rd.p0 >= live) break;
-            const int lo = max(bp, rd.p0), hi = min(live, rd.p0 + rd.n);
-            if (lo < hi) {
-              nnew += hi - lo;
-              if (nrun++ == 0) src = rd.t0 + (bp - rd.p0);
-            }
-          }
-          if (nnew == live - bp && nrun == 1) cls = 2;
-          else if (nnew > 0 && y >= 0) cls = 3;
-        }
-      }
-      const bool patch = __any_sync(0xffffffffu, cls == 3);
-      // A pool box is a whole block; a box of new rows holds kn_box_tokens
-      // tokens (8, fewer only when the batch has fewer tokens).
-      const uint32_t my_bytes = cls == 2   ? 2u * a.kn_box_tokens * S::kHalves * 128u
-                                : cls != 0 ? static_cast<uint32_t>(S::kHalves * kBlockSize * 128)
-                                           : 0u;
-      const uint32_t bytes = __reduce_add_sync(0xffffffffu, my_bytes);
-      // Free stage: V after the release that follows its tile's PVs; K after
-      // the S commit of the tile that last read it (j - nst), i.e. tile B's
-      // where B reaches that key tile, else tile A's.  Before a stage's first
-      // use, parity 1 of a fresh barrier passes at once.
-      const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile1 ? kKSt : 0) + st : B::kVEmpty + st;
-      if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
-      // Test hook: CTA 0 never issues its first K tile, so that the issuer's
-      // bounded wait for it runs out.
-      if (a.withhold == 2 && is_k && j == 0 && blockIdx.x == 0) return true;
-      uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
-      uint64_t* bar = patch ? landed : full;
-      if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-      __syncwarp();
-      uint8_t* dst = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + lane * S::kBlkBytes;
-      if (cls == 2) {
-        // Two 8-token boxes of the new rows, one per 8-key group of the block.
-        const CUtensorMap* m = is_k ? &tmap_kn : &tmap_vn;
-        if constexpr (D == 128) {
-          tma_load_4d(dst, m, 0, g, src, 0, bar);
-          tma_load_4d(dst + S::kGS, m, 0, g, src + 8, 0, bar);
-        } else {
-          tma_load_3d(dst, m, 0, g, src, bar);
-          tma_load_3d(dst + S::kGS, m, 0, g, src + 8, bar);
-        }
-      } else if (cls != 0) {
-        if constexpr (D == 128)
-          tma_load_4d(dst, is_k ? &tmap_k : &tmap_v, 0, 0, 0, 2 * y, bar);
-        else
-          tma_load_2d(dst, is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, bar);
-      }
-      if (patch) {
-        const uint32_t par = (landed_par >> st) & 1u;
-        landed_par ^= 1u << st;
-        if (!mbar_wait_warp(landed, par, s_abort, a.wait_ns)) {
-          (void)mbar_wait(landed, par, nullptr, a.wait_ns);   // let this tile's copies land
-          return false;
-        }
-        uint8_t* stage = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV;
-        uint32_t mm = __ballot_sync(0xffffffffu, cls == 3);
-        while (mm) {
-          const int b = __ffs(mm) - 1;
-          mm &= mm - 1;
-          patch_block(stage + b * S::kBlkBytes, it.kv_start + j * kNK + b * kBlockSize, is_k);
-        }
-        fence_proxy_async_smem();   // the patched slots are read by the tensor cores
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full);
-      }
-      return true;
-    };
-    // K and V stream from two warps, so that neither waits behind the
-    // other's free stages: a K stage frees when its S MMAs finish, a V stage
-    // only when both tiles' PV on it have finished.
-    // FP8 pools: tile j's codes land (on landed barrier j % nst) in the
-    // upper half of its stage; the warp widens the stage in place to f16,
-    // patches the fused call's new rows in (quantised as the append stores
-    // them) and arrives on full.  Copies run one tile ahead of the widening.
-    auto load_f8 = [&](int j, int y, bool is_k) -> bool {
-      const int nst = is_k ? kKSt : kVSt;
-      const int st = j % nst;
-      const uint32_t ph = (j / nst) & 1;
-      const uint32_t bytes = static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, y >= 0))) * (kBlockSize * D);
-      const int empty = is_k ? B::kS + (j >= nst && j - nst < ntile1 ? kKSt : 0) + st : B::kVEmpty + st;
-      if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
-      if (a.withhold == 2 && is_k && j == 0 && blockIdx.x == 0) return true;   // test hook (above)
-      uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
-      if (lane == 0) mbar_arrive_expect_tx(landed, bytes);
-      __syncwarp();
-      if (y >= 0)
-        tma_load_2d(smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + S::kKV / 2 + lane * (kBlockSize * D),
-                    is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, landed);
-      return true;
-    };
-    // The fused call's new rows of block b of a widened stage: each new key's
-    // row, quantised to codes (as the append stores it) and widened to f16.
-    auto patch_block_f8 = [&](uint8_t* stage, int b, int bp, bool is_k) {
-      int tok = -1;
-      const int p = bp + (lane & 15);
-      if (p < kv_end) {
-        for (int r = run_b; r < run_e; ++r) {
-          const RunDesc rd = run_at(r);
-          if (rd.p0 > p) break;
-          if (p < rd.p0 + rd.n) {
-            tok = rd.t0 + (p - rd.p0);
-            break;
-          }
-        }
-      }
-      const uint8_t* src = static_cast<const uint8_t*>(is_k ? a.k_new : a.v_new);
-      const float sc = is_k ? a.pool.k_scale : a.pool.v_scale;
-      constexpr int kC8 = D / 8;   // 8-element chunks per row
-#pragma unroll
-      for (int idx = lane; idx < kBlockSize * kC8; idx += 32) {
-        const int rr = idx / kC8, c = idx % kC8;
-        const int t = __shfl_sync(0xffffffffu, tok, rr);
-        if (t >= 0) {
-          const uint4 x = *reinterpret_cast<const uint4*>(src + ((static_cast<int64_t>(t) * Hkv + g) * D) * 2 + c * 16);
-          const uint32_t c0 = quant_e4m3x4(x.x, x.y, sc), c1 = quant_e4m3x4(x.z, x.w, sc);
-          const uint4 h = make_uint4(e4m3x2_to_f16x2(c0), e4m3x2_to_f16x2(c0 >> 16), e4m3x2_to_f16x2(c1),
-                                     e4m3x2_to_f16x2(c1 >> 16));
-          const int r = b * kBlockSize + rr, hf = c / 8, cw = c % 8, r8 = r % 8;
-          *reinterpret_cast<uint4*>(stage + (r / 8) * S::kGS + hf * S::kHS + r8 * 128 + ((cw ^ r8) * 16)) = h;
-        }
-      }
-    };
-    auto finish_f8 = [&](int j, bool is_k) -> bool {
-      const int nst = is_k ? kKSt : kVSt;
-      const int st = j % nst;
-      uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
-      if (!mbar_wait_warp(landed, (j / nst) & 1, s_abort, a.wait_ns)) return false;
-      uint8_t* stage = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV;
-      widen_stage<D>(stage, lane);
-      if (fused) {
-        __syncwarp();
-        const int key0 = it.kv_start + j * kNK;
-        const int bp = key0 + lane * kBlockSize;
-        bool has_new = false;
-        if (lane < kBlk && bp < kv_end) {
-          const int live = min(bp + kBlockSize, kv_end);
-          for (int r = run_b; r < run_e; ++r) {
-            const RunDesc rd = run_at(r);
-            if (rd.p0 >= live) break;
-            if (max(bp, rd.p0) < min(live, rd.p0 + rd.n)) has_new = true;
-          }
-        }
-        uint32_t mm = __ballot_sync(0xffffffffu, has_new);
-        while (mm) {
-          const int b = __ffs(mm) - 1;
-          mm &= mm - 1;
-          patch_block_f8(stage, b, key0 + b * kBlockSize, is_k);
-        }
-      }
-      fence_proxy_async_smem();   // the widened rows are read by the tensor cores
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[(is_k ? B::kKFull : B::kVFull) + st]);
-      return true;
-    };
+    // Warp 8 also claims the CTA's items (a launch-wide counter: a CTA that
+    // starts late, beside the split-KV kernel, just takes fewer) and loads
+    // each item's query tiles.  K and V stream from two warps, so that
+    // neither waits behind the other's free stages: a K stage frees when its
+    // key tile's S MMAs finish, a V stage when both tiles' PVs on it finish.
     const bool is_k = warp == 8;
     const int nst = is_k ? kKSt : kVSt;
+    constexpr int kBlk = kNK / kBlockSize;   // blocks per key tile (8)
+    constexpr int kWin = 32 / kBlk;          // key tiles per window of 32 block ids
+    constexpr int kNoBlock = INT_MIN;        // past the item's blocks
+    uint32_t landed_par = 0;   // bit st: parity of this warp's next wait on landed barrier st
+    int cnt = 0;               // K (or V) tiles this warp has issued in the launch
+    int fin = 0;               // FP8: tiles widened and handed to the issuer
+    int nq = 0;                // warp 8: items whose query tiles it has issued
     bool ok = true;
-    int nl = 0;   // tiles whose copies this warp has issued
-    if constexpr (F8) {
-      int nf = 0;   // tiles widened and handed to the issuer
-      for (int j = 0; j < ntiles; ++j) {
-        if (!(ok = load_f8(j, block_chunk(j), is_k))) break;
-        nl = j + 1;
-        if (j >= 1) {
-          if (!(ok = finish_f8(j - 1, is_k))) break;
-          nf = j;
+    for (int r = 0; ok; ++r) {
+      int w = n_items;
+      if (is_k) {
+        const int slot = r & 1;
+        if (!(ok = mbar_wait_warp(&bars[B::kItemEmpty + slot], ((r >> 1) & 1) ^ 1, s_abort, a.wait_ns))) break;
+        int v = 0;
+        if (lane == 0) v = atomicAdd(a.tc_next, 1);
+        w = min(__shfl_sync(0xffffffffu, v, 0), n_items);
+        if (lane == 0) {
+          s_item[slot] = w;
+          mbar_arrive(&bars[B::kItemFull + slot]);
+        }
+        __syncwarp();
+      } else if (!(ok = take_item(r, w))) {
+        break;
+      }
+      if (w >= n_items) break;
+      const TcItem iv = tc_item(items, w, G);
+      const WorkItem& it = iv.it;
+      const int g = it.kv_head;
+      const int kv_end = iv.kv_end;
+      if (is_k) {
+        // Query tiles, each once the previous item's last S MMA on it has
+        // completed.  Rows (token, head) of a tile land as [half][row][64
+        // columns]; rows past the tile are other tokens' rows or zeros,
+        // computed and never stored.
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!(ok = mbar_wait_warp(&bars[B::kQEmpty + t], (r & 1) ^ 1, s_abort, a.wait_ns))) break;
+          if (lane == 0) {
+            if ((t ? iv.rows1 : iv.rows0) > 0) {
+              mbar_arrive_expect_tx(&bars[B::kQFull + t], static_cast<uint32_t>(D * 2 * G * a.q_box_tokens));
+              uint8_t* qt = smem + S::kOffQ + t * S::kQ;
+#pragma unroll
+              for (int hf = 0; hf < S::kHalves; ++hf)
+                tma_load_3d(qt + hf * (kTcRows * 128), &tmap_q, hf * 64, g * G, t ? iv.tok01 : iv.tok00,
+                            &bars[B::kQFull + t]);
+            } else {
+              mbar_arrive(&bars[B::kQFull + t]);
+            }
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        nq = r + 1;
+      }
+      // Block ids are read a window ahead: lane l holds the id of block
+      // (first block of the item) + 32 w + l, and the next window is in
+      // flight while the current one is used.  A window's ids are checked
+      // (bad ids flagged) when it becomes current.
+      const int32_t* bt_row = a.block_tables + static_cast<int64_t>(it.req) * a.max_blocks;
+      const int blk_first = it.kv_start / kBlockSize;
+      const int blk_end = (kv_end + kBlockSize - 1) / kBlockSize;
+      auto load_window = [&](int wi) -> int {   // lane l: raw id of block blk_first + 32 wi + l
+        const int col = blk_first + wi * 32 + lane;
+        if (col >= blk_end) return kNoBlock;
+        return col < a.max_blocks ? __ldg(bt_row + col) : -1;
+      };
+      auto check_window = [&](int pb) -> int {   // the id, or -1 for none (an invalid id is flagged)
+        if (pb == kNoBlock) return -1;
+        if (pb < 0 || pb >= a.pool.num_blocks) {
+          atomicOr(a.pool.err, PKV_DEVERR_BLOCK_ID);
+          return -1;
+        }
+        return pb;
+      };
+      int win = 0;
+      int ids_cur = load_window(0), ids_next = load_window(1);
+      int run_b = 0, run_e = 0;   // fused call: the request's runs of new positions
+      if (fused) {
+        run_b = __ldg(a.run_off + it.req);
+        run_e = __ldg(a.run_off + it.req + 1);
+      }
+      ids_cur = check_window(ids_cur);
+      // (block, head) chunk index of this lane's block in key tile j (-1: none).
+      auto block_chunk = [&](int j) -> int {
+        if (j / kWin != win) {
+          win = j / kWin;
+          ids_cur = check_window(ids_next);
+          ids_next = load_window(win + 1);
+        }
+        const int key0 = it.kv_start + j * kNK;
+        const int nblk = (min(kNK, kv_end - key0) + kBlockSize - 1) / kBlockSize;
+        int pb = __shfl_sync(0xffffffffu, ids_cur, (j % kWin) * kBlk + (lane % kBlk));
+        if (lane >= nblk) pb = -1;
+        return pb < 0 ? -1 : pb * Hkv + g;
+      };
+      // Fused call: the tokens of this step are not in the pool yet (the
+      // launch beside this one writes them), so their keys and values come from
+      // the new rows.  Run r says positions [p0, p0 + n) are tokens [t0, t0 + n).
+      auto run_at = [&](int r) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(a.runs) + r);
+        return RunDesc{v.x, v.y, v.z, v.w};
+      };
+      // Overwrites, in a landed stage, every slot of block `blk` (first key bp)
+      // that holds a new key below kv_end with that token's row (swizzled as
+      // the TMA lands it: 16-byte chunk c of row r at chunk c ^ (r % 8) of its
+      // 128-byte line).
+      auto patch_block = [&](uint8_t* blk, int bp, bool is_k) {
+        int tok = -1;
+        const int p = bp + (lane & 15);
+        if (p < kv_end) {
+          for (int r = run_b; r < run_e; ++r) {
+            const RunDesc rd = run_at(r);
+            if (rd.p0 > p) break;
+            if (p < rd.p0 + rd.n) {
+              tok = rd.t0 + (p - rd.p0);
+              break;
+            }
+          }
+        }
+        const uint8_t* src = static_cast<const uint8_t*>(is_k ? a.k_new : a.v_new);
+        constexpr int kCpr = D / 8;   // 16-byte chunks per row
+#pragma unroll
+        for (int idx = lane; idx < kBlockSize * kCpr; idx += 32) {
+          const int rr = idx / kCpr, c = idx % kCpr;
+          const int t = __shfl_sync(0xffffffffu, tok, rr);
+          if (t >= 0) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + ((static_cast<int64_t>(t) * Hkv + g) * D) * 2 + c * 16);
+            *reinterpret_cast<uint4*>(blk + (rr / 8) * S::kGS + (c / 8) * S::kHS + (rr % 8) * 128 +
+                                      (((c % 8) ^ (rr % 8)) * 16)) = v;
+          }
+        }
+      };
+      auto load = [&](int j, int gk, int y) -> bool {
+        const int st = gk % nst;
+        const uint32_t ph = (gk / nst) & 1;
+        uint64_t* full = &bars[(is_k ? B::kKFull : B::kVFull) + st];
+        // Where lane l's block (keys bp .. bp + 15) comes from: 1 the pool; 2
+        // the new rows, tokens src .. src + 15 (every key below kv_end belongs
+        // to one run); 3 the pool, then its new keys patched in; 0 nothing.
+        int cls = y >= 0 ? 1 : 0, src = -1;
+        if (fused) {
+          const int bp = it.kv_start + j * kNK + lane * kBlockSize;
+          if (lane < kBlk && bp < kv_end) {
+            const int live = min(bp + kBlockSize, kv_end);
+            int nnew = 0, nrun = 0;
+            for (int r = run_b; r < run_e; ++r) {
+              const RunDesc rd = run_at(r);
+              if (rd.p0 >= live) break;
+              const int lo = max(bp, rd.p0), hi = min(live, rd.p0 + rd.n);
+              if (lo < hi) {
+                nnew += hi - lo;
+                if (nrun++ == 0) src = rd.t0 + (bp - rd.p0);
+              }
+            }
+            if (nnew == live - bp && nrun == 1) cls = 2;
+            else if (nnew > 0 && y >= 0) cls = 3;
+          }
+        }
+        const bool patch = __any_sync(0xffffffffu, cls == 3);
+        // A pool box is a whole block; a box of new rows holds kn_box_tokens
+        // tokens (8, fewer only when the batch has fewer tokens).
+        const uint32_t my_bytes = cls == 2   ? 2u * a.kn_box_tokens * S::kHalves * 128u
+                                  : cls != 0 ? static_cast<uint32_t>(S::kHalves * kBlockSize * 128)
+                                             : 0u;
+        const uint32_t bytes = __reduce_add_sync(0xffffffffu, my_bytes);
+        // Free stage: released by the issuer after the last MMA that reads it.
+        // Before a stage's first use, parity 1 of a fresh barrier passes at once.
+        const int empty = (is_k ? B::kKEmpty : B::kVEmpty) + st;
+        if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
+        // Test hook: CTA 0 never issues its first K tile, so that the issuer's
+        // bounded wait for it runs out.
+        if (a.withhold == 2 && is_k && gk == 0 && blockIdx.x == 0) return true;
+        uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
+        uint64_t* bar = patch ? landed : full;
+        if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+        __syncwarp();
+        uint8_t* dst = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + lane * S::kBlkBytes;
+        if (cls == 2) {
+          // Two 8-token boxes of the new rows, one per 8-key group of the block.
+          const CUtensorMap* m = is_k ? &tmap_kn : &tmap_vn;
+          if constexpr (D == 128) {
+            tma_load_4d(dst, m, 0, g, src, 0, bar);
+            tma_load_4d(dst + S::kGS, m, 0, g, src + 8, 0, bar);
+          } else {
+            tma_load_3d(dst, m, 0, g, src, bar);
+            tma_load_3d(dst + S::kGS, m, 0, g, src + 8, bar);
+          }
+        } else if (cls != 0) {
+          if constexpr (D == 128)
+            tma_load_4d(dst, is_k ? &tmap_k : &tmap_v, 0, 0, 0, 2 * y, bar);
+          else
+            tma_load_2d(dst, is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, bar);
+        }
+        if (patch) {
+          const uint32_t par = (landed_par >> st) & 1u;
+          landed_par ^= 1u << st;
+          if (!mbar_wait_warp(landed, par, s_abort, a.wait_ns)) {
+            (void)mbar_wait(landed, par, nullptr, a.wait_ns);   // let this tile's copies land
+            return false;
+          }
+          uint8_t* stage = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV;
+          uint32_t mm = __ballot_sync(0xffffffffu, cls == 3);
+          while (mm) {
+            const int b = __ffs(mm) - 1;
+            mm &= mm - 1;
+            patch_block(stage + b * S::kBlkBytes, it.kv_start + j * kNK + b * kBlockSize, is_k);
+          }
+          fence_proxy_async_smem();   // the patched slots are read by the tensor cores
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full);
+        }
+        return true;
+      };
+      // FP8 pools: the codes of the warp's tile gk (of the launch) land, on
+      // landed barrier gk % nst, in the upper half of its stage; the warp widens the stage in place to f16,
+      // patches the fused call's new rows in (quantised as the append stores
+      // them) and arrives on full.  Copies run one tile ahead of the widening.
+      auto load_f8 = [&](int gk, int y) -> bool {
+        const int st = gk % nst;
+        const uint32_t ph = (gk / nst) & 1;
+        const uint32_t bytes = static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, y >= 0))) * (kBlockSize * D);
+        const int empty = (is_k ? B::kKEmpty : B::kVEmpty) + st;
+        if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
+        if (a.withhold == 2 && is_k && gk == 0 && blockIdx.x == 0) return true;   // test hook (above)
+        uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
+        if (lane == 0) mbar_arrive_expect_tx(landed, bytes);
+        __syncwarp();
+        if (y >= 0)
+          tma_load_2d(smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + S::kKV / 2 + lane * (kBlockSize * D),
+                      is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, landed);
+        return true;
+      };
+      // The fused call's new rows of block b of a widened stage: each new key's
+      // row, quantised to codes (as the append stores it) and widened to f16.
+      auto patch_block_f8 = [&](uint8_t* stage, int b, int bp, bool is_k) {
+        int tok = -1;
+        const int p = bp + (lane & 15);
+        if (p < kv_end) {
+          for (int r = run_b; r < run_e; ++r) {
+            const RunDesc rd = run_at(r);
+            if (rd.p0 > p) break;
+            if (p < rd.p0 + rd.n) {
+              tok = rd.t0 + (p - rd.p0);
+              break;
+            }
+          }
+        }
+        const uint8_t* src = static_cast<const uint8_t*>(is_k ? a.k_new : a.v_new);
+        const float sc = is_k ? a.pool.k_scale : a.pool.v_scale;
+        constexpr int kC8 = D / 8;   // 8-element chunks per row
+#pragma unroll
+        for (int idx = lane; idx < kBlockSize * kC8; idx += 32) {
+          const int rr = idx / kC8, c = idx % kC8;
+          const int t = __shfl_sync(0xffffffffu, tok, rr);
+          if (t >= 0) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + ((static_cast<int64_t>(t) * Hkv + g) * D) * 2 + c * 16);
+            const uint32_t c0 = quant_e4m3x4(x.x, x.y, sc), c1 = quant_e4m3x4(x.z, x.w, sc);
+            const uint4 h = make_uint4(e4m3x2_to_f16x2(c0), e4m3x2_to_f16x2(c0 >> 16), e4m3x2_to_f16x2(c1),
+                                       e4m3x2_to_f16x2(c1 >> 16));
+            const int r = b * kBlockSize + rr, hf = c / 8, cw = c % 8, r8 = r % 8;
+            *reinterpret_cast<uint4*>(stage + (r / 8) * S::kGS + hf * S::kHS + r8 * 128 + ((cw ^ r8) * 16)) = h;
+          }
+        }
+      };
+      auto finish_f8 = [&](int j, int gk) -> bool {
+        const int st = gk % nst;
+        uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
+        if (!mbar_wait_warp(landed, (gk / nst) & 1, s_abort, a.wait_ns)) return false;
+        uint8_t* stage = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV;
+        widen_stage<D>(stage, lane);
+        if (fused) {
+          __syncwarp();
+          const int key0 = it.kv_start + j * kNK;
+          const int bp = key0 + lane * kBlockSize;
+          bool has_new = false;
+          if (lane < kBlk && bp < kv_end) {
+            const int live = min(bp + kBlockSize, kv_end);
+            for (int r = run_b; r < run_e; ++r) {
+              const RunDesc rd = run_at(r);
+              if (rd.p0 >= live) break;
+              if (max(bp, rd.p0) < min(live, rd.p0 + rd.n)) has_new = true;
+            }
+          }
+          uint32_t mm = __ballot_sync(0xffffffffu, has_new);
+          while (mm) {
+            const int b = __ffs(mm) - 1;
+            mm &= mm - 1;
+            patch_block_f8(stage, b, key0 + b * kBlockSize, is_k);
+          }
+        }
+        fence_proxy_async_smem();   // the widened rows are read by the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[(is_k ? B::kKFull : B::kVFull) + st]);
+        return true;
+      };
+      if constexpr (F8) {
+        // Copies run one tile ahead of the widening (within the item).
+        for (int j = 0; j < iv.ntiles; ++j) {
+          if (!(ok = load_f8(cnt, block_chunk(j)))) break;
+          ++cnt;
+          if (j >= 1) {
+            if (!(ok = finish_f8(j - 1, cnt - 2))) break;
+            fin = cnt - 1;
+          }
+        }
+        if (ok && iv.ntiles > 0 && (ok = finish_f8(iv.ntiles - 1, cnt - 1))) fin = cnt;
+      } else {
+        for (int j = 0; j < iv.ntiles; ++j) {
+          if (!(ok = load(j, cnt, block_chunk(j)))) break;
+          ++cnt;
         }
       }
-      if (ok && ntiles > 0 && (ok = finish_f8(ntiles - 1, is_k))) nf = ntiles;
-      if (!ok) {   // gave up: flag it and let copies already issued land
-        if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
-        *s_abort = 1;
-        for (int i = nf; i < nl; ++i)
+    }
+    if (!ok) {   // gave up: flag it and let copies already issued land
+      if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
+      *s_abort = 1;
+      if constexpr (F8) {
+        for (int i = fin; i < cnt; ++i)
           (void)mbar_wait(&bars[(is_k ? B::kKLanded : B::kVLanded) + i % nst], (i / nst) & 1, nullptr, a.wait_ns);
-      }
-    } else {
-      for (int j = 0; j < ntiles; ++j) {
-        if (!(ok = load(j, block_chunk(j), is_k))) break;
-        nl = j + 1;
-      }
-      if (!ok) {   // gave up: flag it and let copies already issued land
-        if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
-        *s_abort = 1;
-        for (int i = max(0, nl - nst); i < nl; ++i)
+      } else {
+        for (int i = max(0, cnt - nst); i < cnt; ++i)
           (void)mbar_wait(&bars[(is_k ? B::kKFull : B::kVFull) + i % nst], (i / nst) & 1, nullptr, a.wait_ns);
+      }
+      if (is_k && nq > 0) {
+        for (int t = 0; t < 2; ++t) (void)mbar_wait(&bars[B::kQFull + t], (nq - 1) & 1, nullptr, a.wait_ns);
       }
     }
   } else if (warp == 9) {
@@ -558,45 +630,18 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     // apart (leading offset) and 8-key groups kGS apart (stride offset).
     const uint64_t dk = make_sdesc_sw128(sK, 16, S::kGS);
     const uint64_t dv = make_sdesc_sw128(sV, S::kHS, S::kGS);
-    // Both query tiles by TMA, issued here rather than before the CTA barrier:
-    // the copy's first use of the per-call tensor map takes a few thousand
-    // cycles, which the producers' first K/V copies need not wait for.  Rows
-    // (token, head) of a tile land as [half][row][64 columns] (rows past the
-    // tile are other tokens' rows or zeros, computed and never stored).
-    if (lane == 0) {
-      const uint32_t qbytes = static_cast<uint32_t>(D * 2 * G * a.q_box_tokens);
-      for (int t = 0; t < 2; ++t) {
-        if (rows_of(t) > 0) {
-          mbar_arrive_expect_tx(&bars[B::kQ + t], qbytes);
-          uint8_t* qt = smem + S::kOffQ + t * S::kQ;
-#pragma unroll
-          for (int hf = 0; hf < S::kHalves; ++hf)
-            tma_load_3d(qt + hf * (kTcRows * 128), &tmap_q, hf * 64, g * G, tok0_of(t), &bars[B::kQ + t]);
-        } else {
-          mbar_arrive(&bars[B::kQ + t]);
-        }
-      }
-    }
-    __syncwarp();
-    // FP8 pools: wait for the softmax warps' f16 conversion of the tiles instead.
-    constexpr int kQReady = F8 ? B::kQc : B::kQ;
-    bool ok = mbar_wait_warp(&bars[kQReady], 0, s_abort, a.wait_ns) &&
-              mbar_wait_warp(&bars[kQReady + 1], 0, s_abort, a.wait_ns);
-    const int last_nkeys = ntiles > 0 ? min(kNK, kv_end - (it.kv_start + (ntiles - 1) * kNK)) : kNK;
-    // Descriptors that do not change in the loop are built here, and each
-    // step's stage descriptors once per step (not per tile): work between
-    // MMAs in the issuing thread measurably slows their issue.
     const uint64_t dqA = make_sdesc_sw128(sQ, 16, 1024), dqB = make_sdesc_sw128(sQ + S::kQ, 16, 1024);
-    auto k_desc = [&](int j) { return dk + static_cast<uint64_t>(((j % kKSt) * S::kKV) >> 4); };
-    auto v_desc = [&](int j) { return dv + static_cast<uint64_t>(((j % kVSt) * S::kKV) >> 4); };
+    auto k_desc = [&](int gk) { return dk + static_cast<uint64_t>(((gk % kKSt) * S::kKV) >> 4); };
+    auto v_desc = [&](int gv) { return dv + static_cast<uint64_t>(((gv % kVSt) * S::kKV) >> 4); };
     // The warp stays converged through the MMA issue: every lane computes the
     // same descriptors and executes the issue instructions, predicated so
     // that only the elected lane issues (one thread's MMAs, in order).  A
     // lane-0 branch around the issue measured a 129-cycle MMA cadence in the
     // steady state, against 64 cycles of tensor work per MMA.
     const uint32_t lead = elect_one();
-    // S_t(j) = Q_t K(j)^T into tile t's S columns (K(j) is in its stage, kd).
-    auto issue_s = [&](int t, int j, uint64_t kd) {
+    auto release = [&](int bar) { tc_commit_lead(lead, &bars[bar]); };
+    // S_t = Q_t K^T into tile t's S columns (the key tile is in its stage, kd).
+    auto issue_s = [&](int t, uint64_t kd) {
       const uint64_t dq = t ? dqB : dqA;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -604,68 +649,107 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         tc_mma_lead(lead, tmem + t * kNK, dq + static_cast<uint64_t>((hf * (kTcRows * 128) + kk * 32) >> 4),
                     kd + static_cast<uint64_t>((hf * S::kHS + kk * 32) >> 4), idesc_s, ks > 0 ? 1u : 0u);
       }
-      tc_commit_lead(lead, &bars[B::kS + t * kKSt + j % kKSt]);
+      release(B::kS + t);
     };
-    // O_t += P_t(j) V(j), P_t(j) from TMEM (over S_t(j)); V(j) in its stage, vd.
-    auto issue_pv = [&](int t, int j, uint64_t vd) {
+    // O_t (+)= P_t V, P_t from TMEM (over S_t); the key tile's V in its stage, vd.
+    auto issue_pv = [&](int t, bool acc, uint64_t vd) {
 #pragma unroll
       for (int ks = 0; ks < kNK / 16; ++ks)
         tc_mma_ts_lead(lead, tmem + kColO + t * 128, tmem + t * kNK + ks * 8,
-                       vd + static_cast<uint64_t>((ks * 2 * S::kGS) >> 4), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-      // Only the epilogue waits for PV: earlier PVs are covered by the next
-      // S commit of the tile (the tensor pipe completes one thread's MMAs in order).
-      if (j == ntile_of(t) - 1) tc_commit_lead(lead, &bars[B::kPv + t]);
+                       vd + static_cast<uint64_t>((ks * 2 * S::kGS) >> 4), idesc_o, (acc || ks > 0) ? 1u : 0u);
     };
-    // Each V stage is released once per tile, and only after its tile has
-    // landed: an mbarrier does not keep phases apart, so a release for a later
-    // use of a stage must never arrive before the current use is complete.
-    // (A K stage is freed by the S commits, which follow its landing.)
-    // Commits, like the MMAs, come from the elected lane of the converged warp.
-    auto release = [&](int bar) { tc_commit_lead(lead, &bars[bar]); };
-    if (ok && ntiles > 0) {
-      if ((ok = mbar_wait_warp(&bars[B::kKFull], 0, s_abort, a.wait_ns))) {
-        tc_fence_after();
-        if (ntile0 > 0) issue_s(0, 0, dk);
-        if (ntile1 > 0) issue_s(1, 0, dk);
-      }
-    }
-    for (int j = 0; ok && j < ntiles; ++j) {
-      bool k_next = false;                // K(j+1) seen in its stage
-      const uint64_t vd = v_desc(j), kd_next = k_desc(j + 1);
-      if (!(ok = mbar_wait_warp(&bars[B::kVFull + j % kVSt], (j / kVSt) & 1, s_abort, a.wait_ns))) break;
-      if (j == ntiles - 1 && last_nkeys < kNK) {
-        // Keys past the item's end in its last tile: zero their V rows so that
-        // 0 * stale data cannot produce NaN in the tensor core.
-        uint8_t* vst = smem + S::kOffV + (j % kVSt) * S::kKV;
-        for (int idx = lane; idx < (kNK - last_nkeys) * S::kHalves * 8; idx += 32) {
-          const int hf = idx / ((kNK - last_nkeys) * 8);
-          const int rem = idx % ((kNK - last_nkeys) * 8);
-          const int key = last_nkeys + rem / 8, chunk = rem % 8;
-          *reinterpret_cast<uint4*>(vst + (key / 8) * S::kGS + hf * S::kHS + (key % 8) * 128 + chunk * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
+    // FP8 pools: wait for the softmax warps' f16 conversion of the tiles instead.
+    constexpr int kQReady = F8 ? B::kQc : B::kQFull;
+    int kc = 0, vc = 0;        // K / V tiles of the launch consumed so far
+    uint32_t pc0 = 0, pc1 = 0; // P phases of tile A / B waited so far
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      int w = n_items;
+      if (!(ok = take_item(r, w))) break;
+      if (w >= n_items) break;
+      const TcItem iv = tc_item(items, w, G);
+      const int ntile0 = iv.ntile0, ntile1 = iv.ntile1, ntiles = iv.ntiles;
+      auto ntile_of = [&](int t) { return t ? ntile1 : ntile0; };
+      const int last_nkeys = ntiles > 0 ? min(kNK, iv.kv_end - (iv.it.kv_start + (ntiles - 1) * kNK)) : kNK;
+      if (!(ok = mbar_wait_warp(&bars[kQReady], r & 1, s_abort, a.wait_ns) &&
+                 mbar_wait_warp(&bars[kQReady + 1], r & 1, s_abort, a.wait_ns)))
+        break;
+      // Every tile releases its query buffer after its last S MMA and reports
+      // its output after its last PV: a tile without key tiles at once.
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
-        if (j < ntile_of(t)) {
-          if (!(ok = mbar_wait_warp(&bars[B::kP + t], j & 1, s_abort, a.wait_ns))) break;
-          tc_fence_after();
-          issue_pv(t, j, vd);
-          if (j + 1 < ntile_of(t)) {
-            if (!k_next && !(ok = mbar_wait_warp(&bars[B::kKFull + (j + 1) % kKSt], ((j + 1) / kKSt) & 1, s_abort, a.wait_ns)))
-              break;
-            k_next = true;
-            // No tcgen05 fence: TMA data is ordered by the K barrier, and the P
-            // wait above already ordered the softmax's TMEM writes before this
-            // thread's MMAs, which the tensor pipe runs in issue order.
-            issue_s(t, j + 1, kd_next);
-          }
+        if (ntile_of(t) == 0) {
+          release(B::kQEmpty + t);
+          release(B::kPv + t);
         }
       }
-      if (!ok) break;
-      release(B::kVEmpty + j % kVSt);
+      if (ntiles > 0) {
+        if (!(ok = mbar_wait_warp(&bars[B::kKFull + kc % kKSt], (kc / kKSt) & 1, s_abort, a.wait_ns))) break;
+        tc_fence_after();
+        const uint64_t kd = k_desc(kc);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (ntile_of(t) > 0) {
+            issue_s(t, kd);
+            if (ntile_of(t) == 1) release(B::kQEmpty + t);
+          }
+        }
+        release(B::kKEmpty + kc % kKSt);
+        ++kc;
+      }
+      // Per key tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), so that tile B's
+      // softmax runs while the tensor pipe works on tile A and the other way
+      // round.
+      for (int j = 0; ok && j < ntiles; ++j) {
+        bool k_next = false;   // key tile j+1 seen in its stage
+        const uint64_t vd = v_desc(vc), kd_next = k_desc(kc);
+        if (!(ok = mbar_wait_warp(&bars[B::kVFull + vc % kVSt], (vc / kVSt) & 1, s_abort, a.wait_ns))) break;
+        if (j == ntiles - 1 && last_nkeys < kNK) {
+          // Keys past the item's end in its last tile: zero their V rows so that
+          // 0 * stale data cannot produce NaN in the tensor core.
+          uint8_t* vst = smem + S::kOffV + (vc % kVSt) * S::kKV;
+          for (int idx = lane; idx < (kNK - last_nkeys) * S::kHalves * 8; idx += 32) {
+            const int hf = idx / ((kNK - last_nkeys) * 8);
+            const int rem = idx % ((kNK - last_nkeys) * 8);
+            const int key = last_nkeys + rem / 8, chunk = rem % 8;
+            *reinterpret_cast<uint4*>(vst + (key / 8) * S::kGS + hf * S::kHS + (key % 8) * 128 + chunk * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < ntile_of(t)) {
+            if (!(ok = mbar_wait_warp(&bars[B::kP + t], (t ? pc1 : pc0) & 1, s_abort, a.wait_ns))) break;
+            if (t) ++pc1; else ++pc0;
+            tc_fence_after();
+            issue_pv(t, j > 0, vd);
+            // Only the epilogue waits for PV: earlier PVs are covered by the
+            // next S commit of the tile (the tensor pipe completes one thread's
+            // MMAs in order).
+            if (j == ntile_of(t) - 1) release(B::kPv + t);
+            if (j + 1 < ntile_of(t)) {
+              if (!k_next &&
+                  !(ok = mbar_wait_warp(&bars[B::kKFull + kc % kKSt], (kc / kKSt) & 1, s_abort, a.wait_ns)))
+                break;
+              k_next = true;
+              // No tcgen05 fence: TMA data is ordered by the K barrier, and the P
+              // wait above already ordered the softmax's TMEM writes before this
+              // thread's MMAs, which the tensor pipe runs in issue order.
+              issue_s(t, kd_next);
+              if (j + 1 == ntile_of(t) - 1) release(B::kQEmpty + t);
+            }
+          }
+        }
+        if (!ok) break;
+        if (k_next) {
+          release(B::kKEmpty + kc % kKSt);
+          ++kc;
+        }
+        release(B::kVEmpty + vc % kVSt);
+        ++vc;
+      }
     }
     if (!ok) {
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
@@ -676,176 +760,185 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     (void)mbar_wait_warp(&bars[B::kDrain], 0, nullptr, a.wait_ns);
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue of tile X
+    const int X = (warp >> 2) & 1;            // query tile of the warp (0 = A, 1 = B)
+    const int row = threadIdx.x & 127;        // its row within the tile (TMEM lane)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t colS = X * kNK, colO = kColO + X * 128;
-    const int nrows = rows_of(X);
-    const int nt = ntile_of(X);
-    const int min_pos = X ? it.pos_min[1] : it.pos_min[0];
     // FP8 pools: S holds q . code, so k_scale joins the score scale (and
     // v_scale the final 1/l).
     const float sl2 = F8 ? a.scale_log2 * a.pool.k_scale : a.scale_log2;
-    float m = -CUDART_INF_F, l = 0.f;
+    uint32_t sc = 0;   // S phases of the tile waited so far
     bool ok = true;
-    if constexpr (F8) {
-      // The widened K and V are f16, and both operands of an MMA share one
-      // type: convert this thread's Q row of its tile to f16 in place once the
-      // tile has landed (exact within f16's range).
-      ok = mbar_wait_warp(&bars[B::kQ + X], 0, s_abort, a.wait_ns);
+    for (int r = 0; ok; ++r) {
+      int w = n_items;
+      if (!(ok = take_item(r, w))) break;
+      if (w >= n_items) break;
+      const TcItem iv = tc_item(items, w, G);
+      const WorkItem& it = iv.it;
+      const int g = it.kv_head;
+      const int nrows = X ? iv.rows1 : iv.rows0;
+      const int nt = X ? iv.ntile1 : iv.ntile0;
+      const int min_pos = X ? it.pos_min[1] : it.pos_min[0];
+      const int kv_end = iv.kv_end;
+      const int rows0 = iv.rows0;
+      auto tok0_of = [&](int t) { return t ? iv.tok01 : iv.tok00; };
+      int qpos = -1;
+      if (row < nrows) qpos = __ldg(a.q_positions + tok0_of(X) + row / G);
+      float m = -CUDART_INF_F, l = 0.f;
+      if constexpr (F8) {
+        // The widened K and V are f16, and both operands of an MMA share one
+        // type: convert this thread's Q row of its tile to f16 in place once the
+        // tile has landed (exact within f16's range).
+        ok = mbar_wait_warp(&bars[B::kQFull + X], r & 1, s_abort, a.wait_ns);
+        if (ok) {
+          uint8_t* qrow = smem + S::kOffQ + X * S::kQ + row * 128;
+#pragma unroll
+          for (int hf = 0; hf < S::kHalves; ++hf) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint4* q16 = reinterpret_cast<uint4*>(qrow + hf * (kTcRows * 128) + c * 16);
+              uint4 v = *q16;
+              v.x = pack_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x));
+              v.y = pack_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
+              v.z = pack_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z));
+              v.w = pack_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w));
+              *q16 = v;
+            }
+          }
+          fence_proxy_async_smem();   // read by the tensor cores
+        }
+        mbar_arrive(&bars[B::kQc + X]);
+      }
+      for (int j = 0; ok && j < nt; ++j) {
+        const int key0 = it.kv_start + j * kNK;
+        if (!(ok = mbar_wait_warp(&bars[B::kS + X], sc & 1, s_abort, a.wait_ns))) break;
+        ++sc;
+          tc_fence_after();
+          float s[kNK];
+#pragma unroll
+          for (int c = 0; c < kNK; c += 16) tmem_ld16(tmem + lane_base + colS + c, s + c);
+          tmem_wait_ld();
+          if (key0 + kNK - 1 > min_pos || key0 + kNK > kv_end) {
+            // The row sees keys [0, min(qpos + 1, kv_end)): a prefix of the tile.
+            const int lim = min(qpos + 1, kv_end) - key0;
+#pragma unroll
+            for (int c = 0; c < kNK; ++c) s[c] = c < lim ? s[c] : -CUDART_INF_F;
+          }
+          // Row max as 8 independent partials of 3-input maxima (one long
+          // dependency chain would leave the softmax warps latency-bound).
+          float mx8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(s[2 * k], s[2 * k + 1]);
+#pragma unroll
+          for (int c = 16; c < kNK; c += 2) mx8[(c >> 1) & 7] = max3f(mx8[(c >> 1) & 7], s[c], s[c + 1]);
+          const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+          // Lazy rescaling: rows keep their reference max m while the tile max stays
+          // within 2^kRescaleLog2 of it (P then stays <= 2^kRescaleLog2, fine for bf16
+          // and fp32 sums); O and l always share the same reference, so the result
+          // is exact.  The decision is per warp because TMEM loads and stores are
+          // warp-collective.
+          const float m_tile = mx * sl2;
+          const bool grow = __any_sync(0xffffffffu, m_tile > m + kRescaleLog2);
+          const float m_new = grow ? fmaxf(m, m_tile) : m;
+          const float neg_m = m_new == -CUDART_INF_F ? 0.f : -m_new;
+          float rs0[4] = {0.f, 0.f, 0.f, 0.f}, rs1[4] = {0.f, 0.f, 0.f, 0.f};
+          // P = 2^(s * scale * log2 e - m) as bf16, written over S 32 keys at a
+          // time (16 columns); S columns are all in registers already.
+#pragma unroll
+          for (int cc = 0; cc < kNK; cc += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = cc; c < cc + 32; c += 2) {
+              float x0 = s[c], x1 = s[c + 1];
+              fma2(x0, x1, sl2, neg_m);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              add2(rs0[(c >> 1) & 3], rs1[(c >> 1) & 3], p0, p1);
+              pk[(c - cc) / 2] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tmem + lane_base + colS + cc / 2, reinterpret_cast<const float*>(pk));
+          }
+          const float rsum = ((rs0[0] + rs1[0]) + (rs0[1] + rs1[1])) + ((rs0[2] + rs1[2]) + (rs0[3] + rs1[3]));
+          const float alpha = grow ? fast_exp2(m + neg_m) : 1.f;
+          // O(j-1) is complete (S(j) was issued after PV(j-1) finished).
+          if (grow && j > 0) {
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+              float o[32];
+              tmem_ld16(tmem + lane_base + colO + c, o);
+              tmem_ld16(tmem + lane_base + colO + c + 16, o + 16);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tmem_st16(tmem + lane_base + colO + c, o);
+              tmem_st16(tmem + lane_base + colO + c + 16, o + 16);
+            }
+          }
+          l = l * alpha + rsum;
+          m = m_new;
+          tmem_wait_st();
+          tc_fence_before();
+        mbar_arrive(&bars[B::kP + X]);
+      }
+      if (ok && !(ok = mbar_wait_warp(&bars[B::kPv + X], r & 1, s_abort, a.wait_ns))) break;
+      tc_fence_after();
+      // Epilogue.  `ok` is uniform within a warp; the TMEM loads are executed by
+      // every thread of the warp, only the stores depend on the row being valid.
       if (ok) {
-        uint8_t* qrow = smem + S::kOffQ + X * S::kQ + row * 128;
+        constexpr float kLn2 = 0.69314718055994530942f;
+        const bool valid = row < nrows;
+        const float inv = l > 0.f ? (F8 ? a.pool.v_scale : 1.f) / l : 0.f;
+        const float lse = l > 0.f ? (m + fast_log2(l)) * kLn2 : -CUDART_INF_F;
+        const int t = tok0_of(X) + (valid ? row / G : 0);
+        const int h = g * G + row % G;
+        const int prow = it.part + (X == 0 ? row : rows0 + row);
+        uint4* dst_o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D);
+        float4* dst_p = it.part >= 0 ? reinterpret_cast<float4*>(a.part_o + static_cast<int64_t>(prow) * D) : nullptr;
+        // O in 64-column batches: four TMEM loads in flight per wait.
 #pragma unroll
-        for (int hf = 0; hf < S::kHalves; ++hf) {
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          float ob[64];
+          if (nt > 0) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4* q16 = reinterpret_cast<uint4*>(qrow + hf * (kTcRows * 128) + c * 16);
-            uint4 v = *q16;
-            v.x = pack_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x));
-            v.y = pack_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y));
-            v.z = pack_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z));
-            v.w = pack_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w));
-            *q16 = v;
+            for (int c = 0; c < 64; c += 16) tmem_ld16(tmem + lane_base + colO + c0 + c, ob + c);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) ob[e] = 0.f;
+          }
+          if (valid) {
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+              const float* o = ob + c;
+              if (it.part < 0) {
+                uint4 w0, w1;
+                w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);   w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);   w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+                w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);   w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
+                w1.z = pack_bf16x2(o[12] * inv, o[13] * inv); w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
+                dst_o[(c0 + c) / 8] = w0;
+                dst_o[(c0 + c) / 8 + 1] = w1;
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; e += 4)
+                  dst_p[(c0 + c + e) / 4] = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+              }
+            }
           }
         }
-        fence_proxy_async_smem();   // read by the tensor cores
-      }
-      mbar_arrive(&bars[B::kQc + X]);
-    }
-    for (int j = 0; ok && j < nt; ++j) {
-      const int key0 = it.kv_start + j * kNK;
-      if (!mbar_wait_warp(&bars[B::kS + X * kKSt + j % kKSt], (j / kKSt) & 1, s_abort, a.wait_ns)) { ok = false; break; }
-      tc_fence_after();
-      float s[kNK];
-#pragma unroll
-      for (int c = 0; c < kNK; c += 16) tmem_ld16(tmem + lane_base + colS + c, s + c);
-      tmem_wait_ld();
-      if (key0 + kNK - 1 > min_pos || key0 + kNK > kv_end) {
-        // The row sees keys [0, min(qpos + 1, kv_end)): a prefix of the tile.
-        const int lim = min(qpos + 1, kv_end) - key0;
-#pragma unroll
-        for (int c = 0; c < kNK; ++c) s[c] = c < lim ? s[c] : -CUDART_INF_F;
-      }
-      // Row max as 8 independent partials of 3-input maxima (one long
-      // dependency chain would leave the softmax warps latency-bound).
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(s[2 * k], s[2 * k + 1]);
-#pragma unroll
-      for (int c = 16; c < kNK; c += 2) mx8[(c >> 1) & 7] = max3f(mx8[(c >> 1) & 7], s[c], s[c + 1]);
-      const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      // Lazy rescaling: rows keep their reference max m while the tile max stays
-      // within 2^kRescaleLog2 of it (P then stays <= 2^kRescaleLog2, fine for bf16
-      // and fp32 sums); O and l always share the same reference, so the result
-      // is exact.  The decision is per warp because TMEM loads and stores are
-      // warp-collective.
-      const float m_tile = mx * sl2;
-      const bool grow = __any_sync(0xffffffffu, m_tile > m + kRescaleLog2);
-      const float m_new = grow ? fmaxf(m, m_tile) : m;
-      const float neg_m = m_new == -CUDART_INF_F ? 0.f : -m_new;
-      float rs0[4] = {0.f, 0.f, 0.f, 0.f}, rs1[4] = {0.f, 0.f, 0.f, 0.f};
-      // P = 2^(s * scale * log2 e - m) as bf16, written over S 32 keys at a
-      // time (16 columns); S columns are all in registers already.
-#pragma unroll
-      for (int cc = 0; cc < kNK; cc += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = cc; c < cc + 32; c += 2) {
-          float x0 = s[c], x1 = s[c + 1];
-          fma2(x0, x1, sl2, neg_m);
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          add2(rs0[(c >> 1) & 3], rs1[(c >> 1) & 3], p0, p1);
-          pk[(c - cc) / 2] = F8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tmem + lane_base + colS + cc / 2, reinterpret_cast<const float*>(pk));
-      }
-      const float rsum = ((rs0[0] + rs1[0]) + (rs0[1] + rs1[1])) + ((rs0[2] + rs1[2]) + (rs0[3] + rs1[3]));
-      const float alpha = grow ? fast_exp2(m + neg_m) : 1.f;
-      // O(j-1) is complete (S(j) was issued after PV(j-1) finished).
-      if (grow && j > 0) {
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          float o[32];
-          tmem_ld16(tmem + lane_base + colO + c, o);
-          tmem_ld16(tmem + lane_base + colO + c + 16, o + 16);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st16(tmem + lane_base + colO + c, o);
-          tmem_st16(tmem + lane_base + colO + c + 16, o + 16);
+        if (valid) {
+          if (it.part < 0) {
+            if (a.lse) a.lse[static_cast<int64_t>(t) * a.num_q_heads + h] = lse;
+          } else {
+            a.part_lse[prow] = lse;
+          }
         }
       }
-      l = l * alpha + rsum;
-      m = m_new;
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars[B::kP + X]);
     }
-    if (ok && nt > 0) {
-      if (!mbar_wait_warp(&bars[B::kPv + X], 0, s_abort, a.wait_ns)) ok = false;
-      tc_fence_after();
-    }
+
     if (!ok) {
       if (lane == 0) atomicOr(a.pool.err, PKV_DEVERR_TIMEOUT);
       *s_abort = 1;
     }
-    // Epilogue.  `ok` is uniform within a warp; the TMEM loads are executed by
-    // every thread of the warp, only the stores depend on the row being valid.
-    if (ok) {
-      constexpr float kLn2 = 0.69314718055994530942f;
-      const bool valid = row < nrows;
-      const float inv = l > 0.f ? (F8 ? a.pool.v_scale : 1.f) / l : 0.f;
-      const float lse = l > 0.f ? (m + fast_log2(l)) * kLn2 : -CUDART_INF_F;
-      const int t = tok0_of(X) + (valid ? row / G : 0);
-      const int h = g * G + row % G;
-      const int prow = it.part + (X == 0 ? row : rows0 + row);
-      uint4* dst_o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + (static_cast<int64_t>(t) * a.num_q_heads + h) * D);
-      float4* dst_p = it.part >= 0 ? reinterpret_cast<float4*>(a.part_o + static_cast<int64_t>(prow) * D) : nullptr;
-      // O in 64-column batches: four TMEM loads in flight per wait.
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 64) {
-        float ob[64];
-        if (nt > 0) {
-#pragma unroll
-          for (int c = 0; c < 64; c += 16) tmem_ld16(tmem + lane_base + colO + c0 + c, ob + c);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 64; ++e) ob[e] = 0.f;
-        }
-        if (valid) {
-#pragma unroll
-          for (int c = 0; c < 64; c += 16) {
-            const float* o = ob + c;
-            if (it.part < 0) {
-              uint4 w0, w1;
-              w0.x = pack_bf16x2(o[0] * inv, o[1] * inv);   w0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-              w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);   w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-              w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);   w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
-              w1.z = pack_bf16x2(o[12] * inv, o[13] * inv); w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-              dst_o[(c0 + c) / 8] = w0;
-              dst_o[(c0 + c) / 8 + 1] = w1;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; e += 4)
-                dst_p[(c0 + c + e) / 4] = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
-            }
-          }
-        }
-      }
-      if (valid) {
-        if (it.part < 0) {
-          if (a.lse) a.lse[static_cast<int64_t>(t) * a.num_q_heads + h] = lse;
-        } else {
-          a.part_lse[prow] = lse;
-        }
-      }
-    }
-  }
-
-  // The query-tile copies have landed before shared memory is released (at
-  // once unless a wait above gave up before the issuer saw them).
-  if (threadIdx.x == 0) {
-    (void)mbar_wait(&bars[B::kQ], 0, nullptr, a.wait_ns);
-    (void)mbar_wait(&bars[B::kQ + 1], 0, nullptr, a.wait_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -864,8 +957,8 @@ static int launch_tc_d(const AttnArgs& a, const CUtensorMap* tk, const CUtensorM
   const int smem = TcSmem<D>::kTotal;
   cudaError_t e = smem_attr_once<tc_attn_kernel<D, F8>>(smem);
   if (e != cudaSuccess) return e;
-  tc_attn_kernel<D, F8><<<n_items, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, *tk, *tv, *tq, *tkn,
-                                                                                        *tvn, items);
+  tc_attn_kernel<D, F8><<<a.tc_ctas, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(a, *tk, *tv, *tq, *tkn,
+                                                                                          *tvn, items, n_items);
   return cudaGetLastError();
 }
 

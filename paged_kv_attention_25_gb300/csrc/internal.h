@@ -89,7 +89,8 @@ struct Plan {
   int num_partial_rows = 0;
   pkv_plan_stats stats{};
   // Workspace layout (byte offsets, 256-aligned sections).
-  size_t off_decode = 0, off_tc = 0, off_merge = 0, off_merge_dec = 0, off_merge_cnt = 0, off_runs = 0, off_run_off = 0;
+  size_t off_decode = 0, off_tc = 0, off_merge = 0, off_merge_dec = 0, off_merge_cnt = 0, off_runs = 0, off_run_off = 0,
+         off_tc_next = 0;
   size_t off_part_o = 0, off_part_lse = 0, total = 0;
   bool valid = false;
   int64_t builds = 0;   // plans built into this object so far
@@ -160,6 +161,8 @@ struct AttnArgs {
   const MergeItem* merge_dec;   // merge items of split-KV groups (merged by their last split)
   int* merge_cnt;               // splits finished per such item (zeroed by the work-list upload)
   int q_box_tokens;             // tokens per query-tile copy of the tensor-core kernel's Q tensor map
+  int* tc_next;                 // the tensor-core kernel's next unclaimed item (zeroed by the work-list upload)
+  int tc_ctas;                  // CTAs of the tensor-core launch: one per SM, at most one per item
   // Fused append (pkv_append_paged_attn); k_new is nullptr in a plain call.
   // The attention kernels read the new tokens' keys and values from k_new /
   // v_new ([T][Hkv][D] bf16), never from the pool, and n_append_ctas extra

@@ -104,7 +104,7 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   plan->num_partial_rows = 0;
   plan->stats = pkv_plan_stats{};
   plan->off_decode = plan->off_tc = plan->off_merge = plan->off_merge_dec = plan->off_merge_cnt = 0;
-  plan->off_runs = plan->off_run_off = 0;
+  plan->off_runs = plan->off_run_off = plan->off_tc_next = 0;
   plan->off_part_o = plan->off_part_lse = plan->total = 0;
   plan->valid = false;
   const int R = pp.num_reqs, T = pp.num_tokens, Hq = pp.num_q_heads, Hkv = pp.num_kv_heads, D = pp.head_dim;
@@ -389,6 +389,8 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   off = align256(off + plan->merge_dec.size() * sizeof(MergeItem));
   plan->off_merge_cnt = off;   // counters, uploaded as zeros with the work lists
   off = align256(off + plan->merge_dec.size() * sizeof(int32_t));
+  plan->off_tc_next = off;     // the tensor-core kernel's next-item counter, uploaded as zero
+  off = align256(off + sizeof(int32_t));
   plan->off_runs = off;
   off = align256(off + plan->runs.size() * sizeof(RunDesc));
   plan->off_run_off = off;

@@ -96,12 +96,8 @@ def test_fp8_split_kv_attention_matches_oracle(hq, hkv, d, tokens):
     assert st["num_decode_items"] > b.num_reqs * hkv   # the long request is split over several items
 
 
-def test_fp8_full_size_decode_workload_sampled():
-    b = wl.decode_lognormal()
-    rng = np.random.default_rng(9)
-    rt = rng.integers(0, b.num_tokens, size=96).astype(np.int32)
-    rh = rng.integers(0, b.num_q_heads, size=96).astype(np.int32)
-    check_attention(b, 2.0 ** -6, 2.0 ** -6, rows=(rt, rh))
+def test_fp8_full_size_decode_workload_every_row():
+    check_attention(wl.decode_lognormal(), 2.0 ** -6, 2.0 ** -6)
 
 
 def test_fp8_swap_bit_exact():
@@ -153,12 +149,8 @@ def test_fp8_tensor_core_edge_shapes(G, D):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["llama13b_mixed", "llama70b_gqa", "long_skewed_evict"])
-def test_fp8_full_size_mixed_workloads_sampled(name):
-    b = wl.WORKLOADS[name]()
-    rng = np.random.default_rng(10)
-    rt = rng.integers(0, b.num_tokens, size=400).astype(np.int32)
-    rh = rng.integers(0, b.num_q_heads, size=400).astype(np.int32)
-    check_attention(b, 2.0 ** -6, 2.0 ** -6, rows=(rt, rh), want_tc=True)
+def test_fp8_full_size_mixed_workloads_every_row(name):
+    check_attention(wl.WORKLOADS[name](), 2.0 ** -6, 2.0 ** -6, want_tc=True)
 
 
 def test_fp8_pool_rejects_bad_scales():

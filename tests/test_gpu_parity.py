@@ -297,17 +297,6 @@ def test_swap_out_in_bit_exact():
 
 # ----------------------------------------------------------------------------- full-size workloads
 
-def sampled_rows(batch, n, seed):
-    """A seeded sample of (token, head) rows, always including every request's first and last token."""
-    rng = np.random.default_rng(seed)
-    t = rng.integers(0, batch.num_tokens, size=n)
-    firsts = batch.cu_q_lens[:-1][np.diff(batch.cu_q_lens) > 0]
-    lasts = batch.cu_q_lens[1:][np.diff(batch.cu_q_lens) > 0] - 1
-    t = np.concatenate([t, firsts, lasts]).astype(np.int32)
-    h = rng.integers(0, batch.num_q_heads, size=t.shape[0]).astype(np.int32)
-    return t, h
-
-
 @pytest.mark.slow
 @pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("nbytes,offset", [(1 << 20, 0), (12345, 0), (4099, 3), (16, 0), (0, 0)])
@@ -332,18 +321,16 @@ def test_host_copies_bit_exact(pinned, nbytes, offset):
 
 
 @pytest.mark.parametrize("name", ["llama13b_mixed", "decode_lognormal", "llama70b_gqa", "long_skewed_evict"])
-def test_full_size_workloads_sampled(name):
+def test_full_size_workloads_every_row(name):
+    """Every (token, head) row of the full-size workload against the fp64 oracle, in the bench's launch shape."""
     batch = wl.WORKLOADS[name]()
     run = GpuRun(batch)
     o, lse = run.step()
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
     kp, vp = oracle_pools(batch)
-    t, h = sampled_rows(batch, 600, seed=7)
-    O, L = oracle.paged_attn_rows(batch.q, kp, vp, batch.block_tables, batch.ctx_lens, batch.cu_q_lens,
-                                  batch.q_positions, batch.scale, t, h)
-    o_np = bf16_to_f64(o)[t, h]
-    l_np = lse.cpu().numpy().astype(np.float64)[t, h]
-    assert_close(o_np, l_np, O, L, name)
+    O, L = oracle.paged_attn(batch.q, kp, vp, batch.block_tables, batch.ctx_lens, batch.cu_q_lens,
+                             batch.q_positions, batch.scale)
+    assert_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O, L, name)
 
 
 def test_plan_cache_tells_apart_batches_of_one_shape():
