@@ -674,15 +674,14 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       if (!(ok = mbar_wait_warp(&bars[kQReady], r & 1, s_abort, a.wait_ns) &&
                  mbar_wait_warp(&bars[kQReady + 1], r & 1, s_abort, a.wait_ns)))
         break;
-      // Every tile releases its query buffer after its last S MMA and reports
-      // its output after its last PV: a tile without key tiles at once.
+      // Every tile releases its query buffer after its last S MMA, a tile
+      // without key tiles at once.  Its last PV is reported (kPv) only for a
+      // tile with key tiles: an immediate report would complete together with
+      // the previous item's (both wait for the same MMAs), two phases before
+      // the softmax warps look, and their parity wait would miss it.
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (ntile_of(t) == 0) {
-          release(B::kQEmpty + t);
-          release(B::kPv + t);
-        }
-      }
+      for (int t = 0; t < 2; ++t)
+        if (ntile_of(t) == 0) release(B::kQEmpty + t);
       if (ntiles > 0) {
         if (!(ok = mbar_wait_warp(&bars[B::kKFull + kc % kKSt], (kc / kKSt) & 1, s_abort, a.wait_ns))) break;
         tc_fence_after();
@@ -768,6 +767,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     // v_scale the final 1/l).
     const float sl2 = F8 ? a.scale_log2 * a.pool.k_scale : a.scale_log2;
     uint32_t sc = 0;   // S phases of the tile waited so far
+    uint32_t pvc = 0;  // its items with key tiles so far (kPv phases)
     bool ok = true;
     for (int r = 0; ok; ++r) {
       int w = n_items;
@@ -879,7 +879,10 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           tc_fence_before();
         mbar_arrive(&bars[B::kP + X]);
       }
-      if (ok && !(ok = mbar_wait_warp(&bars[B::kPv + X], r & 1, s_abort, a.wait_ns))) break;
+      if (ok && nt > 0) {
+        if (!(ok = mbar_wait_warp(&bars[B::kPv + X], pvc & 1, s_abort, a.wait_ns))) break;
+        ++pvc;
+      }
       tc_fence_after();
       // Epilogue.  `ok` is uniform within a warp; the TMEM loads are executed by
       // every thread of the warp, only the stores depend on the row being valid.

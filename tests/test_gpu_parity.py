@@ -361,3 +361,19 @@ def test_plan_cache_tells_apart_batches_of_one_shape():
     oracle.append(kp, vp, b.block_tables, b.cu_q_lens, b.q_positions, b.k_new, b.v_new)
     O, L = oracle.paged_attn(b.q, kp, vp, b.block_tables, b.ctx_lens, b.cu_q_lens, b.q_positions, b.scale)
     assert_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O, L, "second batch")
+
+
+@pytest.mark.parametrize("name,mode", [("llama13b_mixed", 1), ("llama13b_mixed", 2), ("long_skewed_evict", 1)])
+def test_repeated_calls_bit_identical_without_device_errors(name, mode):
+    """Forty calls on one full-size batch (the persistent tensor-core kernel reuses every barrier across the
+    items of a CTA, including single-tile items): no bounded wait gives up, and every output equals the first."""
+    batch = wl.WORKLOADS[name]()
+    run = GpuRun(batch)
+    o0, l0 = run.step()
+    pkv.pkv_profile_enable(run.pool, mode)
+    for _ in range(40):
+        o, lse = run.attn()
+    torch.cuda.synchronize()
+    pkv.pkv_profile_enable(run.pool, 0)
+    assert pkv.pkv_check_device_errors(run.pool) == 0
+    assert torch.equal(o, o0) and torch.equal(lse, l0)
