@@ -145,13 +145,6 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
       : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
 }
 
-// Two e4m3 codes (low byte first) -> two f16 (low half first): exact, since
-// every e4m3 value is an f16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
-
 // Writes 16 consecutive f16 values (two 16-byte chunks) of key r, starting at
 // element 16 * cc, into a K/V stage in the MMA operand layout:
 // [8-key group][64-column half][8 keys][128 bytes], 16-byte chunk c of a
@@ -179,10 +172,10 @@ __device__ __forceinline__ void widen_stage(uint8_t* stage, int lane) {
   const uint8_t* codes = stage + S::kKV / 2;
   auto widen = [&](int q, uint4 v) {
     uint4 lo, hi;
-    lo.x = e4m3x2_to_f16x2(v.x); lo.y = e4m3x2_to_f16x2(v.x >> 16);
-    lo.z = e4m3x2_to_f16x2(v.y); lo.w = e4m3x2_to_f16x2(v.y >> 16);
-    hi.x = e4m3x2_to_f16x2(v.z); hi.y = e4m3x2_to_f16x2(v.z >> 16);
-    hi.z = e4m3x2_to_f16x2(v.w); hi.w = e4m3x2_to_f16x2(v.w >> 16);
+    e4m3x4_to_f16x4(v.x, lo.x, lo.y);
+    e4m3x4_to_f16x4(v.y, lo.z, lo.w);
+    e4m3x4_to_f16x4(v.z, hi.x, hi.y);
+    e4m3x4_to_f16x4(v.w, hi.z, hi.w);
     store_f16x16<D>(stage, q / kCpr, q % kCpr, lo, hi);
   };
   uint4 hold[kPer];
@@ -549,8 +542,9 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           if (t >= 0) {
             const uint4 x = *reinterpret_cast<const uint4*>(src + ((static_cast<int64_t>(t) * Hkv + g) * D) * 2 + c * 16);
             const uint32_t c0 = quant_e4m3x4(x.x, x.y, sc), c1 = quant_e4m3x4(x.z, x.w, sc);
-            const uint4 h = make_uint4(e4m3x2_to_f16x2(c0), e4m3x2_to_f16x2(c0 >> 16), e4m3x2_to_f16x2(c1),
-                                       e4m3x2_to_f16x2(c1 >> 16));
+            uint4 h;
+            e4m3x4_to_f16x4(c0, h.x, h.y);
+            e4m3x4_to_f16x4(c1, h.z, h.w);
             const int r = b * kBlockSize + rr, hf = c / 8, cw = c % 8, r8 = r % 8;
             *reinterpret_cast<uint4*>(stage + (r / 8) * S::kGS + hf * S::kHS + r8 * 128 + ((cw ^ r8) * 16)) = h;
           }

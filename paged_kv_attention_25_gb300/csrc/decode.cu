@@ -70,17 +70,11 @@ __device__ __forceinline__ void load_row(const uint8_t* p, float* f) {
 }
 // The same dims of one row of e4m3 codes as f16 values, two per 32-bit word
 // (lowest element in the low half): the conversion instruction widens each
-// pair of codes exactly (every e4m3 value is an f16 value), on the
-// conversion pipe rather than the integer ALU.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v16), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
+// pair of codes exactly (every e4m3 value is an f16 value).
 template <int kDPL>
 __device__ __forceinline__ void load_row_f16(const uint8_t* p, uint32_t* w) {
-  const uint32_t v = kDPL == 4 ? *reinterpret_cast<const uint32_t*>(p) : *reinterpret_cast<const uint16_t*>(p);
-  w[0] = e4m3x2_to_f16x2(v & 0xffffu);
-  if constexpr (kDPL == 4) w[1] = e4m3x2_to_f16x2(v >> 16);
+  if constexpr (kDPL == 4) e4m3x4_to_f16x4(*reinterpret_cast<const uint32_t*>(p), w[0], w[1]);
+  else w[0] = e4m3x2_lo_to_f16x2(*reinterpret_cast<const uint16_t*>(p));
 }
 // c0 += lo(a) * lo(b), c1 += hi(a) * hi(b): f16 operands, exact products,
 // fp32 accumulation.
@@ -373,9 +367,12 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
           w1[4 * u] = x1.x; w1[4 * u + 1] = x1.y; w1[4 * u + 2] = x1.z; w1[4 * u + 3] = x1.w;
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_16816(sc, e4m3x2_to_f16x2(w0[k] & 0xffffu), e4m3x2_to_f16x2(w1[k] & 0xffffu),
-                    e4m3x2_to_f16x2(w0[k] >> 16), e4m3x2_to_f16x2(w1[k] >> 16), qb[k][0], qb[k][1]);
+        for (int k = 0; k < 8; ++k) {
+          uint32_t a0, a2, a1, a3;
+          e4m3x4_to_f16x4(w0[k], a0, a2);
+          e4m3x4_to_f16x4(w1[k], a1, a3);
+          mma_16816(sc, a0, a1, a2, a3, qb[k][0], qb[k][1]);
+        }
       }
       float s0 = sc[0] * s_scale, s1 = sc[2] * s_scale;   // keys g and g + 8
       if (key0 + mg > qpos[0] || key0 + mg >= kv_end) s0 = -CUDART_INF_F;
@@ -423,10 +420,13 @@ __device__ __forceinline__ void stream_item(const AttnArgs& a, const WorkItem& i
         for (int i = 0; i < 4; ++i) {   // word i: dims 16g + 4i .. 16g + 4i + 3 (m-tiles 2i and 2i + 1)
           const uint32_t lo01 = __byte_perm(v[0][i], v[1][i], 0x5140), hi01 = __byte_perm(v[0][i], v[1][i], 0x7362);
           const uint32_t lo89 = __byte_perm(v[2][i], v[3][i], 0x5140), hi89 = __byte_perm(v[2][i], v[3][i], 0x7362);
-          mma_16816(acm[2 * i], e4m3x2_to_f16x2(lo01 & 0xffffu), e4m3x2_to_f16x2(lo01 >> 16),
-                    e4m3x2_to_f16x2(lo89 & 0xffffu), e4m3x2_to_f16x2(lo89 >> 16), pb0, pb1);
-          mma_16816(acm[2 * i + 1], e4m3x2_to_f16x2(hi01 & 0xffffu), e4m3x2_to_f16x2(hi01 >> 16),
-                    e4m3x2_to_f16x2(hi89 & 0xffffu), e4m3x2_to_f16x2(hi89 >> 16), pb0, pb1);
+          uint32_t a[8];
+          e4m3x4_to_f16x4(lo01, a[0], a[1]);
+          e4m3x4_to_f16x4(lo89, a[2], a[3]);
+          e4m3x4_to_f16x4(hi01, a[4], a[5]);
+          e4m3x4_to_f16x4(hi89, a[6], a[7]);
+          mma_16816(acm[2 * i], a[0], a[1], a[2], a[3], pb0, pb1);
+          mma_16816(acm[2 * i + 1], a[4], a[5], a[6], a[7], pb0, pb1);
         }
       };
       if (key0 + kBlockSize > kv_end) pv(std::true_type{});   // warp-uniform

@@ -162,6 +162,23 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// e4m3 codes -> f16 with the conversion instruction (exact: every e4m3 value
+// is an f16 value), lowest code in the low half.  e4m3x4_to_f16x4: four codes
+// (lowest first) into two f16x2 words, codes 0-1 in `lo`, 2-3 in `hi`; the
+// 16-bit halves of the word are the instruction's inputs as they stand.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
+}
+// The two codes in the low 16 bits of `codes`.
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t codes) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(r) : "r"(codes));
+  return r;
+}
+
 // Leader-predicated forms for a converged warp: every lane executes them
 // (so the operands stay warp-uniform values and no lane-dependent branch
 // surrounds the issue), and only the lane whose `lead` is non-zero issues.
