@@ -145,50 +145,42 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
       : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
 }
 
-// Writes 16 consecutive f16 values (two 16-byte chunks) of key r, starting at
-// element 16 * cc, into a K/V stage in the MMA operand layout:
-// [8-key group][64-column half][8 keys][128 bytes], 16-byte chunk c of a
-// key's 128-byte line at c ^ (key % 8) (128-byte swizzle).
-template <int D>
-__device__ __forceinline__ void store_f16x16(uint8_t* stage, int r, int cc, uint4 lo, uint4 hi) {
-  using S = TcSmem<D>;
-  const int c0 = 2 * cc, hf = c0 / 8, cw = c0 % 8, r8 = r % 8;
-  uint8_t* line = stage + (r / 8) * S::kGS + hf * S::kHS + r8 * 128;
-  *reinterpret_cast<uint4*>(line + ((cw ^ r8) * 16)) = lo;
-  *reinterpret_cast<uint4*>(line + (((cw + 1) ^ r8) * 16)) = hi;
-}
-
 // FP8 pools: a stage holds the tile's e4m3 codes, [128 keys][D] bytes, in its
-// upper half (as the TMA landed them); widen them in place to the f16
-// operand layout of the whole stage.  Keys 64..127 are read into registers
-// first, because their f16 rows overwrite the codes; keys 0..63 are widened
-// straight from shared memory (their rows fill the lower half).  One warp.
+// upper half (as the TMA landed them); widen them in place to the f16 operand
+// layout of the whole stage: [8-key group][64-column half][8 keys][128 bytes],
+// 16-byte chunk c of a key's 128-byte line at c ^ (key % 8).  One warp.
+//
+// Each lane converts 8 codes into one 16-byte chunk per step, so the 8 lanes
+// of a store phase fill the 8 chunks of one line (distinct banks after the
+// swizzle) and read one key's contiguous codes.  Keys go in increasing order,
+// 16 steps' codes loaded before any of their stores (the loads would
+// otherwise wait behind the previous step's store).  The f16 line of key r
+// (for r >= 64, in the upper half) covers the codes of a key no later than r:
+// a batch overwrites only codes it or an earlier batch has already read.
 template <int D>
 __device__ __forceinline__ void widen_stage(uint8_t* stage, int lane) {
   using S = TcSmem<D>;
-  constexpr int kCpr = D / 16;              // 16-code chunks per key
-  constexpr int kHalfChunks = 64 * kCpr;    // chunks of keys 0..63
-  constexpr int kPer = kHalfChunks / 32;    // chunks of each half per lane
+  constexpr int kGroups = D / 8;              // 8-code groups per key
+  constexpr int kKeysPerStep = 32 / kGroups;  // keys converted per warp step
+  constexpr int kBatch = 16;                  // steps whose codes are loaded together
   const uint8_t* codes = stage + S::kKV / 2;
-  auto widen = [&](int q, uint4 v) {
-    uint4 lo, hi;
-    e4m3x4_to_f16x4(v.x, lo.x, lo.y);
-    e4m3x4_to_f16x4(v.y, lo.z, lo.w);
-    e4m3x4_to_f16x4(v.z, hi.x, hi.y);
-    e4m3x4_to_f16x4(v.w, hi.z, hi.w);
-    store_f16x16<D>(stage, q / kCpr, q % kCpr, lo, hi);
-  };
-  uint4 hold[kPer];
+  const int kk = lane / kGroups, g8 = lane % kGroups;
+  const int hf = (g8 * 8) / 64, cw = g8 % 8;
+#pragma unroll 1
+  for (int b = 0; b < kNK / kKeysPerStep; b += kBatch) {
+    uint2 v[kBatch];
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) hold[i] = *reinterpret_cast<const uint4*>(codes + (kHalfChunks + i * 32 + lane) * 16);
-#pragma unroll 4
-  for (int i = 0; i < kPer; ++i) {
-    const int q = i * 32 + lane;
-    widen(q, *reinterpret_cast<const uint4*>(codes + q * 16));
+    for (int u = 0; u < kBatch; ++u)
+      v[u] = *reinterpret_cast<const uint2*>(codes + ((b + u) * kKeysPerStep + kk) * D + g8 * 8);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int r = (b + u) * kKeysPerStep + kk, r8 = r % 8;
+      uint4 h;
+      e4m3x4_to_f16x4(v[u].x, h.x, h.y);
+      e4m3x4_to_f16x4(v[u].y, h.z, h.w);
+      *reinterpret_cast<uint4*>(stage + (r / 8) * S::kGS + hf * S::kHS + r8 * 128 + ((cw ^ r8) * 16)) = h;
+    }
   }
-  __syncwarp();   // every lane has read the codes the rows below overwrite
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) widen(kHalfChunks + i * 32 + lane, hold[i]);
 }
 
 template <int D, bool F8>
