@@ -494,20 +494,17 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       // landed barrier gk % nst, in the upper half of its stage; the warp widens the stage in place to f16,
       // patches the fused call's new rows in (quantised as the append stores
       // them) and arrives on full.  Copies run one tile ahead of the widening.
-      auto load_f8 = [&](int gk, int y) -> bool {
+      // Issues the copy of the warp's tile gk into its stage, which is free.
+      auto issue_f8 = [&](int gk, int y) {
         const int st = gk % nst;
-        const uint32_t ph = (gk / nst) & 1;
         const uint32_t bytes = static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, y >= 0))) * (kBlockSize * D);
-        const int empty = (is_k ? B::kKEmpty : B::kVEmpty) + st;
-        if (!mbar_wait_warp(&bars[empty], ph ^ 1, s_abort, a.wait_ns)) return false;
-        if (a.withhold == 2 && is_k && gk == 0 && blockIdx.x == 0) return true;   // test hook (above)
+        if (a.withhold == 2 && is_k && gk == 0 && blockIdx.x == 0) return;   // test hook (above)
         uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
         if (lane == 0) mbar_arrive_expect_tx(landed, bytes);
         __syncwarp();
         if (y >= 0)
           tma_load_2d(smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV + S::kKV / 2 + lane * (kBlockSize * D),
                       is_k ? &tmap_k : &tmap_v, 0, y * kBlockSize, landed);
-        return true;
       };
       // The fused call's new rows of block b of a widened stage: each new key's
       // row, quantised to codes (as the append stores it) and widened to f16.
@@ -542,10 +539,9 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           }
         }
       };
-      auto finish_f8 = [&](int j, int gk) -> bool {
+      // Widens the warp's landed tile gk (key tile j of the item) and hands it to the issuer.
+      auto finish_f8 = [&](int j, int gk) {
         const int st = gk % nst;
-        uint64_t* landed = &bars[(is_k ? B::kKLanded : B::kVLanded) + st];
-        if (!mbar_wait_warp(landed, (gk / nst) & 1, s_abort, a.wait_ns)) return false;
         uint8_t* stage = smem + (is_k ? S::kOffK : S::kOffV) + st * S::kKV;
         widen_stage<D>(stage, lane);
         if (fused) {
@@ -571,19 +567,42 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         fence_proxy_async_smem();   // the widened rows are read by the tensor cores
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[(is_k ? B::kKFull : B::kVFull) + st]);
-        return true;
       };
       if constexpr (F8) {
-        // Copies run one tile ahead of the widening (within the item).
-        for (int j = 0; j < iv.ntiles; ++j) {
-          if (!(ok = load_f8(cnt, block_chunk(j)))) break;
-          ++cnt;
-          if (j >= 1) {
-            if (!(ok = finish_f8(j - 1, cnt - 2))) break;
-            fin = cnt - 1;
+        // A tile's codes are copied as soon as a stage is free, and widened as
+        // soon as they have landed.  The warp tests both (without suspending)
+        // and does whichever is ready: waiting for the next free stage before
+        // widening a landed tile would serialise the widening with the MMAs
+        // that free the stage.
+        int jl = 0, jw = 0;      // key tiles of the item copied / widened
+        uint64_t idle0 = 0;      // start of the current stretch without progress
+        while (jw < iv.ntiles) {
+          bool moved = false;
+          if (jl < iv.ntiles && cnt - fin < nst &&
+              mbar_test_warp(&bars[(is_k ? B::kKEmpty : B::kVEmpty) + cnt % nst], ((cnt / nst) & 1) ^ 1)) {
+            issue_f8(cnt, block_chunk(jl));
+            ++cnt;
+            ++jl;
+            moved = true;
+          }
+          if (fin < cnt && mbar_test_warp(&bars[(is_k ? B::kKLanded : B::kVLanded) + fin % nst], (fin / nst) & 1)) {
+            finish_f8(jw, fin);
+            ++fin;
+            ++jw;
+            moved = true;
+          }
+          if (moved) {
+            idle0 = 0;
+          } else {
+            const uint64_t now = globaltimer_ns();
+            if (idle0 == 0) idle0 = now;
+            // One decision for the warp (each lane reads its own clock).
+            if (__any_sync(0xffffffffu, *s_abort != 0 || now - idle0 > a.wait_ns)) {
+              ok = false;
+              break;
+            }
           }
         }
-        if (ok && iv.ntiles > 0 && (ok = finish_f8(iv.ntiles - 1, cnt - 1))) fin = cnt;
       } else {
         for (int j = 0; j < iv.ntiles; ++j) {
           if (!(ok = load(j, cnt, block_chunk(j)))) break;
