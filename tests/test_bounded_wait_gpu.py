@@ -31,13 +31,24 @@ def built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
+FP8_SCALE = 2.0 ** -6
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
 @pytest.mark.parametrize("kernel", [1, 2])
-def test_wait_that_runs_out_is_reported_and_pool_recovers(kernel):
-    # Decodes for the split-KV kernel and new turns for the tensor-core kernel.
+def test_wait_that_runs_out_is_reported_and_pool_recovers(kernel, dtype):
+    # Decodes for the split-KV kernel and new turns for the tensor-core kernel.  FP8 pools take
+    # other waits: the tensor-core producers poll their barriers and give up on their own limit.
+    fp8 = dtype == "fp8_e4m3"
     reqs = [wl._decode(5000), wl._decode(700), wl._new_turn(2000, 300), wl._new_turn(0, 130)]
-    b = wl.build_batch(f"timeout_{kernel}", reqs, num_q_heads=4, num_kv_heads=4, head_dim=128, seed=90 + kernel)
-    pool = pkv.Pool(b.num_blocks, b.num_kv_heads, b.head_dim)
-    wl.fill_pool(b, pool.k, pool.v)
+    b = wl.build_batch(f"timeout_{kernel}_{dtype}", reqs, num_q_heads=4, num_kv_heads=4, head_dim=128,
+                       seed=90 + kernel)
+    if fp8:
+        pool = pkv.Pool(b.num_blocks, b.num_kv_heads, b.head_dim, dtype=dtype, k_scale=FP8_SCALE, v_scale=FP8_SCALE)
+        wl.fill_pool_fp8(b, pool.k, pool.v)
+    else:
+        pool = pkv.Pool(b.num_blocks, b.num_kv_heads, b.head_dim)
+        wl.fill_pool(b, pool.k, pool.v)
     d = wl.upload(b)
     meta = pkv.HostMeta(b.cu_q_lens, b.ctx_lens, b.q_positions)
     pkv.pkv_append(pool, d["block_tables"], d["cu_q_lens"], d["q_positions"], d["k_new"], d["v_new"])
@@ -63,9 +74,16 @@ def test_wait_that_runs_out_is_reported_and_pool_recovers(kernel):
     o, lse = attn()
     torch.cuda.synchronize()
     assert pkv.pkv_check_device_errors(pool) == 0
-    kp, vp = b.pool_arrays()
-    oracle.append(kp, vp, b.block_tables, b.cu_q_lens, b.q_positions, b.k_new, b.v_new)
-    O, L = oracle.paged_attn(b.q, kp, vp, b.block_tables, b.ctx_lens, b.cu_q_lens, b.q_positions, b.scale)
+    if fp8:
+        kp, vp = wl.fp8_pool_arrays(b)
+        oracle.append_fp8(kp, vp, np.float32(FP8_SCALE), np.float32(FP8_SCALE), b.block_tables, b.cu_q_lens,
+                          b.q_positions, b.k_new, b.v_new)
+        O, L = oracle.paged_attn_fp8(b.q, kp, vp, FP8_SCALE, FP8_SCALE, b.block_tables, b.ctx_lens, b.cu_q_lens,
+                                     b.q_positions, b.scale)
+    else:
+        kp, vp = b.pool_arrays()
+        oracle.append(kp, vp, b.block_tables, b.cu_q_lens, b.q_positions, b.k_new, b.v_new)
+        O, L = oracle.paged_attn(b.q, kp, vp, b.block_tables, b.ctx_lens, b.cu_q_lens, b.q_positions, b.scale)
     err = np.abs(o.float().cpu().numpy() - O)
     assert (err <= ATOL + RTOL * np.abs(O)).all(), f"max err {err.max():.3e}"
     assert np.abs(lse.cpu().numpy() - L).max() <= LSE_TOL
