@@ -321,6 +321,27 @@ int build_plan(const PlanParams& pp, const pkv_host_meta& meta, Plan* plan, cons
   };
   longest_first(plan->decode);
   longest_first(plan->tc);
+  // Tensor-core items of one request then go out together.  The request's
+  // tile pairs read the same K/V (each pair a prefix of the request's keys),
+  // so with them in flight at once a K/V tile comes from DRAM about once and
+  // the other pairs find it in L2; ordered by their own lengths alone, the
+  // pairs of a request end up hundreds of claims apart.  A request's rank is
+  // the position of its first (longest) item, and a stable counting sort on
+  // it keeps the longest-first order inside each request.
+  if (plan->tc.size() > 1) {
+    std::vector<WorkItem>& v = plan->tc;
+    const size_t n = v.size();
+    std::vector<uint32_t> rank(R, UINT32_MAX), start(R + 1, 0);
+    uint32_t ranks = 0;
+    for (size_t i = 0; i < n; ++i)
+      if (rank[v[i].req] == UINT32_MAX) rank[v[i].req] = ranks++;
+    for (size_t i = 0; i < n; ++i) ++start[rank[v[i].req] + 1];
+    for (uint32_t b = 0; b < ranks; ++b) start[b + 1] += start[b];
+    std::vector<WorkItem>& tmp = plan->order_tmp;
+    tmp.resize(n);
+    for (size_t i = 0; i < n; ++i) tmp[start[rank[v[i].req]]++] = v[i];
+    v.swap(tmp);
+  }
   plan->num_partial_rows = part_rows;
 
   // 4. Statistics (algorithmic work; each (request, KV head) KV read once).

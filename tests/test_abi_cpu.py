@@ -81,10 +81,23 @@ def check_plan(batch, num_sms=148):
     Hq, Hkv, D = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
     G = Hq // Hkv
     items, st = pkv.pkv_plan_inspect(Hq, Hkv, D, num_sms, meta)
-    # Each kernel's list runs longest item first (split-KV items, then tensor-core items).
-    for k in (1, 2):
-        lens = [int(it["kv_end"]) - int(it["kv_start"]) for it in items if int(it["kernel"]) == k]
-        assert all(a >= b for a, b in zip(lens, lens[1:])), f"kernel {k} items not longest first"
+    # Split-KV items run longest first.  Tensor-core items run one request
+    # after another (a request's tile pairs share its K/V in L2): each
+    # request's items are contiguous and longest first, and requests follow
+    # the order of their longest items.
+    lens = [int(it["kv_end"]) - int(it["kv_start"]) for it in items if int(it["kernel"]) == 1]
+    assert all(a >= b for a, b in zip(lens, lens[1:])), "split-KV items not longest first"
+    tc = [(int(it["req"]), int(it["kv_end"]) - int(it["kv_start"])) for it in items if int(it["kernel"]) == 2]
+    runs = []
+    for r, n in tc:
+        if runs and runs[-1][0] == r:
+            assert runs[-1][1][-1] >= n, "tensor-core items of a request not longest first"
+            runs[-1][1].append(n)
+        else:
+            assert all(rr != r for rr, _ in runs), "tensor-core items of a request not contiguous"
+            runs.append((r, [n]))
+    heads = [ns[0] for _, ns in runs]
+    assert all(a >= b for a, b in zip(heads, heads[1:])), "requests not ordered by their longest item"
     # Group items by (kernel, request, kv head, q_start, q_count).
     groups = {}
     for it in items:
