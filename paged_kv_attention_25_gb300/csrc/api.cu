@@ -622,6 +622,7 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   a.ctx_lens = c.ctx_lens;
   a.scale_log2 = c.scale * 1.4426950408889634f;
   a.o = c.o;
+  a.o_align32 = (reinterpret_cast<uintptr_t>(c.o) & 31u) == 0;
   a.lse = c.lse;
   a.part_o = reinterpret_cast<float*>(ws + pl.off_part_o);
   a.part_lse = reinterpret_cast<float*>(ws + pl.off_part_lse);

@@ -709,16 +709,16 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
         const uint64_t vd = v_desc(vc), kd_next = k_desc(kc);
         if (!(ok = mbar_wait_warp(&bars[B::kVFull + vc % kVSt], (vc / kVSt) & 1, s_abort, a.wait_ns))) break;
         if (j == ntiles - 1 && last_nkeys < kNK) {
-          // Keys past the item's end in its last tile: zero their V rows so that
-          // 0 * stale data cannot produce NaN in the tensor core.
+          // Keys past the item's end in its last tile: zero their V rows (the
+          // unused tail of the last block holds any bits, stages past it stale
+          // or never written data) so that 0 * that data cannot produce NaN in
+          // the tensor core.  Lane l clears 16-byte chunk l % kCh of a row.
           uint8_t* vst = smem + S::kOffV + (vc % kVSt) * S::kKV;
-          for (int idx = lane; idx < (kNK - last_nkeys) * S::kHalves * 8; idx += 32) {
-            const int hf = idx / ((kNK - last_nkeys) * 8);
-            const int rem = idx % ((kNK - last_nkeys) * 8);
-            const int key = last_nkeys + rem / 8, chunk = rem % 8;
-            *reinterpret_cast<uint4*>(vst + (key / 8) * S::kGS + hf * S::kHS + (key % 8) * 128 + chunk * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
+          constexpr int kCh = S::kHalves * 8;   // 16-byte chunks of a key's row
+          const int ch = lane % kCh;
+          uint8_t* col = vst + (ch / 8) * S::kHS + (ch % 8) * 16;
+          for (int key = last_nkeys + lane / kCh; key < kNK; key += 32 / kCh)
+            *reinterpret_cast<uint4*>(col + (key / 8) * S::kGS + (key % 8) * 128) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
           __syncwarp();
         }
@@ -773,12 +773,25 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
     const float sl2 = F8 ? a.scale_log2 * a.pool.k_scale : a.scale_log2;
     uint32_t sc = 0;   // S phases of the tile waited so far
     uint32_t pvc = 0;  // its items with key tiles so far (kPv phases)
-    bool ok = true;
-    for (int r = 0; ok; ++r) {
-      int w = n_items;
-      if (!(ok = take_item(r, w))) break;
-      if (w >= n_items) break;
-      const TcItem iv = tc_item(items, w, G);
+    // The next item (its index, descriptor and this row's query position) is
+    // read before the current item's epilogue: its global loads then overlap
+    // the epilogue instead of delaying the next item's first softmax step.
+    // The K producer claims it once it has issued the current item's last K
+    // tile, which the S MMAs of the steps already softmaxed have consumed.
+    TcItem nv{};
+    int nqpos = -1;
+    auto fetch = [&](int wi) {
+      if (wi >= n_items) return;
+      nv = tc_item(items, wi, G);
+      const int nr = X ? nv.rows1 : nv.rows0;
+      nqpos = row < nr ? __ldg(a.q_positions + (X ? nv.tok01 : nv.tok00) + row / G) : -1;
+    };
+    int w = n_items;
+    bool ok = take_item(0, w);
+    if (ok) fetch(w);
+    for (int r = 0; ok && w < n_items; ++r) {
+      const TcItem iv = nv;
+      const int qpos = nqpos;
       const WorkItem& it = iv.it;
       const int g = it.kv_head;
       const int nrows = X ? iv.rows1 : iv.rows0;
@@ -787,8 +800,6 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
       const int kv_end = iv.kv_end;
       const int rows0 = iv.rows0;
       auto tok0_of = [&](int t) { return t ? iv.tok01 : iv.tok00; };
-      int qpos = -1;
-      if (row < nrows) qpos = __ldg(a.q_positions + tok0_of(X) + row / G);
       float m = -CUDART_INF_F, l = 0.f;
       if constexpr (F8) {
         // The widened K and V are f16, and both operands of an MMA share one
@@ -884,6 +895,8 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           tc_fence_before();
         mbar_arrive(&bars[B::kP + X]);
       }
+      int wn = n_items;
+      if (ok && (ok = take_item(r + 1, wn))) fetch(wn);
       if (ok && nt > 0) {
         if (!(ok = mbar_wait_warp(&bars[B::kPv + X], pvc & 1, s_abort, a.wait_ns))) break;
         ++pvc;
@@ -923,8 +936,14 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
                 w0.z = pack_bf16x2(o[4] * inv, o[5] * inv);   w0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
                 w1.x = pack_bf16x2(o[8] * inv, o[9] * inv);   w1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
                 w1.z = pack_bf16x2(o[12] * inv, o[13] * inv); w1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-                dst_o[(c0 + c) / 8] = w0;
-                dst_o[(c0 + c) / 8 + 1] = w1;
+                // A thread writes its own row: one 32-byte store a sector
+                // (half the requests of two 16-byte stores) where o allows it.
+                if (a.o_align32) {
+                  st_global_v8(dst_o + (c0 + c) / 8, w0, w1);
+                } else {
+                  dst_o[(c0 + c) / 8] = w0;
+                  dst_o[(c0 + c) / 8 + 1] = w1;
+                }
               } else {
 #pragma unroll
                 for (int e = 0; e < 16; e += 4)
@@ -941,6 +960,7 @@ tc_attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmap_k, con
           }
         }
       }
+      w = wn;
     }
 
     if (!ok) {

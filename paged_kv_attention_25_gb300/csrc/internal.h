@@ -155,6 +155,7 @@ struct AttnArgs {
   const int32_t* ctx_lens;
   float scale_log2;      // scale * log2(e)
   void* o;
+  int o_align32;         // o is 32-byte aligned: output rows take 32-byte stores
   float* lse;
   float* part_o;         // [num_partial_rows][head_dim]
   float* part_lse;       // [num_partial_rows]

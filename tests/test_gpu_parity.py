@@ -235,6 +235,26 @@ def test_nan_in_slots_past_the_context_does_not_leak(G):
     assert_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O, L, batch.name)
 
 
+def test_output_16_byte_aligned_matches_32_byte_aligned():
+    """The tensor-core epilogue stores 32 bytes a row at a time when the output is 32-byte aligned,
+    else 16; an output 16 bytes past a 32-byte boundary must get the same bits."""
+    batch = wl.random_small(31, num_q_heads=8, num_kv_heads=2, head_dim=128, max_ctx=900, max_q=300)
+    run, o1, l1 = full_parity(batch)
+    assert pkv.pkv_plan_inspect(batch.num_q_heads, batch.num_kv_heads, batch.head_dim, 148, run.meta)[1][
+        "num_tc_items"] > 0
+    T, Hq, D = o1.shape
+    flat = torch.full((T * Hq * D + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = flat[8:].view(T, Hq, D)
+    assert out.data_ptr() % 32 == 16
+    d = run.d
+    o2, l2 = pkv.pkv_paged_attn(run.pool, d["q"], d["q_positions"], d["block_tables"], d["ctx_lens"],
+                                d["cu_q_lens"], run.meta, batch.scale, out=out)
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_errors(run.pool) == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.isnan(flat[:8].float()).all()   # nothing written before the output
+
+
 def test_zero_tokens_is_a_no_op():
     batch = wl.tiny_mixed(1)
     run = GpuRun(batch)
