@@ -14,9 +14,12 @@ namespace pkv {
 namespace {
 
 // Each thread moves kUnroll 16-byte chunks per round (all loads, then all
-// stores) so that enough requests are in flight to cover the link's latency.
+// stores): 64 KB a CTA in flight, which covers HBM latency while the
+// attention kernels load HBM beside a swap (4 chunks a thread measured about
+// half the link rate there).  A round past a block's end is predicated rather
+// than finished one dependent chunk at a time.
 constexpr int kSwapThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 16;
 // CTAs of 256 threads that saturate the CPU-GPU link on GB300 (measured):
 // writes to host memory reach about 187 GB/s with 8, reads from it about
 // 199 GB/s with 24.  More CTAs only take SMs from the attention kernels that
@@ -35,24 +38,16 @@ __global__ void __launch_bounds__(kSwapThreads) swap_kernel(uint4* __restrict__ 
     for (int kv = 0; kv < 2; ++kv) {
       uint4* p = (kv ? vpool : kpool) + pool_off;
       uint4* h = host + (2 * static_cast<int64_t>(b) + kv) * blk_chunks;
-      int c = threadIdx.x;
-      for (; c + (kUnroll - 1) * kSwapThreads < blk_chunks; c += kUnroll * kSwapThreads) {
+      const uint4* src = to_host ? p : h;
+      uint4* dst = to_host ? h : p;
+      for (int c0 = threadIdx.x; c0 < blk_chunks; c0 += kUnroll * kSwapThreads) {
         uint4 v[kUnroll];
-        if (to_host) {
 #pragma unroll
-          for (int u = 0; u < kUnroll; ++u) v[u] = p[c + u * kSwapThreads];
+        for (int u = 0; u < kUnroll; ++u)
+          if (c0 + u * kSwapThreads < blk_chunks) v[u] = src[c0 + u * kSwapThreads];
 #pragma unroll
-          for (int u = 0; u < kUnroll; ++u) h[c + u * kSwapThreads] = v[u];
-        } else {
-#pragma unroll
-          for (int u = 0; u < kUnroll; ++u) v[u] = h[c + u * kSwapThreads];
-#pragma unroll
-          for (int u = 0; u < kUnroll; ++u) p[c + u * kSwapThreads] = v[u];
-        }
-      }
-      for (; c < blk_chunks; c += kSwapThreads) {
-        if (to_host) h[c] = p[c];
-        else p[c] = h[c];
+        for (int u = 0; u < kUnroll; ++u)
+          if (c0 + u * kSwapThreads < blk_chunks) dst[c0 + u * kSwapThreads] = v[u];
       }
     }
   }
