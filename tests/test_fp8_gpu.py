@@ -133,6 +133,10 @@ def test_fp8_swap_bit_exact():
                             num_kv_heads=2, head_dim=128, seed=74), 2.0 ** -12, 2.0 ** 10),
     (lambda: wl.random_small(75, num_q_heads=10, num_kv_heads=2, head_dim=128, max_ctx=900, max_q=60),
      2.0 ** -6, 2.0 ** -6),
+    # The other way round: subnormal K codes (the widened tiles then hold f16 subnormals) and
+    # saturating V codes.
+    (lambda: wl.build_batch("fp8_extreme_k", [wl._new_turn(0, n) for n in (45, 129, 260, 3)], num_q_heads=8,
+                            num_kv_heads=2, head_dim=128, seed=76), 2.0 ** 10, 2.0 ** -12),
 ])
 def test_fp8_tensor_core_attention_matches_oracle(maker, ks, vs):
     check_attention(maker(), ks, vs, want_tc=True)
