@@ -9,6 +9,18 @@
 
 namespace pkv {
 
+// The fp32 quotient x / scale, correctly rounded.  For a scale that is a
+// power of two with a normal reciprocal, x times that reciprocal rounds the
+// same real number and is the same float (overflow and subnormal results
+// included), without a division; any other scale divides.  The test is the
+// same for every thread (one scale per pool).
+__device__ __forceinline__ float quant_div(float x, float scale) {
+  const uint32_t sb = __float_as_uint(scale);   // scale > 0
+  const uint32_t e = sb >> 23;
+  if ((sb & 0x7fffffu) == 0 && e >= 1u && e <= 253u) return x * __uint_as_float((254u - e) << 23);
+  return __fdiv_rn(x, scale);
+}
+
 // Four bf16 (two packed words, lowest element in the low half) -> four e4m3
 // codes, lowest element in the lowest byte: the code nearest (ties to even)
 // to the fp32 quotient x / scale, finite values beyond 448 saturating (the
@@ -16,9 +28,9 @@ namespace pkv {
 __device__ __forceinline__ uint32_t quant_e4m3x4(uint32_t w0, uint32_t w1, float scale) {
   const float x0 = __uint_as_float(w0 << 16), x1 = __uint_as_float(w0 & 0xffff0000u);
   const float x2 = __uint_as_float(w1 << 16), x3 = __uint_as_float(w1 & 0xffff0000u);
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale)), __NV_SATFINITE,
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(quant_div(x0, scale), quant_div(x1, scale)), __NV_SATFINITE,
                                                __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(x2, scale), __fdiv_rn(x3, scale)), __NV_SATFINITE,
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(quant_div(x2, scale), quant_div(x3, scale)), __NV_SATFINITE,
                                                __NV_E4M3);
   return lo | (hi << 16);
 }
@@ -26,7 +38,8 @@ __device__ __forceinline__ uint32_t quant_e4m3x4(uint32_t w0, uint32_t w1, float
 // Two bf16 (one packed word) -> two e4m3 codes (lowest element in the low byte).
 __device__ __forceinline__ uint32_t quant_e4m3x2(uint32_t w, float scale) {
   const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xffff0000u);
-  return __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale)), __NV_SATFINITE, __NV_E4M3);
+  return __nv_cvt_float2_to_fp8x2(make_float2(quant_div(x0, scale), quant_div(x1, scale)), __NV_SATFINITE,
+                                  __NV_E4M3);
 }
 
 // Stores one chunk (8 bf16 of K and of V) at chunk index dst of the pool.
