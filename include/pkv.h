@@ -75,11 +75,13 @@ extern "C" {
  * is e4m3(c) * k_scale (or v_scale).  pkv_append quantises each new bf16
  * element x to the code nearest (ties to even) to the fp32 quotient x / scale,
  * finite values beyond 448 saturating to +-448.  Attention reads the codes
- * (half the bytes of bf16): the split-KV kernel multiplies them with bf16 q
- * in fp32; the tensor-core kernel widens each K/V tile to f16 in shared
- * memory (exact) and runs its MMAs with f16 operands, Q converted from bf16
- * to f16 (exact for |q| within f16's range, below 65504) and P rounded to
- * f16.  Q, O and the new K/V given to pkv_append stay bf16. */
+ * (half the bytes of bf16) and widens them to f16 (exact): the split-KV
+ * kernel takes the dot products with q converted to f16 and fp32
+ * accumulation (for one-row items on the warp-level MMA); the tensor-core
+ * kernel widens each K/V tile in shared memory and runs its MMAs with f16
+ * operands, P rounded to f16.  Q is converted from bf16 to f16 (exact for
+ * |q| within f16's range, below 65504).  Q, O and the new K/V given to
+ * pkv_append stay bf16. */
 #define PKV_DTYPE_FP8_E4M3 1
 
 /* Bits of the device error word (pkv_check_device_errors). */
