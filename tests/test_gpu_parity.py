@@ -103,6 +103,36 @@ def test_append_bit_exact_whole_pool(maker):
     assert np.array_equal(to_np_bits(run.pool.v), vp)
 
 
+def test_append_more_requests_than_staged_offsets():
+    """2,100 requests: the append's request search then reads cu_q_lens from global memory rather
+    than from its shared-memory copy (which holds up to 2,048 entries); empty requests among them
+    share offsets with their neighbours.  The pool must still match the oracle bit for bit."""
+    rng = np.random.default_rng(61)
+    reqs = []
+    for i in range(2100):
+        if i % 97 == 5:
+            reqs.append(wl.RequestSpec(ctx=int(rng.integers(1, 40)), q_positions=np.zeros(0, np.int32)))
+        elif i % 5 == 0:
+            reqs.append(wl._new_turn(int(rng.integers(0, 30)), int(rng.integers(1, 20))))
+        else:
+            reqs.append(wl._decode(int(rng.integers(0, 60))))
+    batch = wl.build_batch("many_requests", reqs, num_q_heads=4, num_kv_heads=2, head_dim=64, seed=61)
+    assert batch.num_reqs + 1 > 2048
+    run = GpuRun(batch)
+    run.append()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_errors(run.pool) == 0
+    kp, vp = oracle_pools(batch)
+    assert np.array_equal(to_np_bits(run.pool.k), kp)
+    assert np.array_equal(to_np_bits(run.pool.v), vp)
+    o, lse = run.attn()
+    torch.cuda.synchronize()
+    assert pkv.pkv_check_device_errors(run.pool) == 0
+    O, L = oracle.paged_attn(batch.q, kp, vp, batch.block_tables, batch.ctx_lens, batch.cu_q_lens,
+                             batch.q_positions, batch.scale)
+    assert_close(bf16_to_f64(o), lse.cpu().numpy().astype(np.float64), O, L, batch.name)
+
+
 def test_append_full_size_gqa_workload():
     batch = wl.llama70b_gqa()
     run = GpuRun(batch)
