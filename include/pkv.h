@@ -420,10 +420,15 @@ int pkv_check_device_errors(pkv_pool* pool, void* stream, unsigned* flags);
  *     (tensor-core) kernel never issues its first K copy, so that the wait for
  *     it runs out: the kernel records PKV_DEVERR_TIMEOUT, drains its copies,
  *     frees what it holds and returns, and that call's outputs are undefined;
- *     0 = off (default).
+ *     0 = off (default);
+ *   PKV_DEBUG_FUSED_FORM: how pkv_append_paged_attn appends: 0 = chosen per
+ *     batch (default), 1 = inside the attention launches whenever the pool
+ *     allows it, 2 = the append kernel first.  Every form gives the same pool
+ *     and the same O and LSE bits.
  * Errors: PKV_EINVAL for an unknown setting or a value out of range. */
 #define PKV_DEBUG_WAIT_LIMIT_NS 1
 #define PKV_DEBUG_WITHHOLD_COPY 2
+#define PKV_DEBUG_FUSED_FORM 3
 int pkv_debug_set(pkv_pool* pool, int what, int64_t value);
 
 /* Kernel timing with CUDA events recorded around every launch on the launch

@@ -121,6 +121,7 @@ struct pkv_pool {
   // Test and diagnostic settings (pkv_debug_set).
   uint64_t wait_ns = 1000000000ull;   // limit of every bounded wait in the kernels
   int withhold = 0;                   // see AttnArgs::withhold
+  int fused_form = 0;                 // PKV_DEBUG_FUSED_FORM
 
   // profiling (prof_mode 2: the two attention kernels run one after the other)
   bool prof_on = false;
@@ -640,7 +641,21 @@ int pkv::paged_attn_call(pkv_pool* pool, const AttnCall& c) {
   // so that the codes match the pool's) on its producer warp: measured about
   // seven times the attention's time on recompute-heavy batches.  The result
   // is the same either way.
-  const bool append_first = fused && pool->elem_bytes == 1 && !pl.tc.empty();
+  //
+  // Any other fused call appends inside the split-KV launch (CTAs after its
+  // work items) only when split-KV work dominates the batch.  Those CTAs take
+  // about twice the stand-alone append kernel's time, which the split-KV
+  // launch's own tail hides when its KV bytes are at least three times the
+  // tensor-core kernel's; otherwise they hold SMs the tensor-core CTAs wait
+  // for (measured: 13B mix 0.203 fused against 0.199 ms appending first, 70B
+  // mix 0.564 against 0.561; decode 1.253 against 1.278 and long context
+  // 0.338 against 0.344 the other way).  Either way the pool and the outputs
+  // are the same bits.
+  const bool in_kernel_ok = !(pool->elem_bytes == 1 && !pl.tc.empty());
+  const bool in_kernel_pays =
+      pl.tc.empty() || pl.stats.decode_kv_bytes >= 3 * pl.stats.tc_kv_bytes;
+  const bool append_first =
+      fused && (!in_kernel_ok || pool->fused_form == 2 || (pool->fused_form == 0 && !in_kernel_pays));
   const bool in_kernel = fused && !append_first;
   if (append_first) {
     PoolView pv = pool->view();
@@ -969,6 +984,10 @@ int pkv_debug_set(pkv_pool* pool, int what, int64_t value) {
     case PKV_DEBUG_WITHHOLD_COPY:
       if (value < 0 || value > 2) return fail(PKV_EINVAL, "withhold must be 0, 1 or 2");
       pool->withhold = static_cast<int>(value);
+      return PKV_OK;
+    case PKV_DEBUG_FUSED_FORM:
+      if (value < 0 || value > 2) return fail(PKV_EINVAL, "fused form must be 0, 1 or 2");
+      pool->fused_form = static_cast<int>(value);
       return PKV_OK;
     default:
       return fail(PKV_EINVAL, "unknown debug setting");

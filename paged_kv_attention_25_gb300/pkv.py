@@ -34,6 +34,7 @@ PKV_DEVERR_TIMEOUT = 4
 PKV_DEVERR_INTERNAL = 8
 PKV_DEBUG_WAIT_LIMIT_NS = 1
 PKV_DEBUG_WITHHOLD_COPY = 2
+PKV_DEBUG_FUSED_FORM = 3
 
 KERNELS = ("append", "split_kv", "tensor_core", "merge", "swap")
 
@@ -524,7 +525,8 @@ def pkv_profile_enable(pool: Pool, on=True):
 
 
 def pkv_debug_set(pool: Pool, what: int, value: int):
-    """Test settings: PKV_DEBUG_WAIT_LIMIT_NS (bounded-wait limit) or PKV_DEBUG_WITHHOLD_COPY (0, 1, 2)."""
+    """Test settings: PKV_DEBUG_WAIT_LIMIT_NS (bounded-wait limit), PKV_DEBUG_WITHHOLD_COPY (0, 1, 2) or
+    PKV_DEBUG_FUSED_FORM (0 per batch, 1 in-kernel append, 2 append first)."""
     _check(load_library().pkv_debug_set(pool.handle, int(what), int(value)))
 
 

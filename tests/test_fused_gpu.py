@@ -75,8 +75,10 @@ def oracle_after(b, fp8):
     return kp, vp, O, L
 
 
-def run_both(b, fp8=False, poison=True):
-    """(fused O, LSE, pool K, pool V) and (unfused O, LSE) on fresh pools holding the same history."""
+def run_both(b, fp8=False, poison=True, form=1):
+    """(fused O, LSE, pool K, pool V) and (unfused O, LSE) on fresh pools holding the same history.
+    form: PKV_DEBUG_FUSED_FORM of the fused call's pool (1, in-kernel append wherever the pool allows
+    it, unless a test asks for the per-batch choice (0) or append-first (2))."""
     d = wl.upload(b)
     meta = pkv.HostMeta(b.cu_q_lens, b.ctx_lens, b.q_positions)
     ref_pool = make_pool(b, fp8)
@@ -86,6 +88,7 @@ def run_both(b, fp8=False, poison=True):
     torch.cuda.synchronize()
     assert pkv.pkv_check_device_errors(ref_pool) == 0
     pool = make_pool(b, fp8)
+    pkv.pkv_debug_set(pool, pkv.PKV_DEBUG_FUSED_FORM, form)
     if poison:
         poison_new_slots(b, pool)
     torch.cuda.synchronize()
@@ -97,8 +100,8 @@ def run_both(b, fp8=False, poison=True):
     return (o, lse, pool), (o_ref, l_ref), st
 
 
-def check(b, fp8=False, poison=True, need_tc=None):
-    (o, lse, pool), (o_ref, l_ref), st = run_both(b, fp8, poison)
+def check(b, fp8=False, poison=True, need_tc=None, form=1):
+    (o, lse, pool), (o_ref, l_ref), st = run_both(b, fp8, poison, form)
     if need_tc is not None:
         assert (st["num_tc_items"] > 0) == need_tc
     kp, vp, O, L = oracle_after(b, fp8)
@@ -168,6 +171,27 @@ def test_fused_fp8_decode_regime(maker):
                                                            max_ctx=700, max_q=50)])
 def test_fused_fp8_tensor_core(maker):
     check(maker(), fp8=True, need_tc=True)
+
+
+@pytest.mark.parametrize("form", [0, 2])
+@pytest.mark.parametrize("maker", [
+    lambda: wl.random_small(4, num_q_heads=16, num_kv_heads=2, head_dim=128, max_ctx=2000, max_q=300),
+    lambda: wl.random_small(5, num_q_heads=2, num_kv_heads=2, head_dim=128, num_reqs=12, max_ctx=5000, max_q=200),
+    lambda: wl.decode_small(61, num_q_heads=4, num_kv_heads=4, head_dim=128),
+])
+def test_fused_other_forms_same_bits(maker, form):
+    """The per-batch choice (0) and append-first (2) give the oracle's pool and the unfused outputs,
+    bit for bit, as the in-kernel append does."""
+    check(maker(), form=form)
+
+
+def test_fused_form_setting_range():
+    b = wl.tiny_mixed(1)
+    pool = make_pool(b, False)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_debug_set(pool, pkv.PKV_DEBUG_FUSED_FORM, 3)
+    assert e.value.code == pkv.PKV_EINVAL
+    pool.close()
 
 
 def test_fused_needs_host_positions():
